@@ -1,0 +1,125 @@
+/*
+ * kda.h -- C ABI of the KDA (Kimi Delta Attention) kernels for GB300 (sm_103a).
+ *
+ * KDA is a gated delta-rule linear attention with a per-channel gate.  Per
+ * head it keeps a fixed-size state S (dk x dv, fp32) and, for every token t:
+ *
+ *     S   = Diag(exp(g_t)) S                decay first, one rate per channel
+ *     S   = S + beta_t k_t (v_t - S^T k_t)^T   write the delta along k_t
+ *     o_t = S^T q_t                          read out with the new state
+ *
+ * Sources: the delta rule and the decay-then-write order are in the lineage
+ * essay "Baseten 엔지니어가 분석한 7년간의 어텐션 메커니즘 진화: GPT-2부터
+ * Kimi K3까지", sections "DeltaNet: 이제 메모리를 편집할 수 있습니다" and
+ * "Gated DeltaNet: 이제는 '망각'할 수 있습니다"; the per-channel gate in its
+ * section "KDA: Kimi의 비법" and in "KV 캐시를 75% 줄였는데 성능은 더
+ * 좋아졌다", section "KDA: 지우고 다시 쓰는 메모, 채널마다 다른 망각률".
+ * The chunked form of prefill follows the essay's section "병렬화 트릭"
+ * (chunks of C = 64 tokens, masked attention inside a chunk, the state
+ * carried between chunks, a Householder/UT reparameterisation resolving all
+ * deltas of a chunk at once).
+ *
+ * Conventions for every entry point
+ *   - All tensors are dense, row-major, contiguous, in DEVICE memory owned by
+ *     the caller.  Base pointers must be 16-byte aligned.  The library never
+ *     allocates, frees or retains caller memory and keeps no per-call state.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
+ *     the legacy default stream).  Outputs are valid once the stream reaches
+ *     that point.
+ *   - Arguments are validated on the host before any launch, without reading
+ *     device memory.  A rejected call launches nothing and returns
+ *     KDA_ERR_INVALID_ARG (malformed) or KDA_ERR_UNSUPPORTED (well formed but
+ *     outside the compiled shapes).  A failed launch returns KDA_ERR_CUDA; the
+ *     CUDA error is cleared with cudaGetLastError so that it does not leak
+ *     into the caller's later checks.  No C++ exception or abort crosses the
+ *     ABI.
+ *   - Gates g are the log of the per-channel forgetting rate alpha in (0, 1]:
+ *     finite values <= 0.  beta is the write strength in [0, 1].
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,  /* null pointer, misalignment, bad size       */
+    KDA_ERR_UNSUPPORTED = 2,  /* head size / chunk / dtype not compiled in   */
+    KDA_ERR_CUDA = 3,         /* a CUDA launch or attribute call failed      */
+    KDA_ERR_TIMEOUT = 4       /* reserved: a bounded device wait gave up     */
+} kda_status;
+
+typedef enum kda_dtype {
+    KDA_BF16 = 0,             /* q, k, v and o are bfloat16                  */
+    KDA_FP32 = 1              /* q, k, v and o are float32                   */
+} kda_dtype;
+
+/*
+ * kda_prefill_chunked -- chunked prefill over a packed batch of N sequences.
+ *
+ *   q, k       [T_total, H, dk]   dtype        queries, keys
+ *   v          [T_total, H, dv]   dtype        values
+ *   g          [T_total, H, dk]   float32      log-gate, finite, <= 0
+ *   beta       [T_total, H]       float32      write strength
+ *   S0         [N, H, dk, dv]     float32      initial states, or NULL (zeros)
+ *   cu_seqlens [N + 1]            int32        sequence offsets: cu[0] = 0,
+ *                                              non-decreasing, cu[N] = T_total
+ *   o          [T_total, H, dv]   dtype        outputs (written)
+ *   S_T        [N, H, dk, dv]     float32      final states (written); may be
+ *                                              the same buffer as S0
+ *   dk, dv     64 or 128, dk == dv
+ *   chunk      64 (tokens per chunk); chunks never cross sequences and a
+ *              partial last chunk is handled as if padded with no-op tokens
+ *   dtype      KDA_BF16 or KDA_FP32
+ *
+ * Sequence n covers tokens [cu[n], cu[n+1]).  A sequence of length 0 copies
+ * its S0 (or zeros) to S_T.  cu_seqlens lives in device memory and is not
+ * read on the host; the kernels clamp every offset into [0, T_total], so
+ * inconsistent offsets can only shorten sequences, never cause an
+ * out-of-bounds access.  N = 0 with T_total = 0 is a valid no-op.
+ */
+kda_status kda_prefill_chunked(const void *q, const void *k, const void *v,
+                               const float *g, const float *beta,
+                               const float *S0, const int32_t *cu_seqlens,
+                               int32_t N, int64_t T_total, int32_t H,
+                               int32_t dk, int32_t dv, int32_t dtype,
+                               int32_t chunk, void *o, float *S_T,
+                               void *stream);
+
+/*
+ * kda_decode_step -- one token for each of B independent sequences; the
+ * states are updated in place.
+ *
+ *   q, k       [B, H, dk]         dtype
+ *   v          [B, H, dv]         dtype
+ *   g          [B, H, dk]         float32      log-gate, finite, <= 0
+ *   beta       [B, H]             float32
+ *   S          [B, H, dk, dv]     float32      read, then overwritten with S'
+ *   o          [B, H, dv]         dtype        outputs (written)
+ *   dk, dv     64 or 128, dk == dv
+ *
+ * The essay's section "KV 캐시: 재계산하지 말고 저장하라" notes that decode
+ * is bound by memory bandwidth, not arithmetic: this kernel streams each
+ * state from HBM once and writes it back once.  B = 0 is a valid no-op.
+ * S must not overlap any input or output.
+ */
+kda_status kda_decode_step(const void *q, const void *k, const void *v,
+                           const float *g, const float *beta, float *S,
+                           int32_t B, int32_t H, int32_t dk, int32_t dv,
+                           int32_t dtype, void *o, void *stream);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char *kda_status_string(int32_t status);
+
+/* ABI version of this library: (major << 16) | minor. */
+int32_t kda_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,0 +1,160 @@
+"""ctypes binding of ``libkda.so`` over torch tensors (marshalling only).
+
+Every step of the computation runs in the CUDA kernels behind the C ABI in
+``include/kda.h``; this module only checks tensor placement, dtype and shape,
+allocates outputs that the caller did not provide, and passes raw device
+pointers plus the current CUDA stream.  If the compiled library is missing,
+loading fails with an error -- there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libkda.so")
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_CUDA = 3
+KDA_ERR_TIMEOUT = 4
+KDA_BF16 = 0
+KDA_FP32 = 1
+
+_DTYPE_CODE = {torch.bfloat16: KDA_BF16, torch.float32: KDA_FP32}
+_lock = threading.Lock()
+_lib = None
+
+
+class KdaError(RuntimeError):
+    """A KDA entry point returned a non-OK status."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = int(status)
+        super().__init__("%s failed: %s" % (fn, status_string(status)))
+
+
+def load() -> ctypes.CDLL:
+    """Load ``libkda.so`` (built by ``serving_kda_chunked_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                "libkda.so is not built (%s); build it with "
+                "`python -m serving_kda_chunked_gb300.build`" % LIB_PATH)
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        lib.kda_prefill_chunked.argtypes = [
+            vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, i32,
+            vp, vp, vp]
+        lib.kda_prefill_chunked.restype = ctypes.c_int
+        lib.kda_decode_step.argtypes = [
+            vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]
+        lib.kda_decode_step.restype = ctypes.c_int
+        lib.kda_status_string.argtypes = [i32]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_abi_version.argtypes = []
+        lib.kda_abi_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def abi_version() -> int:
+    return int(load().kda_abi_version())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream))
+
+
+def _check_cuda(name, t, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor (the KDA kernels run on the GPU only)" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, S0=None, *, chunk: int = 64,
+                        o=None, S_T=None, stream=None):
+    """Chunked KDA prefill over a packed batch (``kda_prefill_chunked`` in kda.h).
+
+    q, k [T, H, dk] and v [T, H, dv] in bf16 or fp32 (all the same); g
+    [T, H, dk] fp32 log-gates; beta [T, H] fp32; cu_seqlens [N+1] int32 on the
+    device; S0 [N, H, dk, dv] fp32 or None.  Returns (o, S_T); pass ``o`` /
+    ``S_T`` to write into existing buffers (``S_T`` may be ``S0``).
+    """
+    _check_cuda("q", q)
+    if q.dtype not in _DTYPE_CODE:
+        raise ValueError("q must be bfloat16 or float32")
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    _check_cuda("k", k, q.dtype, (T, H, dk))
+    _check_cuda("v", v, q.dtype, (T, H, dv))
+    _check_cuda("g", g, torch.float32, (T, H, dk))
+    _check_cuda("beta", beta, torch.float32, (T, H))
+    _check_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    N = cu_seqlens.shape[0] - 1
+    if S0 is not None:
+        _check_cuda("S0", S0, torch.float32, (N, H, dk, dv))
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
+    _check_cuda("o", o, q.dtype, (T, H, dv))
+    if S_T is None:
+        S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    _check_cuda("S_T", S_T, torch.float32, (N, H, dk, dv))
+    st = load().kda_prefill_chunked(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
+        N, T, H, dk, dv, _DTYPE_CODE[q.dtype], int(chunk), _ptr(o), _ptr(S_T),
+        _stream(stream))
+    if st != KDA_OK:
+        raise KdaError("kda_prefill_chunked", st)
+    return o, S_T
+
+
+def kda_decode_step(q, k, v, g, beta, S, *, o=None, stream=None):
+    """One batched KDA decode step (``kda_decode_step`` in kda.h).
+
+    q, k [B, H, dk], v [B, H, dv] (bf16 or fp32); g [B, H, dk] fp32; beta
+    [B, H] fp32; S [B, H, dk, dv] fp32, updated in place.  Returns o.
+    """
+    _check_cuda("q", q)
+    if q.dtype not in _DTYPE_CODE:
+        raise ValueError("q must be bfloat16 or float32")
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    _check_cuda("k", k, q.dtype, (B, H, dk))
+    _check_cuda("v", v, q.dtype, (B, H, dv))
+    _check_cuda("g", g, torch.float32, (B, H, dk))
+    _check_cuda("beta", beta, torch.float32, (B, H))
+    _check_cuda("S", S, torch.float32, (B, H, dk, dv))
+    if o is None:
+        o = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
+    _check_cuda("o", o, q.dtype, (B, H, dv))
+    st = load().kda_decode_step(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S), B, H, dk, dv,
+        _DTYPE_CODE[q.dtype], _ptr(o), _stream(stream))
+    if st != KDA_OK:
+        raise KdaError("kda_decode_step", st)
+    return o

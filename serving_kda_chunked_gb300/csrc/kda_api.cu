@@ -1,0 +1,83 @@
+// kda_api.cu -- the C ABI: host-side validation and dispatch (see kda.h).
+#include "../../include/kda.h"
+#include "kda_internal.cuh"
+
+namespace {
+
+inline bool aligned16(const void *p) { return p == nullptr || ((uintptr_t)p & 15u) == 0; }
+inline bool aligned4(const void *p) { return p == nullptr || ((uintptr_t)p & 3u) == 0; }
+inline bool head_ok(int32_t dk, int32_t dv) { return dk == dv && (dk == 64 || dk == 128); }
+
+kda_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return KDA_OK;
+    (void)cudaGetLastError();  // clear a sticky launch error for the caller
+    return KDA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_prefill_chunked(const void *q, const void *k, const void *v,
+                               const float *g, const float *beta,
+                               const float *S0, const int32_t *cu_seqlens,
+                               int32_t N, int64_t T_total, int32_t H,
+                               int32_t dk, int32_t dv, int32_t dtype,
+                               int32_t chunk, void *o, float *S_T,
+                               void *stream) {
+    if (N < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
+    if (dk <= 0 || dv <= 0 || chunk <= 0) return KDA_ERR_INVALID_ARG;
+    if (!head_ok(dk, dv) || chunk != 64) return KDA_ERR_UNSUPPORTED;
+    if (N == 0) return T_total == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens || !S_T) return KDA_ERR_INVALID_ARG;
+    if (T_total > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) ||
+        !aligned16(o) || !aligned16(S0) || !aligned16(S_T) || !aligned4(beta) ||
+        !aligned4(cu_seqlens))
+        return KDA_ERR_INVALID_ARG;
+    if ((int64_t)N * H * (dv / 32) > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+
+    kda::PrefillArgs a;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S0 = S0;
+    a.cu_seqlens = cu_seqlens; a.o = o; a.S_T = S_T;
+    a.N = N; a.H = H; a.dk = dk; a.dv = dv; a.dtype = dtype; a.chunk = chunk;
+    a.T = T_total;
+    return cuda_status(kda::launch_prefill_simt(a, (cudaStream_t)stream));
+}
+
+kda_status kda_decode_step(const void *q, const void *k, const void *v,
+                           const float *g, const float *beta, float *S,
+                           int32_t B, int32_t H, int32_t dk, int32_t dv,
+                           int32_t dtype, void *o, void *stream) {
+    if (B < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
+    if (dk <= 0 || dv <= 0) return KDA_ERR_INVALID_ARG;
+    if (!head_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
+    if (B == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !S || !o) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) ||
+        !aligned16(S) || !aligned16(o) || !aligned4(beta))
+        return KDA_ERR_INVALID_ARG;
+    if ((int64_t)B * H > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+
+    kda::DecodeArgs a;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S = S; a.o = o;
+    a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.dtype = dtype;
+    return cuda_status(kda::launch_decode(a, (cudaStream_t)stream));
+}
+
+const char *kda_status_string(int32_t status) {
+    switch (status) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: shape, chunk or dtype not supported";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call failed";
+    case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded device wait gave up";
+    default: return "KDA_ERR_UNKNOWN: unknown status";
+    }
+}
+
+int32_t kda_abi_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

@@ -1,0 +1,77 @@
+// kda_internal.cuh -- shared declarations of the KDA CUDA library (internal).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+// Arguments of one prefill call after host validation.
+struct PrefillArgs {
+    const void *q, *k, *v;
+    const float *g, *beta, *S0;
+    const int32_t *cu_seqlens;
+    void *o;
+    float *S_T;
+    int32_t N, H, dk, dv, dtype, chunk;
+    int64_t T;
+};
+
+// Arguments of one decode call after host validation.
+struct DecodeArgs {
+    const void *q, *k, *v;
+    const float *g, *beta;
+    float *S;
+    void *o;
+    int32_t B, H, dk, dv, dtype;
+};
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t stream);
+
+// ---- element access helpers ------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Four consecutive elements starting at a 4-element-aligned index.
+__device__ __forceinline__ float4 load4(const float *p) {
+    return *reinterpret_cast<const float4 *>(p);
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
+    uint2 raw = *reinterpret_cast<const uint2 *>(p);
+    __nv_bfloat162 lo = *reinterpret_cast<__nv_bfloat162 *>(&raw.x);
+    __nv_bfloat162 hi = *reinterpret_cast<__nv_bfloat162 *>(&raw.y);
+    float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void store4(float *p, float4 x) {
+    *reinterpret_cast<float4 *>(p) = x;
+}
+__device__ __forceinline__ void store4(__nv_bfloat16 *p, float4 x) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
+    uint2 raw;
+    raw.x = *reinterpret_cast<uint32_t *>(&lo);
+    raw.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(p) = raw;
+}
+
+// Sequence bounds read from device offsets, clamped into [0, T] so that
+// inconsistent offsets never lead outside the token arrays.
+__device__ __forceinline__ void seq_bounds(const int32_t *cu, int n, int64_t T,
+                                           int64_t &bos, int64_t &eos) {
+    int64_t a = cu[n], b = cu[n + 1];
+    a = a < 0 ? 0 : (a > T ? T : a);
+    b = b < a ? a : (b > T ? T : b);
+    bos = a;
+    eos = b;
+}
+
+}  // namespace kda

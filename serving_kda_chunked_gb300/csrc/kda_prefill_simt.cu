@@ -1,0 +1,230 @@
+// kda_prefill_simt.cu -- chunked KDA prefill on CUDA cores, fp32 arithmetic.
+//
+// This is the fp32 path (fp32 q/k/v/o) and the arithmetic scaffold of the
+// tensor-core path: it runs the same chunked algebra with every product in
+// fp32 on CUDA cores.
+//
+// Chunking follows the lineage essay "GPT-2부터 Kimi K3까지", section
+// "병렬화 트릭": within a chunk of C = 64 tokens the deltas are resolved all
+// at once (a unit-lower-triangular solve, the UT form of the Householder
+// reparameterisation), and only the state crosses chunk boundaries.  For the
+// per-channel gate (section "KDA: Kimi의 비법") and a chunk entering with
+// state S, with gamma = per-channel cumulative log-gate inside the chunk:
+//
+//   A[r,i] = beta_r sum_c k_rc k_ic exp(gamma_rc - gamma_ic)   (i < r)
+//   P[r,i] =        sum_c q_rc k_ic exp(gamma_rc - gamma_ic)   (i <= r)
+//   (I + A) U = Diag(beta) (V - (K * exp(gamma)) S)
+//   O      = (Q * exp(gamma)) S + P U
+//   S_next = Diag(exp(gamma_last)) S + (K * exp(gamma_last - gamma))^T U
+//
+// Every exponent above is <= 0 (pairs with i <= r only), so nothing can
+// overflow.  Columns of S are independent, so one CTA owns one (sequence,
+// head, block of DVS state columns) and walks the sequence's chunks in order
+// with its state slice in shared memory.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int C = 64;      // tokens per chunk
+constexpr int NT = 256;    // threads per CTA
+
+template <int DK, int DVS>
+struct SimtSmem {
+    static constexpr int KP = DK + 1;  // padded row stride of [C][DK] tiles
+    static constexpr int CP = C + 1;   // padded row stride of [C][C] tiles
+    static constexpr size_t floats =
+        3 * (size_t)C * KP + 2 * (size_t)C * CP + (size_t)DK * DVS +
+        (size_t)C * DVS + C + 2 * DK;
+    static constexpr size_t bytes = floats * sizeof(float);
+};
+
+template <int DK, int DVS, typename Tin>
+__global__ void __launch_bounds__(NT, 1)
+prefill_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
+                    const Tin *__restrict__ v, const float *__restrict__ g,
+                    const float *__restrict__ beta, const float *S0,
+                    const int32_t *__restrict__ cu, Tin *__restrict__ o,
+                    float *S_T, int H, int64_t T, int n_slices) {
+    using Sm = SimtSmem<DK, DVS>;
+    constexpr int KP = Sm::KP, CP = Sm::CP;
+    constexpr int DV = DK;
+    extern __shared__ float smem[];
+    float *sK = smem;              // [C][KP]  k, then k * exp(gamma)
+    float *sQ = sK + C * KP;       // [C][KP]  q, then q * exp(gamma)
+    float *sG = sQ + C * KP;       // [C][KP]  g, then gamma, then kbar
+    float *sA = sG + C * KP;       // [C][CP]  A
+    float *sP = sA + C * CP;       // [C][CP]  P
+    float *sS = sP + C * CP;       // [DK][DVS] state slice
+    float *sV = sS + DK * DVS;     // [C][DVS] v, then rhs, then U
+    float *sB = sV + C * DVS;      // [C] beta
+    float *sGL = sB + C;           // [DK] gamma at the chunk's last row
+    float *sEL = sGL + DK;         // [DK] exp(gamma_last)
+
+    const int tid = threadIdx.x;
+    const int unit = blockIdx.x;
+    const int slice = unit % n_slices;
+    const int h = (unit / n_slices) % H;
+    const int n = unit / (n_slices * H);
+    const int col0 = slice * DVS;
+    int64_t bos, eos;
+    seq_bounds(cu, n, T, bos, eos);
+
+    const int64_t sbase = ((int64_t)n * H + h) * DK * DV;
+    for (int idx = tid; idx < DK * DVS; idx += NT) {
+        const int c = idx / DVS, j = idx % DVS;
+        sS[idx] = S0 ? S0[sbase + (int64_t)c * DV + col0 + j] : 0.f;
+    }
+
+    for (int64_t c0 = bos; c0 < eos; c0 += C) {
+        const int L = (int)((eos - c0) < C ? (eos - c0) : C);
+        // ---- stage the chunk; rows past the sequence end are no-op tokens
+        for (int idx = tid; idx < C * DK; idx += NT) {
+            const int r = idx / DK, c = idx % DK;
+            float kv = 0.f, qv = 0.f, gv = 0.f;
+            if (r < L) {
+                const int64_t off = ((c0 + r) * H + h) * DK + c;
+                kv = to_f32(k[off]);
+                qv = to_f32(q[off]);
+                gv = g[off];
+            }
+            sK[r * KP + c] = kv;
+            sQ[r * KP + c] = qv;
+            sG[r * KP + c] = gv;
+        }
+        for (int idx = tid; idx < C * DVS; idx += NT) {
+            const int r = idx / DVS, j = idx % DVS;
+            sV[idx] = r < L ? to_f32(v[((c0 + r) * H + h) * DV + col0 + j]) : 0.f;
+        }
+        for (int r = tid; r < C; r += NT)
+            sB[r] = r < L ? beta[(c0 + r) * H + h] : 0.f;
+        __syncthreads();
+
+        // ---- per-channel cumulative log-gate
+        if (tid < DK) {
+            float acc = 0.f;
+            for (int r = 0; r < C; ++r) {
+                acc += sG[r * KP + tid];
+                sG[r * KP + tid] = acc;
+            }
+            sGL[tid] = acc;
+            sEL[tid] = expf(acc);
+        }
+        __syncthreads();
+
+        // ---- gated K K^T (strictly lower, times beta_r) and Q K^T (lower)
+        for (int pidx = tid; pidx < C * C; pidx += NT) {
+            const int r = pidx / C, i = pidx % C;
+            float a = 0.f, p = 0.f;
+            if (i <= r) {
+                const float *gr = sG + r * KP, *gi = sG + i * KP;
+                const float *kr = sK + r * KP, *ki = sK + i * KP, *qr = sQ + r * KP;
+#pragma unroll 4
+                for (int c = 0; c < DK; ++c) {
+                    const float kie = ki[c] * expf(gr[c] - gi[c]);
+                    a += kr[c] * kie;
+                    p += qr[c] * kie;
+                }
+            }
+            sA[r * CP + i] = i < r ? sB[r] * a : 0.f;
+            sP[r * CP + i] = p;
+        }
+        __syncthreads();
+
+        // ---- K*exp(gamma), Q*exp(gamma), kbar = K*exp(gamma_last - gamma)
+        for (int idx = tid; idx < C * DK; idx += NT) {
+            const int r = idx / DK, c = idx % DK;
+            const float gam = sG[r * KP + c];
+            const float e = expf(gam);
+            const float kk = sK[r * KP + c];
+            sG[r * KP + c] = kk * expf(sGL[c] - gam);
+            sK[r * KP + c] = kk * e;
+            sQ[r * KP + c] *= e;
+        }
+        __syncthreads();
+
+        // ---- right-hand side: beta (V - (K*exp(gamma)) S)
+        for (int idx = tid; idx < C * DVS; idx += NT) {
+            const int r = idx / DVS, j = idx % DVS;
+            float acc = 0.f;
+            const float *kr = sK + r * KP;
+#pragma unroll 8
+            for (int c = 0; c < DK; ++c) acc += kr[c] * sS[c * DVS + j];
+            sV[idx] = sB[r] * (sV[idx] - acc);
+        }
+        __syncthreads();
+
+        // ---- forward substitution (I + A) U = rhs, one column per warp pass
+        {
+            const int warp = tid / 32, lane = tid % 32;
+            for (int j = warp; j < DVS; j += NT / 32) {
+                float x0 = sV[lane * DVS + j];
+                float x1 = sV[(lane + 32) * DVS + j];
+                for (int r = 0; r < C; ++r) {
+                    const float ur = __shfl_sync(0xffffffffu, r < 32 ? x0 : x1, r & 31);
+                    if (lane > r) x0 -= sA[lane * CP + r] * ur;
+                    if (lane + 32 > r) x1 -= sA[(lane + 32) * CP + r] * ur;
+                }
+                sV[lane * DVS + j] = x0;
+                sV[(lane + 32) * DVS + j] = x1;
+            }
+        }
+        __syncthreads();
+
+        // ---- outputs O = (Q*exp(gamma)) S + P U
+        for (int idx = tid; idx < C * DVS; idx += NT) {
+            const int r = idx / DVS, j = idx % DVS;
+            if (r >= L) continue;
+            float acc = 0.f;
+            const float *qr = sQ + r * KP;
+#pragma unroll 8
+            for (int c = 0; c < DK; ++c) acc += qr[c] * sS[c * DVS + j];
+            const float *pr = sP + r * CP;
+            for (int i = 0; i <= r; ++i) acc += pr[i] * sV[i * DVS + j];
+            o[((c0 + r) * H + h) * DV + col0 + j] = from_f32<Tin>(acc);
+        }
+        __syncthreads();
+
+        // ---- state carry S = Diag(exp(gamma_last)) S + kbar^T U
+        for (int idx = tid; idx < DK * DVS; idx += NT) {
+            const int c = idx / DVS, j = idx % DVS;
+            float acc = sEL[c] * sS[idx];
+#pragma unroll 8
+            for (int r = 0; r < C; ++r) acc += sG[r * KP + c] * sV[r * DVS + j];
+            sS[idx] = acc;
+        }
+        __syncthreads();
+    }
+
+    for (int idx = tid; idx < DK * DVS; idx += NT) {
+        const int c = idx / DVS, j = idx % DVS;
+        S_T[sbase + (int64_t)c * DV + col0 + j] = sS[idx];
+    }
+}
+
+template <int DK, int DVS, typename Tin>
+cudaError_t launch(const PrefillArgs &a, cudaStream_t st) {
+    using Sm = SimtSmem<DK, DVS>;
+    auto kern = prefill_simt_kernel<DK, DVS, Tin>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Sm::bytes);
+    if (e != cudaSuccess) return e;
+    const int n_slices = DK / DVS;
+    const int64_t units = (int64_t)a.N * a.H * n_slices;
+    kern<<<(unsigned)units, NT, Sm::bytes, st>>>(
+        (const Tin *)a.q, (const Tin *)a.k, (const Tin *)a.v, a.g, a.beta, a.S0,
+        a.cu_seqlens, (Tin *)a.o, a.S_T, a.H, a.T, n_slices);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t st) {
+    if ((int64_t)a.N * a.H == 0) return cudaSuccess;
+    const bool bf = a.dtype == 0;
+    if (a.dk == 128)
+        return bf ? launch<128, 32, __nv_bfloat16>(a, st) : launch<128, 32, float>(a, st);
+    return bf ? launch<64, 32, __nv_bfloat16>(a, st) : launch<64, 32, float>(a, st);
+}
+
+}  // namespace kda

@@ -1,0 +1,123 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load, export every function that ``include/*.h`` declares,
+and reject malformed or unsupported arguments on the host before touching the
+GPU.  Only argument combinations that are rejected (or are documented no-ops)
+are called here, so no CUDA work is issued.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import serving_kda_chunked_gb300 as kda
+from serving_kda_chunked_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kda.load()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(kda_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = _declared_functions()
+    for n in ("kda_prefill_chunked", "kda_decode_step", "kda_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), "libkda.so does not export %s" % name
+
+
+def test_status_strings(lib):
+    assert kda.status_string(kda.KDA_OK) == "KDA_OK"
+    assert "INVALID" in kda.status_string(kda.KDA_ERR_INVALID_ARG)
+    assert "UNSUPPORTED" in kda.status_string(kda.KDA_ERR_UNSUPPORTED)
+    assert "UNKNOWN" in kda.status_string(99)
+    assert kda.abi_version() >> 16 == 1
+
+
+P = 0x10000  # a 16-byte aligned stand-in address; never dereferenced here
+
+
+def _prefill(lib, **kw):
+    a = dict(q=P, k=P, v=P, g=P, beta=P, S0=None, cu=P, N=1, T=64, H=2, dk=128,
+             dv=128, dtype=0, chunk=64, o=P, S_T=P)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.kda_prefill_chunked(
+        vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]),
+        vp(a["S0"]), vp(a["cu"]), a["N"], a["T"], a["H"], a["dk"], a["dv"],
+        a["dtype"], a["chunk"], vp(a["o"]), vp(a["S_T"]), None)
+
+
+def _decode(lib, **kw):
+    a = dict(q=P, k=P, v=P, g=P, beta=P, S=P, B=4, H=2, dk=128, dv=128, dtype=0, o=P)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.kda_decode_step(
+        vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), vp(a["S"]),
+        a["B"], a["H"], a["dk"], a["dv"], a["dtype"], vp(a["o"]), None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(H=0), kda.KDA_ERR_INVALID_ARG),
+    (dict(N=-1), kda.KDA_ERR_INVALID_ARG),
+    (dict(T=-5), kda.KDA_ERR_INVALID_ARG),
+    (dict(dtype=7), kda.KDA_ERR_INVALID_ARG),
+    (dict(dk=96, dv=96), kda.KDA_ERR_UNSUPPORTED),
+    (dict(dk=128, dv=64), kda.KDA_ERR_UNSUPPORTED),
+    (dict(chunk=32), kda.KDA_ERR_UNSUPPORTED),
+    (dict(chunk=0), kda.KDA_ERR_INVALID_ARG),
+    (dict(q=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(g=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(o=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(cu=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(S_T=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(q=P + 2), kda.KDA_ERR_INVALID_ARG),
+    (dict(v=P + 8), kda.KDA_ERR_INVALID_ARG),
+    (dict(S0=P + 4), kda.KDA_ERR_INVALID_ARG),
+    (dict(beta=P + 1), kda.KDA_ERR_INVALID_ARG),
+    (dict(N=0, T=10), kda.KDA_ERR_INVALID_ARG),
+    (dict(N=0, T=0), kda.KDA_OK),                      # empty batch: no-op
+])
+def test_prefill_host_validation(lib, kw, expect):
+    assert _prefill(lib, **kw) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(H=0), kda.KDA_ERR_INVALID_ARG),
+    (dict(B=-1), kda.KDA_ERR_INVALID_ARG),
+    (dict(dtype=2), kda.KDA_ERR_INVALID_ARG),
+    (dict(dk=32, dv=32), kda.KDA_ERR_UNSUPPORTED),
+    (dict(S=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(beta=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(S=P + 4), kda.KDA_ERR_INVALID_ARG),
+    (dict(o=P + 2), kda.KDA_ERR_INVALID_ARG),
+    (dict(B=0), kda.KDA_OK),                           # empty batch: no-op
+])
+def test_decode_host_validation(lib, kw, expect):
+    assert _decode(lib, **kw) == expect
+
+
+def test_binding_rejects_host_tensors(lib):
+    import torch
+    q = torch.zeros(4, 2, 64)
+    with pytest.raises(ValueError, match="CUDA"):
+        kda.kda_decode_step(q, q, q, q, torch.zeros(4, 2), torch.zeros(4, 2, 64, 64))

@@ -1,0 +1,264 @@
+"""GPU parity: the CUDA kernels (through the C ABI) against the fp64 oracle.
+
+Inputs come from ``kda_inputs`` (seeded, drawn on the GPU), the oracle
+consumes exactly the stored values, and every output is compared with the
+metric in ``parity.py``: err <= 2e-3 for bf16 inputs with fp32 state, <= 1e-5
+for fp32 inputs.  Sizes span several chunks and ragged tails; the full-size
+workloads are checked in full where the oracle finishes in seconds, else on
+the sampled subsets named in each test.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kda_inputs as ki
+import oracle
+import serving_kda_chunked_gb300 as kda
+from parity import TOL, assert_close, err, oracle_prefill_windowed
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+DT = {"bf16": torch.bfloat16, "fp32": torch.float32}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from serving_kda_chunked_gb300 import build
+    build.build()
+    kda.load()
+
+
+def _run_prefill(inp, chunk=64, S0=None):
+    S0 = inp["S0"] if S0 is None else S0
+    o, S_T = kda.kda_prefill_chunked(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                     inp["cu_seqlens"], S0, chunk=chunk)
+    torch.cuda.synchronize()
+    return o, S_T
+
+
+def _oracle_prefill(inp, S0="default"):
+    S0 = inp["S0"] if isinstance(S0, str) else S0
+    o, S_T, _ = oracle.prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                               S0, inp["cu_seqlens"])
+    return o, S_T
+
+
+# ---------------------------------------------------------------------------
+# decode
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_decode_small_multi_step(d, dtype):
+    cfg = ki.DecodeConfig("t", B=5, H=3, d=d, steps=12, dtype=dtype)
+    inp = ki.decode_inputs(cfg, device=DEV, seed=1)
+    S = inp["S0"].clone()
+    S_ref = inp["S0"].double().cpu().numpy()
+    for s in range(cfg.steps):
+        o = kda.kda_decode_step(inp["q"][s], inp["k"][s], inp["v"][s], inp["g"][s],
+                                inp["beta"][s], S)
+        o_ref, S_ref = oracle.decode_step(inp["q"][s], inp["k"][s], inp["v"][s],
+                                          inp["g"][s], inp["beta"][s], S_ref)
+        torch.cuda.synchronize()
+        assert_close("o step %d" % s, o, o_ref, TOL[DT[dtype]])
+        assert_close("S step %d" % s, S, S_ref, TOL[DT[dtype]])
+
+
+def test_decode_workload_first_steps_full():
+    """B=256, H=32, d=128 decode: every sequence and head, first 8 steps."""
+    inp = ki.decode_inputs("decode", device=DEV, steps=8)
+    S = inp["S0"].clone()
+    S_ref = inp["S0"].double().cpu().numpy()
+    for s in range(8):
+        o = kda.kda_decode_step(inp["q"][s], inp["k"][s], inp["v"][s], inp["g"][s],
+                                inp["beta"][s], S)
+        o_ref, S_ref = oracle.decode_step(inp["q"][s], inp["k"][s], inp["v"][s],
+                                          inp["g"][s], inp["beta"][s], S_ref)
+        torch.cuda.synchronize()
+        assert_close("o", o, o_ref, 2e-3)
+    assert_close("S", S, S_ref, 2e-3)
+
+
+def test_decode_workload_1024_steps_sampled_sequences():
+    """All 1024 in-place steps on the full B=256 batch; sequences 0..7 (every
+    head) are checked at every step.  A sequence's decode tokens form one
+    sequence for the oracle's prefill, which is the same recurrence."""
+    inp = ki.decode_inputs("decode", device=DEV)
+    steps, nb = inp["q"].shape[0], 8
+    S = inp["S0"].clone()
+    o_hist = torch.empty((steps, nb, 32, 128), dtype=torch.bfloat16, device=DEV)
+    for s in range(steps):
+        o = kda.kda_decode_step(inp["q"][s], inp["k"][s], inp["v"][s], inp["g"][s],
+                                inp["beta"][s], S)
+        o_hist[s] = o[:nb]
+    torch.cuda.synchronize()
+    seq = lambda x: x[:, :nb].transpose(0, 1).reshape((nb * steps,) + tuple(x.shape[2:]))
+    o_ref, S_ref, _ = oracle.prefill(seq(inp["q"]), seq(inp["k"]), seq(inp["v"]),
+                                     seq(inp["g"]), seq(inp["beta"]), inp["S0"][:nb],
+                                     np.arange(nb + 1) * steps)
+    o_ref = o_ref.reshape(nb, steps, 32, 128).transpose(1, 0, 2, 3)
+    assert_close("o[1024 steps, seq 0..7]", o_hist, o_ref, 2e-3)
+    assert_close("S[seq 0..7]", S[:nb], S_ref, 2e-3)
+
+
+# ---------------------------------------------------------------------------
+# prefill
+# ---------------------------------------------------------------------------
+def test_prefill_tiny_fp32():
+    """B=1, H=2, T=256, d=64, fp32 inputs: tolerance 1e-5."""
+    inp = ki.prefill_inputs("tiny", device=DEV)
+    o, S_T = _run_prefill(inp)
+    o_ref, S_ref = _oracle_prefill(inp)
+    assert_close("o", o, o_ref, 1e-5)
+    assert_close("S_T", S_T, S_ref, 1e-5)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_prefill_ragged_packed_batch(d, dtype):
+    """Packed sequences of lengths that hit every chunk edge: empty, 1, one
+    short of a chunk, exactly one chunk, one past, several chunks + tail."""
+    lengths = [1, 63, 0, 64, 65, 200, 130, 7]
+    cfg = ki.PrefillConfig("ragged", H=3, d=d, dtype=dtype, n_seqs=len(lengths),
+                           s0_std=0.3)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=3, lengths=lengths)
+    o, S_T = _run_prefill(inp)
+    o_ref, S_ref = _oracle_prefill(inp)
+    assert_close("o", o, o_ref, TOL[DT[dtype]])
+    assert_close("S_T", S_T, S_ref, TOL[DT[dtype]])
+    # the empty sequence passes its initial state through unchanged
+    assert torch.equal(S_T[2], inp["S0"][2])
+
+
+def test_prefill_single_sequence_workload():
+    """B=1, H=32, T=8192, d=128, bf16: checked in full."""
+    inp = ki.prefill_inputs("single", device=DEV)
+    o, S_T = _run_prefill(inp)
+    o_ref, S_ref = _oracle_prefill(inp)
+    assert_close("o", o, o_ref, 2e-3)
+    assert_close("S_T", S_T, S_ref, 2e-3)
+
+
+def test_prefill_varlen_workload():
+    """16 packed sequences, lengths in [512, 16384], S0 ~ N(0, 0.02^2): in full."""
+    inp = ki.prefill_inputs("varlen", device=DEV)
+    o, S_T = _run_prefill(inp)
+    o_ref, S_ref = _oracle_prefill(inp)
+    assert_close("o", o, o_ref, 2e-3)
+    assert_close("S_T", S_T, S_ref, 2e-3)
+
+
+def test_prefill_long_context_workload():
+    """T = 1,048,576, H=32, d=128, slow gates.  (i) A 65,536-token prefix call
+    against the oracle in full.  (ii) The oracle continues from the GPU's
+    prefix state over the remaining tokens on state columns 0..7 of every head
+    (columns never mix, so this is exact for those columns) and is compared
+    with the full call's final state.  (iii) The full call's first 65,536
+    outputs equal the prefix call's bit for bit (same chunks, same order)."""
+    inp = ki.prefill_inputs("long", device=DEV)
+    T, P = inp["q"].shape[0], 65536
+    o_full, S_full = _run_prefill(inp)
+    pre = {key: inp[key][:P] for key in ("q", "k", "v", "g", "beta")}
+    pre["cu_seqlens"] = torch.tensor([0, P], dtype=torch.int32, device=DEV)
+    o_pre, S_pre = kda.kda_prefill_chunked(pre["q"], pre["k"], pre["v"], pre["g"],
+                                           pre["beta"], pre["cu_seqlens"], None)
+    torch.cuda.synchronize()
+    # (iii)
+    assert torch.equal(o_full[:P], o_pre)
+    # (i)
+    o_ref, S_ref = oracle_prefill_windowed(inp, 0, P, None)
+    assert_close("o prefix", o_pre, o_ref, 2e-3)
+    assert_close("S prefix", S_pre[0], S_ref, 2e-3)
+    # (ii)
+    cols = slice(0, 8)
+    S_start = S_pre[0][..., cols].double().cpu().numpy()
+    _, S_end = oracle_prefill_windowed(inp, P, T, S_start, cols=cols)
+    assert_close("S_T (cols 0..7, from GPU prefix state)", S_full[0][..., cols], S_end, 2e-3)
+
+
+# ---------------------------------------------------------------------------
+# segmentation, aliasing, determinism, guards
+# ---------------------------------------------------------------------------
+def test_resume_from_state_is_exact_on_chunk_boundaries():
+    cfg = ki.PrefillConfig("seg", H=4, d=128, dtype="bf16", T=640, s0_std=0.1)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=5)
+    o, S_T = _run_prefill(inp)
+    T1 = 256
+    cu1 = torch.tensor([0, T1], dtype=torch.int32, device=DEV)
+    cu2 = torch.tensor([0, 640 - T1], dtype=torch.int32, device=DEV)
+    sl = lambda x, a, b: x[a:b].contiguous()
+    o1, S1 = kda.kda_prefill_chunked(*(sl(inp[n], 0, T1) for n in ("q", "k", "v", "g", "beta")),
+                                     cu1, inp["S0"])
+    o2, S2 = kda.kda_prefill_chunked(*(sl(inp[n], T1, 640) for n in ("q", "k", "v", "g", "beta")),
+                                     cu2, S1)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([o1, o2]), o)
+    assert torch.equal(S2, S_T)
+
+
+def test_prefill_then_decode_matches_longer_prefill():
+    cfg = ki.PrefillConfig("pd", H=4, d=128, dtype="bf16", T=200, s0_std=0.05)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=6)
+    n_dec, T0 = 8, 192
+    cu0 = torch.tensor([0, T0], dtype=torch.int32, device=DEV)
+    _, S = kda.kda_prefill_chunked(*(inp[n][:T0].contiguous() for n in ("q", "k", "v", "g", "beta")),
+                                   cu0, inp["S0"])
+    outs = []
+    for t in range(T0, T0 + n_dec):
+        outs.append(kda.kda_decode_step(*(inp[n][t:t + 1].contiguous() for n in ("q", "k", "v", "g", "beta")),
+                                        S))
+    torch.cuda.synchronize()
+    o_ref, S_ref = _oracle_prefill(inp)
+    assert_close("o decode tail", torch.cat(outs), o_ref[T0:T0 + n_dec], 2e-3)
+    assert_close("S after decode", S, S_ref, 2e-3)
+
+
+def test_state_in_place_alias_and_determinism():
+    lengths = [300, 77]
+    cfg = ki.PrefillConfig("alias", H=2, d=128, dtype="bf16", n_seqs=2, s0_std=0.2)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=7, lengths=lengths)
+    o_a, S_a = _run_prefill(inp)
+    o_b, S_b = _run_prefill(inp)
+    assert torch.equal(o_a, o_b) and torch.equal(S_a, S_b)
+    S_io = inp["S0"].clone()
+    o_c, S_c = kda.kda_prefill_chunked(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                       inp["cu_seqlens"], S_io, S_T=S_io)
+    torch.cuda.synchronize()
+    assert S_c.data_ptr() == S_io.data_ptr()
+    assert torch.equal(o_c, o_a) and torch.equal(S_c, S_a)
+
+
+def test_outputs_stay_inside_their_buffers():
+    """Guard rows around o and S_T keep their sentinel values."""
+    lengths = [70, 129]
+    cfg = ki.PrefillConfig("guard", H=2, d=128, dtype="bf16", n_seqs=2, s0_std=0.1)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=8, lengths=lengths)
+    T, G = sum(lengths), 16
+    o_buf = torch.full((T + 2 * G, 2, 128), 7.0, dtype=torch.bfloat16, device=DEV)
+    s_buf = torch.full((2 + 2, 2, 128, 128), -3.0, dtype=torch.float32, device=DEV)
+    o, S_T = kda.kda_prefill_chunked(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                     inp["cu_seqlens"], inp["S0"], o=o_buf[G:G + T],
+                                     S_T=s_buf[1:3])
+    torch.cuda.synchronize()
+    assert torch.all(o_buf[:G] == 7.0) and torch.all(o_buf[G + T:] == 7.0)
+    assert torch.all(s_buf[0] == -3.0) and torch.all(s_buf[3] == -3.0)
+    o_ref, S_ref = _oracle_prefill(inp)
+    assert_close("o", o, o_ref, 2e-3)
+    assert_close("S_T", S_T, S_ref, 2e-3)
+
+
+def test_corrupt_offsets_stay_in_bounds():
+    """Offsets beyond T_total or decreasing are clamped into [0, T_total] on
+    the device: [0, 60, 1000, 5] with T_total = 100 acts as [0, 60, 100, 100]
+    (the last sequence is empty), and nothing is written outside o / S_T."""
+    cfg = ki.PrefillConfig("bad", H=2, d=64, dtype="bf16", T=100)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=9)
+    cu = torch.tensor([0, 60, 1000, 5], dtype=torch.int32, device=DEV)
+    S0 = torch.zeros((3, 2, 64, 64), device=DEV)
+    o, S_T = kda.kda_prefill_chunked(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                     cu, S0)
+    torch.cuda.synchronize()
+    o_ref, S_ref, _ = oracle.prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                     None, [0, 60, 100, 100])
+    assert_close("o", o, o_ref, 2e-3)
+    assert_close("S_T", S_T, S_ref, 2e-3)
+    assert torch.all(S_T[2] == 0)
