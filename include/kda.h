@@ -50,7 +50,7 @@ typedef enum kda_status {
     KDA_ERR_INVALID_ARG = 1,  /* null pointer, misalignment, bad size       */
     KDA_ERR_UNSUPPORTED = 2,  /* head size / chunk / dtype not compiled in   */
     KDA_ERR_CUDA = 3,         /* a CUDA launch or attribute call failed      */
-    KDA_ERR_TIMEOUT = 4       /* reserved: a bounded device wait gave up     */
+    KDA_ERR_TIMEOUT = 4       /* a bounded device wait gave up (see check) */
 } kda_status;
 
 typedef enum kda_dtype {
@@ -75,6 +75,17 @@ typedef enum kda_dtype {
  *   chunk      64 (tokens per chunk); chunks never cross sequences and a
  *              partial last chunk is handled as if padded with no-op tokens
  *   dtype      KDA_BF16 or KDA_FP32
+ *   workspace  device scratch of at least kda_prefill_workspace_size(...)
+ *              bytes, 16-byte aligned, owned by the caller; may be NULL when
+ *              that size is 0.  Its contents on entry do not matter; calls
+ *              that share one workspace must not overlap on the GPU.
+ *
+ * With bf16 inputs and dk = dv = 128 the work runs on the tensor cores in two
+ * kernels per window of up to 2048 chunks: one resolves every (chunk, head)
+ * independently and writes its operands to the workspace, the next walks
+ * each sequence's chunks in order carrying the fp32 state.  Every other case
+ * (fp32 inputs, or dk = dv = 64) runs a CUDA-core kernel in fp32 arithmetic
+ * that needs no workspace.
  *
  * Sequence n covers tokens [cu[n], cu[n+1]).  A sequence of length 0 copies
  * its S0 (or zeros) to S_T.  cu_seqlens lives in device memory and is not
@@ -88,7 +99,25 @@ kda_status kda_prefill_chunked(const void *q, const void *k, const void *v,
                                int32_t N, int64_t T_total, int32_t H,
                                int32_t dk, int32_t dv, int32_t dtype,
                                int32_t chunk, void *o, float *S_T,
+                               void *workspace, uint64_t workspace_bytes,
                                void *stream);
+
+/*
+ * Bytes of workspace kda_prefill_chunked needs for these sizes (0 for fp32
+ * inputs).  Pure host arithmetic: no device access.  Returns 0 as well for
+ * arguments that kda_prefill_chunked would reject.
+ */
+uint64_t kda_prefill_workspace_size(int32_t N, int64_t T_total, int32_t H,
+                                    int32_t dk, int32_t dv, int32_t dtype,
+                                    int32_t chunk);
+
+/*
+ * Synchronise `stream` and report the device-side status of the last
+ * kda_prefill_chunked call that used `workspace`: KDA_ERR_TIMEOUT if one of
+ * its kernels gave up on a bounded wait (its outputs are then incomplete),
+ * KDA_ERR_CUDA if the stream reports an error, else KDA_OK.
+ */
+kda_status kda_prefill_check(const void *workspace, void *stream);
 
 /*
  * kda_decode_step -- one token for each of B independent sequences; the

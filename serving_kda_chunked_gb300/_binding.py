@@ -50,10 +50,15 @@ def load() -> ctypes.CDLL:
                 "`python -m serving_kda_chunked_gb300.build`" % LIB_PATH)
         lib = ctypes.CDLL(LIB_PATH)
         vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        u64 = ctypes.c_uint64
         lib.kda_prefill_chunked.argtypes = [
             vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, i32,
-            vp, vp, vp]
+            vp, vp, vp, u64, vp]
         lib.kda_prefill_chunked.restype = ctypes.c_int
+        lib.kda_prefill_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32, i32]
+        lib.kda_prefill_workspace_size.restype = u64
+        lib.kda_prefill_check.argtypes = [vp, vp]
+        lib.kda_prefill_check.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [
             vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]
         lib.kda_decode_step.restype = ctypes.c_int
@@ -96,14 +101,28 @@ def _check_cuda(name, t, dtype=None, shape=None):
         raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
 
 
+def kda_prefill_workspace_size(N, T, H, dk, dv, dtype, chunk=64) -> int:
+    """Workspace bytes ``kda_prefill_chunked`` needs (0: none)."""
+    code = _DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(load().kda_prefill_workspace_size(N, T, H, dk, dv, code, chunk))
+
+
+def kda_prefill_check(workspace, stream=None) -> int:
+    """Synchronise the stream and return the device status of the last
+    prefill that used ``workspace`` (KDA_OK or KDA_ERR_TIMEOUT)."""
+    return int(load().kda_prefill_check(_ptr(workspace), _stream(stream)))
+
+
 def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, S0=None, *, chunk: int = 64,
-                        o=None, S_T=None, stream=None):
+                        o=None, S_T=None, workspace=None, stream=None):
     """Chunked KDA prefill over a packed batch (``kda_prefill_chunked`` in kda.h).
 
     q, k [T, H, dk] and v [T, H, dv] in bf16 or fp32 (all the same); g
     [T, H, dk] fp32 log-gates; beta [T, H] fp32; cu_seqlens [N+1] int32 on the
     device; S0 [N, H, dk, dv] fp32 or None.  Returns (o, S_T); pass ``o`` /
     ``S_T`` to write into existing buffers (``S_T`` may be ``S0``).
+    ``workspace``: a uint8 CUDA tensor of at least
+    ``kda_prefill_workspace_size(...)`` bytes; allocated here when omitted.
     """
     _check_cuda("q", q)
     if q.dtype not in _DTYPE_CODE:
@@ -124,10 +143,17 @@ def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, S0=None, *, chunk: int = 6
     if S_T is None:
         S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
     _check_cuda("S_T", S_T, torch.float32, (N, H, dk, dv))
+    need = kda_prefill_workspace_size(N, T, H, dk, dv, q.dtype, chunk)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0
+    if workspace is not None:
+        _check_cuda("workspace", workspace, torch.uint8)
+        ws_bytes = workspace.numel()
     st = load().kda_prefill_chunked(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
         N, T, H, dk, dv, _DTYPE_CODE[q.dtype], int(chunk), _ptr(o), _ptr(S_T),
-        _stream(stream))
+        _ptr(workspace), ws_bytes, _stream(stream))
     if st != KDA_OK:
         raise KdaError("kda_prefill_chunked", st)
     return o, S_T

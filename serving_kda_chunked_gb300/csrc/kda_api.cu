@@ -24,6 +24,7 @@ kda_status kda_prefill_chunked(const void *q, const void *k, const void *v,
                                int32_t N, int64_t T_total, int32_t H,
                                int32_t dk, int32_t dv, int32_t dtype,
                                int32_t chunk, void *o, float *S_T,
+                               void *workspace, uint64_t workspace_bytes,
                                void *stream) {
     if (N < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
     if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
@@ -37,13 +38,39 @@ kda_status kda_prefill_chunked(const void *q, const void *k, const void *v,
         !aligned4(cu_seqlens))
         return KDA_ERR_INVALID_ARG;
     if ((int64_t)N * H * (dv / 32) > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+    const bool tensor_path = dtype == KDA_BF16 && dk == 128;
+    if (tensor_path) {
+        if (T_total / 64 + N > 0x3fffffffLL) return KDA_ERR_UNSUPPORTED;
+        const uint64_t need = kda::prefill_tc_workspace_bytes(N, T_total, H);
+        if (!workspace || workspace_bytes < need || !aligned16(workspace))
+            return KDA_ERR_INVALID_ARG;
+    }
 
     kda::PrefillArgs a;
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S0 = S0;
     a.cu_seqlens = cu_seqlens; a.o = o; a.S_T = S_T;
     a.N = N; a.H = H; a.dk = dk; a.dv = dv; a.dtype = dtype; a.chunk = chunk;
     a.T = T_total;
+    if (tensor_path)
+        return cuda_status(kda::launch_prefill_tc(a, workspace, (cudaStream_t)stream));
     return cuda_status(kda::launch_prefill_simt(a, (cudaStream_t)stream));
+}
+
+uint64_t kda_prefill_workspace_size(int32_t N, int64_t T_total, int32_t H, int32_t dk,
+                                    int32_t dv, int32_t dtype, int32_t chunk) {
+    if (N <= 0 || T_total < 0 || H <= 0 || !head_ok(dk, dv) || chunk != 64) return 0;
+    if (dtype != KDA_BF16 || dk != 128) return 0;
+    return (uint64_t)kda::prefill_tc_workspace_bytes(N, T_total, H);
+}
+
+kda_status kda_prefill_check(const void *workspace, void *stream) {
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (!workspace) return KDA_OK;
+    int32_t word = 0;
+    e = cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e);
+    return word != 0 ? KDA_ERR_TIMEOUT : KDA_OK;
 }
 
 kda_status kda_decode_step(const void *q, const void *k, const void *v,
@@ -78,6 +105,6 @@ const char *kda_status_string(int32_t status) {
     }
 }
 
-int32_t kda_abi_version(void) { return (1 << 16) | 0; }
+int32_t kda_abi_version(void) { return (2 << 16) | 0; }
 
 }  // extern "C"

@@ -29,6 +29,8 @@ struct DecodeArgs {
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, void *workspace, cudaStream_t stream);
+size_t prefill_tc_workspace_bytes(int32_t N, int64_t T, int32_t H);
 
 // ---- element access helpers ------------------------------------------------
 __device__ __forceinline__ float to_f32(float x) { return x; }

@@ -50,7 +50,7 @@ def test_status_strings(lib):
     assert "INVALID" in kda.status_string(kda.KDA_ERR_INVALID_ARG)
     assert "UNSUPPORTED" in kda.status_string(kda.KDA_ERR_UNSUPPORTED)
     assert "UNKNOWN" in kda.status_string(99)
-    assert kda.abi_version() >> 16 == 1
+    assert kda.abi_version() >> 16 == 2
 
 
 P = 0x10000  # a 16-byte aligned stand-in address; never dereferenced here
@@ -58,13 +58,13 @@ P = 0x10000  # a 16-byte aligned stand-in address; never dereferenced here
 
 def _prefill(lib, **kw):
     a = dict(q=P, k=P, v=P, g=P, beta=P, S0=None, cu=P, N=1, T=64, H=2, dk=128,
-             dv=128, dtype=0, chunk=64, o=P, S_T=P)
+             dv=128, dtype=0, chunk=64, o=P, S_T=P, ws=None, ws_bytes=0)
     a.update(kw)
     vp = ctypes.c_void_p
     return lib.kda_prefill_chunked(
         vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]),
         vp(a["S0"]), vp(a["cu"]), a["N"], a["T"], a["H"], a["dk"], a["dv"],
-        a["dtype"], a["chunk"], vp(a["o"]), vp(a["S_T"]), None)
+        a["dtype"], a["chunk"], vp(a["o"]), vp(a["S_T"]), vp(a["ws"]), a["ws_bytes"], None)
 
 
 def _decode(lib, **kw):
@@ -96,6 +96,9 @@ def _decode(lib, **kw):
     (dict(beta=P + 1), kda.KDA_ERR_INVALID_ARG),
     (dict(N=0, T=10), kda.KDA_ERR_INVALID_ARG),
     (dict(N=0, T=0), kda.KDA_OK),                      # empty batch: no-op
+    (dict(ws=None), kda.KDA_ERR_INVALID_ARG),          # bf16, d=128 needs a workspace
+    (dict(ws=P, ws_bytes=1024), kda.KDA_ERR_INVALID_ARG),
+    (dict(ws=P + 8, ws_bytes=1 << 40), kda.KDA_ERR_INVALID_ARG),
 ])
 def test_prefill_host_validation(lib, kw, expect):
     assert _prefill(lib, **kw) == expect
@@ -114,6 +117,18 @@ def test_prefill_host_validation(lib, kw, expect):
 ])
 def test_decode_host_validation(lib, kw, expect):
     assert _decode(lib, **kw) == expect
+
+
+def test_workspace_size_query(lib):
+    n = kda.kda_prefill_workspace_size(1, 8192, 32, 128, 128, kda.KDA_BF16)
+    # header + chunk table, then one 74,240-byte operand block per (chunk, head)
+    assert n == 1024 + (8192 // 64 + 1) * 32 * 74240
+    # long inputs are processed in windows of 2048 chunks
+    big = kda.kda_prefill_workspace_size(1, 1 << 20, 32, 128, 128, kda.KDA_BF16)
+    assert big == 1024 + 2048 * 32 * 74240
+    assert kda.kda_prefill_workspace_size(1, 8192, 32, 128, 128, kda.KDA_FP32) == 0
+    assert kda.kda_prefill_workspace_size(1, 8192, 32, 64, 64, kda.KDA_BF16) == 0
+    assert kda.kda_prefill_workspace_size(1, 8192, 32, 96, 96, kda.KDA_BF16) == 0
 
 
 def test_binding_rejects_host_tensors(lib):
