@@ -38,6 +38,8 @@
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 namespace kda {
@@ -54,7 +56,7 @@ constexpr int NSLICE = D / DVS;
 constexpr uint32_t WS_HEADER = 256;
 constexpr uint32_t IMG_W = 0;          // W   [64 x 128] fp16, K-major SW128 (2 atoms)
 constexpr uint32_t IMG_Q = 16384;      // Q^  [64 x 128] fp16, K-major SW128 (2 atoms)
-constexpr uint32_t IMG_KT = 32768;     // Kb^T [128 x 64] fp16, K-major SW128
+constexpr uint32_t IMG_KT = 32768;     // Kb [64 x 128] fp16, [r][c] SW128 (MN-major A)
 constexpr uint32_t IMG_P = 49152;      // P   [64 x 64] fp16, K-major SW128
 constexpr uint32_t IMG_U = 57344;      // U~  [4 slices][64][32] fp16
 constexpr uint32_t IMG_G = 73728;      // e^gamma_last [128] fp32
@@ -135,24 +137,40 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 // ------------------------------------------------------------------------------
 // K1: intra-chunk kernel
 // ------------------------------------------------------------------------------
+// One CTA per SM walks (chunk, head) tasks.  Per task:
+//   1. TMA brings k, q, v (bf16) and g (fp32) rows [t0, t0 + 64) of head h
+//      into staging (issued one task ahead).
+//   2. Per-channel cumulative log-gate (in place), e^gamma_last, range check.
+//   3. Element-wise prep, 8 channels of one row per unit: tf32 operands
+//      [K e^g ; Q e^g] and K e^-g for A / P, fp16 K e^g and V for W / U~, and
+//      the Q^ and Kbar images written straight to the workspace.
+//   4. One M = 128 tf32 MMA: rows 0-63 give A / beta, rows 64-127 give P.
+//      A chunk whose decay exceeds e^80 on some channel would overflow those
+//      factors, so it takes an exact pairwise CUDA-core path instead.
+//   5. T = (I + A)^-1 on CUDA cores (fp32; 16 x 16 diagonal blocks, then
+//      three block levels), T' = T Diag(beta) as fp16.
+//   6. W = T' (K e^g), U~ = T' V on tcgen05 (fp16), stored to the workspace.
 constexpr int K1_THREADS = 256;
-// shared-memory map (offsets from a 1024-aligned base)
-constexpr uint32_t S1_KH0 = 0, S1_KH1 = 32768;        // K^ (tf32, 64 x 128) x 2
-constexpr uint32_t S1_XT0 = 65536, S1_XT1 = 81920;    // [k~; q~] (tf32, 32 x 128) x 2
-constexpr uint32_t S1_KGT = 98304;                    // (K e^gamma)^T fp16 [128][64]
-constexpr uint32_t S1_VOP = 114688;                   // V fp16, MN-major SW128
-constexpr uint32_t S1_QIMG = 131072;                  // Q^ image
-constexpr uint32_t S1_KTIMG = 147456;                 // Kb^T image
-constexpr uint32_t S1_PIMG = 163840;                  // P image
-constexpr uint32_t S1_TP = 172032;                    // T' fp16 [64][64] SW128
-constexpr uint32_t S1_MISC = 180224;
-constexpr uint32_t S1_BYTES = S1_MISC + 4096 + 1024;  // + alignment slack
-constexpr int AP_COL = 0, W_COL = 128, U_COL = 256;   // TMEM columns
-constexpr int TP = 65;                                 // padded fp32 row stride
+constexpr uint32_t S1_STG_K = 0, S1_STG_Q = 16384, S1_STG_V = 32768;  // bf16 [64][128]
+constexpr uint32_t S1_STG_G = 49152;                                  // fp32 [64][128]
+constexpr uint32_t S1_OPA = 81920;    // tf32 [K e^g ; Q e^g]: 4 atoms x 128 rows x 128 B
+constexpr uint32_t S1_OPB = 147456;   // tf32 K e^-g: 4 atoms x 64 rows x 128 B
+constexpr uint32_t S1_KG16 = 180224;  // fp16 K e^g, [r][c] 128B-swizzled (MN-major B)
+constexpr uint32_t S1_V16 = 196608;   // fp16 V, same layout
+constexpr uint32_t S1_TP = 212992;    // fp16 T', K-major SW128 [r][i]
+constexpr uint32_t S1_MISC = 221184;
+constexpr uint32_t S1_BYTES = S1_MISC + 2048 + 1024;
+// after the A/P MMA has completed the operand area is reused:
+constexpr uint32_t S1_AS = S1_OPA;            // A  fp32 [64][TP]
+constexpr uint32_t S1_TS = S1_OPA + 17408;    // T  fp32 [64][TP]
+constexpr uint32_t S1_Y = S1_OPA + 34816;     // [3][16][17] fp32 scratch
+constexpr int AP_COL = 0, W_COL = 64, U_COL = 192;   // TMEM columns
+constexpr int TP = 65;                                // padded fp32 row stride
+constexpr float RANGE_LIMIT = 80.f;                   // e^80 stays inside fp32
 
 struct K1Params {
-    const __nv_bfloat16 *q, *k, *v;
-    const float *g, *beta;
+    CUtensorMap tm_q, tm_k, tm_v, tm_g;   // 3D maps over [T][H][128]
+    const float *beta;
     const int32_t *cu;
     uint8_t *ws;
     int N, H;
@@ -160,19 +178,38 @@ struct K1Params {
     int w0, w1;
 };
 
-__global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const K1Params p) {
+__device__ __forceinline__ void tma_load_3d(uint8_t *dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint64_t *mbar) {
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4}], [%5];"
+                 :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1),
+                    "r"(c2), "r"(smem_addr(mbar))
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 pack8_h(const float *x) {
+    return make_uint4(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]), pack_h2(x[4], x[5]),
+                      pack_h2(x[6], x[7]));
+}
+
+// [r][c] 128B-swizzled image with 64-channel atoms: byte offset of the 16-byte
+// chunk holding channels c0..c0+7 of row r (c0 a multiple of 8).
+__device__ __forceinline__ uint32_t rc_img_off(int r, int c0) {
+    return (uint32_t)(c0 >> 6) * 8192u + sw128_off(r, (c0 & 63) >> 3);
+}
+
+__global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_constant__ K1Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    float *sRef = reinterpret_cast<float *>(sm + S1_MISC);           // [5][128]
-    float *sTot = sRef + 5 * 128;                                    // [128]
-    float *sB = sTot + 128;                                          // [64]
-    float *sGL = sB + 64;                                            // [128]
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(sGL + 128);        // [3]
+    float *gL = reinterpret_cast<float *>(sm + S1_MISC);   // [128] gamma_last
+    float *eL = gL + 128;                                  // [128] e^gamma_last
+    float *sB = eL + 128;                                  // [64] beta
+    float *tot = sB + 64;                                  // [128] half-chunk totals
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(tot + 128);   // [0] TMA, [1] A/P, [2] W/U
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 3);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = tid & 127, half = tid >> 7;
     int32_t *ws_hdr = reinterpret_cast<int32_t *>(p.ws);
     const int32_t *chunk_base = reinterpret_cast<const int32_t *>(p.ws + WS_HEADER);
     uint8_t *img_base = p.ws + ws_images_offset(p.N);
@@ -193,139 +230,199 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const K1Params p) 
     const int total = chunk_base[p.N];
     const int c_end = min(p.w1, total);
     const int ntask = (c_end > p.w0 ? c_end - p.w0 : 0) * H;
-    bool ok = true;
-    uint32_t iter = 0;
 
-    for (int task = blockIdx.x; task < ntask && ok; task += gridDim.x, ++iter) {
-        const int ch = p.w0 + task / H;     // global chunk
-        const int h = task % H;
+    auto task_pos = [&](int task, int &h, int64_t &t0, int &L) {
+        const int ch = p.w0 + task / H;
+        h = task % H;
         const int n = find_seq(chunk_base, p.N, ch);
         int64_t bos, eos;
         seq_bounds(p.cu, n, p.T, bos, eos);
-        const int64_t t0 = bos + (int64_t)(ch - chunk_base[n]) * C;
-        const int L = (int)((eos - t0) < C ? (eos - t0) : C);
+        t0 = bos + (int64_t)(ch - chunk_base[n]) * C;
+        L = (int)((eos - t0) < C ? (eos - t0) : C);
+    };
+    auto issue_tma = [&](int task) {
+        int h, L;
+        int64_t t0;
+        task_pos(task, h, t0, L);
+        mbar_arrive_expect_tx(&mbar[0], 3 * 16384 + 32768);
+        tma_load_3d(sm + S1_STG_K, &p.tm_k, 0, h, (int)t0, &mbar[0]);
+        tma_load_3d(sm + S1_STG_Q, &p.tm_q, 0, h, (int)t0, &mbar[0]);
+        tma_load_3d(sm + S1_STG_V, &p.tm_v, 0, h, (int)t0, &mbar[0]);
+        tma_load_3d(sm + S1_STG_G, &p.tm_g, 0, h, (int)t0, &mbar[0]);
+    };
+    if (tid == 0 && (int)blockIdx.x < ntask) issue_tma(blockIdx.x);
+
+    bool ok = true;
+    uint32_t it = 0, ap_it = 0;
+    for (int task = blockIdx.x; task < ntask; task += gridDim.x, ++it) {
+        int h, L;
+        int64_t t0;
+        task_pos(task, h, t0, L);
         uint8_t *out = img_base + (uint64_t)task * CH_STRIDE;
-
-        // ---- load this thread's 32 rows of channel c ------------------------
-        float kv[32], qv[32], gam[32];
-        __half vh[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int r = 32 * half + j;
-            float kk = 0.f, qq = 0.f, gg = 0.f, vv = 0.f;
-            if (r < L) {
-                const int64_t off = ((t0 + r) * H + h) * D + c;
-                kk = __bfloat162float(p.k[off]);
-                qq = __bfloat162float(p.q[off]);
-                vv = __bfloat162float(p.v[off]);
-                gg = p.g[off];
-            }
-            kv[j] = kk; qv[j] = qq; gam[j] = gg; vh[j] = __float2half_rn(vv);
-        }
         if (tid < C) sB[tid] = tid < L ? p.beta[(t0 + tid) * H + h] : 0.f;
-
-        // ---- per-channel cumulative log-gate ---------------------------------
-        float acc = 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) { acc += gam[j]; gam[j] = acc; }
-        if (half == 0) sTot[c] = acc;
-        __syncthreads();
-        if (half == 1) {
-            const float off = sTot[c];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) gam[j] += off;
-        }
-        if (half == 0) { sRef[0 * 128 + c] = 0.f; sRef[1 * 128 + c] = gam[15]; sRef[2 * 128 + c] = gam[31]; }
-        else { sRef[3 * 128 + c] = gam[15]; sRef[4 * 128 + c] = gam[31]; }
-        __syncthreads();
-
-        // ---- S-independent images: K e^gamma, Q e^gamma, Kbar, V (fp16) ------
-        {
-            const float gl = sRef[4 * 128 + c];
-            if (half == 0) sGL[c] = __expf(gl);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int r = 32 * half + j;
-                const float e = __expf(gam[j]);
-                const float eb = __expf(gl - gam[j]);
-                const uint32_t o_rc = (uint32_t)(c >> 6) * 8192u + sw128_off(r, (c & 63) >> 3) + (c & 7) * 2;
-                const uint32_t o_cr = sw128_off(c, r >> 3) + (r & 7) * 2;
-                *reinterpret_cast<__half *>(sm + S1_KGT + o_cr) = __float2half_rn(kv[j] * e);
-                *reinterpret_cast<__half *>(sm + S1_KTIMG + o_cr) = __float2half_rn(kv[j] * eb);
-                *reinterpret_cast<__half *>(sm + S1_QIMG + o_rc) = __float2half_rn(qv[j] * e);
-                *reinterpret_cast<__half *>(sm + S1_VOP + o_rc) = vh[j];
-            }
-        }
-
-        // ---- A and P on tcgen05 (tf32), one 16-row block R at a time ---------
-        // MMA R: D[i][jj] = sum_c Khat_R[i][c] X_R[jj][c] into TMEM cols 32R..32R+31,
-        // X_R = [k~ of block R ; q~ of block R]; D = A^T / beta (jj < 16), P^T.
-        for (int R = 0; R < 4; ++R) {
-            const uint32_t kh = (R & 1) ? S1_KH1 : S1_KH0;
-            const uint32_t xt = (R & 1) ? S1_XT1 : S1_XT0;
-            if (R >= 2) ok = __syncthreads_and(mbar_wait(&mbar[R & 1], 0) && ok);
-            if (!ok) break;
-            const float ref = sRef[R * 128 + c];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int r = 32 * half + j;
-                const uint32_t cofs = (uint32_t)(c >> 5);
-                const uint32_t within = (uint32_t)(c & 3) * 4;
-                if ((r >> 4) == R) {
-                    const float er = __expf(gam[j] - ref);
-                    const int row = r & 15;
-                    *reinterpret_cast<float *>(sm + xt + cofs * 4096u + sw128_off(row, (c & 31) >> 2) + within) = kv[j] * er;
-                    *reinterpret_cast<float *>(sm + xt + cofs * 4096u + sw128_off(16 + row, (c & 31) >> 2) + within) = qv[j] * er;
-                }
-                if (r <= 16 * R + 15) {
-                    const float ec = __expf(ref - gam[j]);
-                    *reinterpret_cast<float *>(sm + kh + cofs * 8192u + sw128_off(r, (c & 31) >> 2) + within) = kv[j] * ec;
-                }
-            }
-            fence_async_smem();
-            fence_before_sync();
-            __syncthreads();
-            if (tid == 0) {
-                fence_after_sync();
-                const uint32_t kh_a = smem_addr(sm + kh), xt_a = smem_addr(sm + xt);
-                const uint32_t id = idesc(64, 32, FMT_TF32, FMT_TF32, 0, 0);
-#pragma unroll
-                for (int s = 0; s < 16; ++s) {   // 8 tf32 (32 bytes) per K step
-                    const uint32_t atom = s >> 2, wi = (s & 3) * 32;
-                    mma_tf32(tmem + AP_COL + 32 * R, sdesc_k_sw128(kh_a + atom * 8192 + wi),
-                             sdesc_k_sw128(xt_a + atom * 4096 + wi), id, s > 0);
-                }
-                mma_commit(&mbar[R & 1]);
-            }
-        }
-        ok = __syncthreads_and(ok && mbar_wait(&mbar[0], 1) && mbar_wait(&mbar[1], 1));
-        fence_after_sync();
+        ok = __syncthreads_and(mbar_wait(&mbar[0], it & 1));
         if (!ok) break;
 
-        // ---- read A^T, P^T from TMEM (warps 0-3, lanes 0-15 hold token i) ------
-        float *As = reinterpret_cast<float *>(sm + S1_KH0);   // [64][TP] fp32
-        float *Ts = reinterpret_cast<float *>(sm + S1_KH1);   // [64][TP] fp32
-        if (warp < 4) {
-            const int i = 16 * warp + lane;
-            for (int R = 0; R < 4; ++R) {
-                float a[16], pp[16];
-                tmem_ld16(tmem_at(tmem, warp, AP_COL + 32 * R), a);
-                tmem_ld16(tmem_at(tmem, warp, AP_COL + 32 * R + 16), pp);
-                tmem_wait_ld();
-                if (lane < 16) {
+        // ---- cumulative log-gate, in place (rows past the sequence: g = 0) ----
+        {
+            const int c = tid & 127, half = tid >> 7;
+            float *G = reinterpret_cast<float *>(sm + S1_STG_G);
+            float acc = 0.f;
+            for (int j = 0; j < 32; ++j) {
+                const int r = 32 * half + j;
+                acc += r < L ? G[r * 128 + c] : 0.f;
+                G[r * 128 + c] = acc;
+            }
+            if (half == 0) tot[c] = acc;
+            __syncthreads();
+            if (half == 1) {
+                const float off = tot[c];
+                for (int j = 0; j < 32; ++j) G[(32 + j) * 128 + c] += off;
+                gL[c] = acc + off;
+                eL[c] = __expf(acc + off);
+            }
+        }
+        const bool slow = __syncthreads_or(tid >= 128 && -gL[tid & 127] > RANGE_LIMIT);
+
+        // ---- element-wise prep: unit = (row r, channels c0..c0+7) -------------
+        for (int jj = 0; jj < 4; ++jj) {
+            const int u = tid + K1_THREADS * jj;
+            const int r = u >> 4, c0 = (u & 15) * 8;
+            float kf[8], qf[8], vf[8], gm[8], el[8];
+            {
+                const uint4 kr = *reinterpret_cast<const uint4 *>(sm + S1_STG_K + r * 256 + c0 * 2);
+                const uint4 qr = *reinterpret_cast<const uint4 *>(sm + S1_STG_Q + r * 256 + c0 * 2);
+                const uint4 vr = *reinterpret_cast<const uint4 *>(sm + S1_STG_V + r * 256 + c0 * 2);
+                const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kr);
+                const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qr);
+                const __nv_bfloat162 *v2 = reinterpret_cast<const __nv_bfloat162 *>(&vr);
+                const bool live = r < L;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int r = 16 * R + j;
-                        As[r * TP + i] = r > i ? sB[r] * a[j] : 0.f;
-                        *reinterpret_cast<__half *>(sm + S1_PIMG + sw128_off(r, i >> 3) + (i & 7) * 2) =
-                            __float2half_rn(r >= i ? pp[j] : 0.f);
+                for (int e = 0; e < 4; ++e) {
+                    const float2 a = __bfloat1622float2(k2[e]), b2 = __bfloat1622float2(q2[e]),
+                                 c2 = __bfloat1622float2(v2[e]);
+                    kf[2 * e] = live ? a.x : 0.f; kf[2 * e + 1] = live ? a.y : 0.f;
+                    qf[2 * e] = live ? b2.x : 0.f; qf[2 * e + 1] = live ? b2.y : 0.f;
+                    vf[2 * e] = live ? c2.x : 0.f; vf[2 * e + 1] = live ? c2.y : 0.f;
+                }
+                const float4 g0 = *reinterpret_cast<const float4 *>(sm + S1_STG_G + r * 512 + c0 * 4);
+                const float4 g1 = *reinterpret_cast<const float4 *>(sm + S1_STG_G + r * 512 + c0 * 4 + 16);
+                gm[0] = g0.x; gm[1] = g0.y; gm[2] = g0.z; gm[3] = g0.w;
+                gm[4] = g1.x; gm[5] = g1.y; gm[6] = g1.z; gm[7] = g1.w;
+                const float4 e0 = *reinterpret_cast<const float4 *>(eL + c0);
+                const float4 e1 = *reinterpret_cast<const float4 *>(eL + c0 + 4);
+                el[0] = e0.x; el[1] = e0.y; el[2] = e0.z; el[3] = e0.w;
+                el[4] = e1.x; el[5] = e1.y; el[6] = e1.z; el[7] = e1.w;
+            }
+            float kg[8], qg[8], kh[8], kb[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float ep = __expf(gm[e]);
+                kg[e] = kf[e] * ep;
+                qg[e] = qf[e] * ep;
+                if (!slow) {   // e^-gamma <= e^80 here: Kbar = (K e^-g) e^gamma_last
+                    kh[e] = kf[e] * __expf(-gm[e]);
+                    kb[e] = kh[e] * el[e];
+                } else {
+                    kh[e] = 0.f;
+                    kb[e] = kf[e] * __expf(gL[c0 + e] - gm[e]);
+                }
+            }
+            const uint32_t ioff = rc_img_off(r, c0);
+            *reinterpret_cast<uint4 *>(sm + S1_KG16 + ioff) = pack8_h(kg);
+            *reinterpret_cast<uint4 *>(sm + S1_V16 + ioff) = pack8_h(vf);
+            *reinterpret_cast<uint4 *>(out + IMG_Q + ioff) = pack8_h(qg);
+            *reinterpret_cast<uint4 *>(out + IMG_KT + ioff) = pack8_h(kb);
+            if (!slow) {
+                const uint32_t atom = (uint32_t)(c0 >> 5), ch0 = (uint32_t)(c0 & 31) >> 2;
+#pragma unroll
+                for (int hc = 0; hc < 2; ++hc) {
+                    const uint32_t cc = ch0 + hc;
+                    *reinterpret_cast<float4 *>(sm + S1_OPA + atom * 16384 + sw128_off(r, cc)) =
+                        make_float4(kg[4 * hc], kg[4 * hc + 1], kg[4 * hc + 2], kg[4 * hc + 3]);
+                    *reinterpret_cast<float4 *>(sm + S1_OPA + atom * 16384 + sw128_off(64 + r, cc)) =
+                        make_float4(qg[4 * hc], qg[4 * hc + 1], qg[4 * hc + 2], qg[4 * hc + 3]);
+                    *reinterpret_cast<float4 *>(sm + S1_OPB + atom * 8192 + sw128_off(r, cc)) =
+                        make_float4(kh[4 * hc], kh[4 * hc + 1], kh[4 * hc + 2], kh[4 * hc + 3]);
+                }
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+
+        const int next = task + gridDim.x;
+        float *As = reinterpret_cast<float *>(sm + S1_AS);
+        if (!slow) {
+            // ---- A and P: one tf32 MMA, M = 128 ([K e^g ; Q e^g]), N = 64 (K e^-g)
+            if (tid == 0) {
+                fence_after_sync();
+                const uint32_t oa = smem_addr(sm + S1_OPA), ob = smem_addr(sm + S1_OPB);
+                const uint32_t id = idesc(128, 64, FMT_TF32, FMT_TF32, 0, 0);
+#pragma unroll
+                for (int s2 = 0; s2 < 16; ++s2) {
+                    const uint32_t atom = s2 >> 2, wi = (s2 & 3) * 32;
+                    mma_tf32(tmem + AP_COL, sdesc_k_sw128(oa + atom * 16384 + wi),
+                             sdesc_k_sw128(ob + atom * 8192 + wi), id, s2 > 0);
+                }
+                mma_commit(&mbar[1]);
+                if (next < ntask) issue_tma(next);   // staging is free
+            }
+            ok = __syncthreads_and(mbar_wait(&mbar[1], ap_it & 1));
+            ++ap_it;
+            fence_after_sync();
+            if (!ok) break;
+            if (warp < 4) {   // lane = row: rows 0-63 hold A / beta, 64-127 hold P
+                const int row = tid;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float d[16];
+                    tmem_ld16(tmem_at(tmem, warp, AP_COL + 16 * q4), d);
+                    tmem_wait_ld();
+                    if (row < 64) {
+                        const float b = sB[row];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int i = 16 * q4 + e;
+                            As[row * TP + i] = row > i ? b * d[e] : 0.f;
+                        }
+                    } else {
+                        const int r = row - 64;
+                        float pv[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) pv[e] = (16 * q4 + e) <= r ? d[e] : 0.f;
+                        *reinterpret_cast<uint4 *>(out + IMG_P + sw128_off(r, 2 * q4)) = pack8_h(pv);
+                        *reinterpret_cast<uint4 *>(out + IMG_P + sw128_off(r, 2 * q4 + 1)) = pack8_h(pv + 8);
                     }
                 }
             }
+        } else {
+            // ---- exact pairwise path for chunks whose decay leaves fp32 range
+            const __nv_bfloat16 *Kb = reinterpret_cast<const __nv_bfloat16 *>(sm + S1_STG_K);
+            const __nv_bfloat16 *Qb = reinterpret_cast<const __nv_bfloat16 *>(sm + S1_STG_Q);
+            const float *Gm = reinterpret_cast<const float *>(sm + S1_STG_G);
+            for (int e = tid; e < C * C; e += K1_THREADS) {
+                const int r = e >> 6, i = e & 63;
+                float a = 0.f, pp = 0.f;
+                if (i <= r && r < L) {
+                    for (int c = 0; c < D; ++c) {
+                        const float ki = __bfloat162float(Kb[i * 128 + c]) *
+                                         __expf(Gm[r * 128 + c] - Gm[i * 128 + c]);
+                        a += __bfloat162float(Kb[r * 128 + c]) * ki;
+                        pp += __bfloat162float(Qb[r * 128 + c]) * ki;
+                    }
+                }
+                As[r * TP + i] = i < r ? sB[r] * a : 0.f;
+                *reinterpret_cast<__half *>(out + IMG_P + sw128_off(r, i >> 3) + (i & 7) * 2) =
+                    __float2half_rn(pp);
+            }
+            __syncthreads();
+            if (tid == 0 && next < ntask) issue_tma(next);
         }
         __syncthreads();
 
         // ---- T = (I + A)^-1: 16x16 diagonal blocks, then block levels ---------
+        float *Ts = reinterpret_cast<float *>(sm + S1_TS);
         if (tid < 64) {
             const int R = tid >> 4, j = tid & 15;
             float t[16];
@@ -334,36 +431,36 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const K1Params p) 
 #pragma unroll
             for (int m = 1; m < 16; ++m) {
                 if (m > j) {
-                    float s = 0.f;
+                    float s2 = 0.f;
 #pragma unroll
                     for (int i2 = 0; i2 < m; ++i2)
-                        if (i2 >= j) s += As[(16 * R + m) * TP + 16 * R + i2] * t[i2];
-                    t[m] = -s;
+                        if (i2 >= j) s2 += As[(16 * R + m) * TP + 16 * R + i2] * t[i2];
+                    t[m] = -s2;
                 }
             }
 #pragma unroll
             for (int m = 0; m < 16; ++m) Ts[(16 * R + m) * TP + 16 * R + j] = t[m];
         }
         __syncthreads();
-        float *Ysc = reinterpret_cast<float *>(sm + S1_XT0);   // [3][16][17]
+        float *Ysc = reinterpret_cast<float *>(sm + S1_Y);
         for (int d = 1; d < 4; ++d) {
             const int nb = 4 - d;
             for (int e = tid; e < nb * 256; e += K1_THREADS) {
-                const int b = e >> 8, m = (e >> 4) & 15, nn = e & 15;
-                const int R = d + b, I = R - d;
-                float s = 0.f;
+                const int bI = e >> 8, m = (e >> 4) & 15, nn = e & 15;
+                const int R = d + bI, I = R - d;
+                float s2 = 0.f;
                 for (int kx = 0; kx < 16 * d; ++kx)
-                    s += As[(16 * R + m) * TP + 16 * I + kx] * Ts[(16 * I + kx) * TP + 16 * I + nn];
-                Ysc[b * 272 + m * 17 + nn] = s;
+                    s2 += As[(16 * R + m) * TP + 16 * I + kx] * Ts[(16 * I + kx) * TP + 16 * I + nn];
+                Ysc[bI * 272 + m * 17 + nn] = s2;
             }
             __syncthreads();
             for (int e = tid; e < nb * 256; e += K1_THREADS) {
-                const int b = e >> 8, m = (e >> 4) & 15, nn = e & 15;
-                const int R = d + b, I = R - d;
-                float s = 0.f;
+                const int bI = e >> 8, m = (e >> 4) & 15, nn = e & 15;
+                const int R = d + bI, I = R - d;
+                float s2 = 0.f;
                 for (int kx = 0; kx <= m; ++kx)
-                    s += Ts[(16 * R + m) * TP + 16 * R + kx] * Ysc[b * 272 + kx * 17 + nn];
-                Ts[(16 * R + m) * TP + 16 * I + nn] = -s;
+                    s2 += Ts[(16 * R + m) * TP + 16 * R + kx] * Ysc[bI * 272 + kx * 17 + nn];
+                Ts[(16 * R + m) * TP + 16 * I + nn] = -s2;
             }
             __syncthreads();
         }
@@ -372,44 +469,38 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const K1Params p) 
             const int r = tid >> 2, i0 = (tid & 3) * 16;
 #pragma unroll
             for (int hc = 0; hc < 2; ++hc) {
-                uint32_t w4[4];
+                float tv[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = i0 + hc * 8 + 2 * e;
-                    const float a0 = i <= r ? Ts[r * TP + i] * sB[i] : 0.f;
-                    const float a1 = i + 1 <= r ? Ts[r * TP + i + 1] * sB[i + 1] : 0.f;
-                    w4[e] = pack_h2(a0, a1);
+                for (int e = 0; e < 8; ++e) {
+                    const int i = i0 + hc * 8 + e;
+                    tv[e] = i <= r ? Ts[r * TP + i] * sB[i] : 0.f;
                 }
-                *reinterpret_cast<uint4 *>(sm + S1_TP + sw128_off(r, (i0 >> 3) + hc)) =
-                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                *reinterpret_cast<uint4 *>(sm + S1_TP + sw128_off(r, (i0 >> 3) + hc)) = pack8_h(tv);
             }
         }
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
 
-        // ---- W = T' (K e^gamma), U~ = T' V on tcgen05 (fp16) -----------------
+        // ---- W = T' (K e^g), U~ = T' V on tcgen05 (fp16, B operands MN-major) --
         if (tid == 0) {
             fence_after_sync();
-            const uint32_t tp = smem_addr(sm + S1_TP), kg = smem_addr(sm + S1_KGT),
-                           vo = smem_addr(sm + S1_VOP);
-            const uint32_t id_w = idesc(64, 128, FMT_F16, FMT_F16, 0, 0);
-            const uint32_t id_u = idesc(64, 128, FMT_F16, FMT_F16, 0, 1);
+            const uint32_t tpa = smem_addr(sm + S1_TP), kga = smem_addr(sm + S1_KG16),
+                           va = smem_addr(sm + S1_V16);
+            const uint32_t id = idesc(64, 128, FMT_F16, FMT_F16, 0, 1);
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t a = sdesc_k_sw128(tp + 32 * s);
-                mma_f16(tmem + W_COL, a, sdesc_k_sw128(kg + 32 * s), id_w, s > 0);
-                mma_f16(tmem + U_COL, a, sdesc(vo + 2048 * s, 8192, 1024, LAYOUT_SW128), id_u, s > 0);
+            for (int s2 = 0; s2 < 4; ++s2) {
+                const uint64_t a = sdesc_k_sw128(tpa + 32 * s2);
+                mma_f16(tmem + W_COL, a, sdesc(kga + 2048 * s2, 8192, 1024, LAYOUT_SW128), id, s2 > 0);
+                mma_f16(tmem + U_COL, a, sdesc(va + 2048 * s2, 8192, 1024, LAYOUT_SW128), id, s2 > 0);
             }
             mma_commit(&mbar[2]);
         }
-        ok = __syncthreads_and(ok && mbar_wait(&mbar[2], iter & 1));
+        ok = __syncthreads_and(mbar_wait(&mbar[2], it & 1));
         fence_after_sync();
         if (!ok) break;
 
-        // ---- epilogue: W image, U~ slices, then bulk copies to the workspace --
-        uint8_t *wimg = sm + S1_KH0;   // As no longer needed
-        uint8_t *uimg = sm + S1_KH1;   // Ts no longer needed
+        // ---- epilogue: W image and U~ slices (rows r = 16 w + lane, lane < 16)
         if (warp < 4) {
             const int r = 16 * warp + lane;
             for (int cb = 0; cb < 8; ++cb) {
@@ -421,33 +512,16 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const K1Params p) 
 #pragma unroll
                     for (int hc = 0; hc < 2; ++hc) {
                         const int c0 = 16 * cb + 8 * hc;
-                        uint4 pw = make_uint4(pack_h2(w[8 * hc + 0], w[8 * hc + 1]), pack_h2(w[8 * hc + 2], w[8 * hc + 3]),
-                                              pack_h2(w[8 * hc + 4], w[8 * hc + 5]), pack_h2(w[8 * hc + 6], w[8 * hc + 7]));
-                        uint4 pu = make_uint4(pack_h2(u[8 * hc + 0], u[8 * hc + 1]), pack_h2(u[8 * hc + 2], u[8 * hc + 3]),
-                                              pack_h2(u[8 * hc + 4], u[8 * hc + 5]), pack_h2(u[8 * hc + 6], u[8 * hc + 7]));
-                        *reinterpret_cast<uint4 *>(wimg + (c0 >> 6) * 8192 + sw128_off(r, (c0 & 63) >> 3)) = pw;
-                        *reinterpret_cast<uint4 *>(uimg + (c0 >> 5) * 4096 + r * 64 + (c0 & 31) * 2) = pu;
+                        *reinterpret_cast<uint4 *>(out + IMG_W + rc_img_off(r, c0)) = pack8_h(w + 8 * hc);
+                        *reinterpret_cast<uint4 *>(out + IMG_U + (c0 >> 5) * 4096 + r * 64 + (c0 & 31) * 2) =
+                            pack8_h(u + 8 * hc);
                     }
                 }
             }
+        } else if (tid >= 128) {
+            reinterpret_cast<float *>(out + IMG_G)[tid - 128] = eL[tid - 128];
         }
-        fence_async_smem();
         fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            struct { uint32_t dst, src, bytes; } cp[6] = {
-                {IMG_W, 0u, 16384u}, {IMG_Q, 0u, 16384u}, {IMG_KT, 0u, 16384u},
-                {IMG_P, 0u, 8192u}, {IMG_U, 0u, 16384u}, {IMG_G, 0u, 512u}};
-            const uint8_t *srcs[6] = {wimg, sm + S1_QIMG, sm + S1_KTIMG, sm + S1_PIMG, uimg,
-                                      reinterpret_cast<uint8_t *>(sGL)};
-            for (int e = 0; e < 6; ++e) {
-                asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                             :: "l"(out + cp[e].dst), "r"(smem_addr(srcs[e])), "r"(cp[e].bytes)
-                             : "memory");
-            }
-            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-        }
         __syncthreads();
     }
     if (!ok && tid == 0) ws_fail(ws_hdr, 1);
@@ -558,7 +632,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
 
     const uint32_t sop = smem_addr(sm + S2_SOP), uop = smem_addr(sm + S2_UOP);
     const uint32_t id64 = idesc(64, DVS, FMT_F16, FMT_F16, 0, 1);
-    const uint32_t id128 = idesc(128, DVS, FMT_F16, FMT_F16, 0, 1);
+    const uint32_t id128 = idesc(128, DVS, FMT_F16, FMT_F16, 1, 1);
     bool ok = true;
     for (int ch = a; ch < b && ok; ++ch) {
         const int i = ch - a, stage = i & 1;
@@ -627,7 +701,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const uint64_t bdesc = sdesc(uop + 256 * s, 128, 1024, LAYOUT_NONE);
-                mma_f16(tmem + D2_COL, sdesc_k_sw128(kta + 32 * s), bdesc, id128, s > 0);
+                mma_f16(tmem + D2_COL, sdesc(kta + 2048 * s, 8192, 1024, LAYOUT_SW128), bdesc, id128, s > 0);
                 mma_f16(tmem + D1_COL, sdesc_k_sw128(pa + 32 * s), bdesc, id64, 1);
             }
             mma_commit(&mbar[2]);
@@ -682,6 +756,33 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     if (warp == 0) tmem_dealloc<128>(tmem);
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 3D map over a token-major [T][H][128] tensor; one box = 64 tokens of one head.
+bool token_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, uint32_t esize, int H,
+               int64_t T) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)D * esize, (cuuint64_t)H * D * esize};
+    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)C};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
     static int cached = 0;
     if (!cached) {
@@ -719,17 +820,25 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, void *workspace, cudaStream_
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int nsm = sm_count();
+    K1Params p1;
+    if (a.T > 0) {
+        if (!token_map(&p1.tm_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.H, a.T) ||
+            !token_map(&p1.tm_k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.H, a.T) ||
+            !token_map(&p1.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.H, a.T) ||
+            !token_map(&p1.tm_g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.H, a.T))
+            return cudaErrorInvalidValue;
+    }
+    p1.beta = a.beta; p1.cu = a.cu_seqlens; p1.ws = ws; p1.N = a.N; p1.H = a.H; p1.T = a.T;
     for (int64_t w0 = 0; w0 < bound; w0 += WINDOW_CHUNKS) {
         const int64_t w1 = w0 + WINDOW_CHUNKS;
-        K1Params p1;
-        p1.q = (const __nv_bfloat16 *)a.q; p1.k = (const __nv_bfloat16 *)a.k;
-        p1.v = (const __nv_bfloat16 *)a.v; p1.g = a.g; p1.beta = a.beta; p1.cu = a.cu_seqlens;
-        p1.ws = ws; p1.N = a.N; p1.H = a.H; p1.T = a.T; p1.w0 = (int)w0; p1.w1 = (int)w1;
-        const int64_t tasks = (w1 - w0) * a.H;
-        const int g1 = (int)(tasks < nsm ? tasks : nsm);
-        intra_kernel<<<g1, K1_THREADS, S1_BYTES, st>>>(p1);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        p1.w0 = (int)w0; p1.w1 = (int)w1;
+        if (a.T > 0) {
+            const int64_t tasks = (w1 - w0) * a.H;
+            const int g1 = (int)(tasks < nsm ? tasks : nsm);
+            intra_kernel<<<g1, K1_THREADS, S1_BYTES, st>>>(p1);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
         K2Params p2;
         p2.S0 = a.S0; p2.S_T = a.S_T; p2.o = (__nv_bfloat16 *)a.o; p2.cu = a.cu_seqlens;
         p2.ws = ws; p2.N = a.N; p2.H = a.H; p2.T = a.T; p2.w0 = (int)w0; p2.w1 = (int)w1;
