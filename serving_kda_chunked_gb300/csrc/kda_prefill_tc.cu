@@ -150,7 +150,7 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 //   5. T = (I + A)^-1 on CUDA cores (fp32; 16 x 16 diagonal blocks, then
 //      three block levels), T' = T Diag(beta) as fp16.
 //   6. W = T' (K e^g), U~ = T' V on tcgen05 (fp16), stored to the workspace.
-constexpr int K1_THREADS = 256;
+constexpr int K1_THREADS = 512;
 constexpr uint32_t S1_STG_K = 0, S1_STG_Q = 16384, S1_STG_V = 32768;  // bf16 [64][128]
 constexpr uint32_t S1_STG_G = 49152;                                  // fp32 [64][128]
 constexpr uint32_t S1_OPA = 81920;    // tf32 [K e^g ; Q e^g]: 4 atoms x 128 rows x 128 B
@@ -159,12 +159,12 @@ constexpr uint32_t S1_KG16 = 180224;  // fp16 K e^g, [r][c] 128B-swizzled (MN-ma
 constexpr uint32_t S1_V16 = 196608;   // fp16 V, same layout
 constexpr uint32_t S1_TP = 212992;    // fp16 T', K-major SW128 [r][i]
 constexpr uint32_t S1_MISC = 221184;
-constexpr uint32_t S1_BYTES = S1_MISC + 2048 + 1024;
+constexpr uint32_t S1_BYTES = S1_MISC + 4096 + 1024;
 // after the A/P MMA has completed the operand area is reused:
 constexpr uint32_t S1_AS = S1_OPA;            // A  fp32 [64][TP]
 constexpr uint32_t S1_TS = S1_OPA + 17408;    // T  fp32 [64][TP]
 constexpr uint32_t S1_Y = S1_OPA + 34816;     // [3][16][17] fp32 scratch
-constexpr int AP_COL = 0, W_COL = 64, U_COL = 192;   // TMEM columns
+constexpr int AP_COL = 0, W_COL = 256, U_COL = 384;  // TMEM: 4 A/P partials of 64, W, U~
 constexpr int TP = 65;                                // padded fp32 row stride
 constexpr float RANGE_LIMIT = 80.f;                   // e^80 stays inside fp32
 
@@ -198,6 +198,42 @@ __device__ __forceinline__ uint32_t rc_img_off(int r, int c0) {
     return (uint32_t)(c0 >> 6) * 8192u + sw128_off(r, (c0 & 63) >> 3);
 }
 
+// One level of the blocked unit-lower-triangular inverse: for every block
+// (R, I = R - d),  T_RI = -T_RR * sum_{J=I}^{R-1} A_RJ T_JI  (16 x 16 blocks).
+template <int d>
+__device__ __forceinline__ void inverse_level(const float *As, float *Ts, float *Ysc, int tid) {
+    constexpr int nb = 4 - d;
+    for (int e = tid; e < nb * 256; e += K1_THREADS) {
+        const int bI = e >> 8, m = (e >> 4) & 15, nn = e & 15;
+        const int R = d + bI, I = R - d;
+        const float *arow = As + (16 * R + m) * TP + 16 * I;
+        const float *tcol = Ts + (16 * I) * TP + 16 * I + nn;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int kx = 0; kx < 16 * d; kx += 4) {
+            s0 += arow[kx] * tcol[kx * TP];
+            s1 += arow[kx + 1] * tcol[(kx + 1) * TP];
+            s2 += arow[kx + 2] * tcol[(kx + 2) * TP];
+            s3 += arow[kx + 3] * tcol[(kx + 3) * TP];
+        }
+        Ysc[bI * 272 + m * 17 + nn] = (s0 + s1) + (s2 + s3);
+    }
+    __syncthreads();
+    for (int e = tid; e < nb * 256; e += K1_THREADS) {
+        const int bI = e >> 8, m = (e >> 4) & 15, nn = e & 15;
+        const int R = d + bI, I = R - d;
+        const float *trow = Ts + (16 * R + m) * TP + 16 * R;
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int kx = 0; kx < 16; kx += 2) {
+            if (kx <= m) s0 += trow[kx] * Ysc[bI * 272 + kx * 17 + nn];
+            if (kx + 1 <= m) s1 += trow[kx + 1] * Ysc[bI * 272 + (kx + 1) * 17 + nn];
+        }
+        Ts[(16 * R + m) * TP + 16 * I + nn] = -(s0 + s1);
+    }
+    __syncthreads();
+}
+
 __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_constant__ K1Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -205,8 +241,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
     float *gL = reinterpret_cast<float *>(sm + S1_MISC);   // [128] gamma_last
     float *eL = gL + 128;                                  // [128] e^gamma_last
     float *sB = eL + 128;                                  // [64] beta
-    float *tot = sB + 64;                                  // [128] half-chunk totals
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(tot + 128);   // [0] TMA, [1] A/P, [2] W/U
+    float *tot = sB + 64;                                  // [4][128] segment totals
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(tot + 512);   // [0] TMA, [1] A/P, [2] W/U
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 3);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -217,8 +253,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
 
     if (tid == 0) {
         mbar_init(&mbar[0], 1);
-        mbar_init(&mbar[1], 1);
-        mbar_init(&mbar[2], 1);
+        mbar_init(&mbar[1], 4);   // four A/P issuers
+        mbar_init(&mbar[2], 2);   // W and U~ issuers
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc<512>(tmem_slot);
@@ -264,28 +300,34 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         if (!ok) break;
 
         // ---- cumulative log-gate, in place (rows past the sequence: g = 0) ----
+        // thread = (channel c, 16-row segment sg)
         {
-            const int c = tid & 127, half = tid >> 7;
+            const int c = tid & 127, sg = tid >> 7;
             float *G = reinterpret_cast<float *>(sm + S1_STG_G);
+            float v[16];
             float acc = 0.f;
-            for (int j = 0; j < 32; ++j) {
-                const int r = 32 * half + j;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int r = 16 * sg + j;
                 acc += r < L ? G[r * 128 + c] : 0.f;
-                G[r * 128 + c] = acc;
+                v[j] = acc;
             }
-            if (half == 0) tot[c] = acc;
+            tot[sg * 128 + c] = acc;
             __syncthreads();
-            if (half == 1) {
-                const float off = tot[c];
-                for (int j = 0; j < 32; ++j) G[(32 + j) * 128 + c] += off;
+            float off = 0.f;
+            for (int s2 = 0; s2 < sg; ++s2) off += tot[s2 * 128 + c];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) G[(16 * sg + j) * 128 + c] = v[j] + off;
+            if (sg == 3) {
                 gL[c] = acc + off;
                 eL[c] = __expf(acc + off);
             }
         }
-        const bool slow = __syncthreads_or(tid >= 128 && -gL[tid & 127] > RANGE_LIMIT);
+        const bool slow = __syncthreads_or(tid >= 384 && -gL[tid & 127] > RANGE_LIMIT);
 
         // ---- element-wise prep: unit = (row r, channels c0..c0+7) -------------
-        for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll 1
+        for (int jj = 0; jj < 2; ++jj) {
             const int u = tid + K1_THREADS * jj;
             const int r = u >> 4, c0 = (u & 15) * 8;
             float kf[8], qf[8], vf[8], gm[8], el[8];
@@ -354,46 +396,52 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         const int next = task + gridDim.x;
         float *As = reinterpret_cast<float *>(sm + S1_AS);
         if (!slow) {
-            // ---- A and P: one tf32 MMA, M = 128 ([K e^g ; Q e^g]), N = 64 (K e^-g)
-            if (tid == 0) {
+            // ---- A and P: tf32 MMAs, M = 128 ([K e^g ; Q e^g]), N = 64 (K e^-g).
+            // Issuing one tcgen05.mma occupies its thread for ~90 cycles, so the
+            // 16 K steps are spread over 4 issuing warps, one accumulator each.
+            if (lane == 0 && warp < 4) {
                 fence_after_sync();
-                const uint32_t oa = smem_addr(sm + S1_OPA), ob = smem_addr(sm + S1_OPB);
+                const uint64_t da = sdesc_k_sw128(smem_addr(sm + S1_OPA));
+                const uint64_t db = sdesc_k_sw128(smem_addr(sm + S1_OPB));
                 const uint32_t id = idesc(128, 64, FMT_TF32, FMT_TF32, 0, 0);
 #pragma unroll
-                for (int s2 = 0; s2 < 16; ++s2) {
-                    const uint32_t atom = s2 >> 2, wi = (s2 & 3) * 32;
-                    mma_tf32(tmem + AP_COL, sdesc_k_sw128(oa + atom * 16384 + wi),
-                             sdesc_k_sw128(ob + atom * 8192 + wi), id, s2 > 0);
+                for (int s2 = 0; s2 < 4; ++s2) {   // channel atom `warp`, 8 tf32 per step
+                    const uint32_t wi = s2 * 32;
+                    mma_tf32(tmem + AP_COL + 64 * warp, sdesc_add(da, warp * 16384 + wi),
+                             sdesc_add(db, warp * 8192 + wi), id, s2 > 0);
                 }
                 mma_commit(&mbar[1]);
-                if (next < ntask) issue_tma(next);   // staging is free
+                if (warp == 0 && next < ntask) issue_tma(next);   // staging is free
             }
             ok = __syncthreads_and(mbar_wait(&mbar[1], ap_it & 1));
             ++ap_it;
             fence_after_sync();
             if (!ok) break;
-            if (warp < 4) {   // lane = row: rows 0-63 hold A / beta, 64-127 hold P
-                const int row = tid;
+            {   // warp = (lane quadrant q, 16-column block cb); lane = row
+                const int q = warp & 3, cb = warp >> 2;
+                const int row = 32 * q + lane;
+                float d[16], d1[16], d2[16], d3[16];
+                tmem_ld16(tmem_at(tmem, q, AP_COL + 16 * cb), d);
+                tmem_ld16(tmem_at(tmem, q, AP_COL + 64 + 16 * cb), d1);
+                tmem_ld16(tmem_at(tmem, q, AP_COL + 128 + 16 * cb), d2);
+                tmem_ld16(tmem_at(tmem, q, AP_COL + 192 + 16 * cb), d3);
+                tmem_wait_ld();
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    float d[16];
-                    tmem_ld16(tmem_at(tmem, warp, AP_COL + 16 * q4), d);
-                    tmem_wait_ld();
-                    if (row < 64) {
-                        const float b = sB[row];
+                for (int e = 0; e < 16; ++e) d[e] = (d[e] + d1[e]) + (d2[e] + d3[e]);
+                if (row < 64) {
+                    const float b = sB[row];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int i = 16 * q4 + e;
-                            As[row * TP + i] = row > i ? b * d[e] : 0.f;
-                        }
-                    } else {
-                        const int r = row - 64;
-                        float pv[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) pv[e] = (16 * q4 + e) <= r ? d[e] : 0.f;
-                        *reinterpret_cast<uint4 *>(out + IMG_P + sw128_off(r, 2 * q4)) = pack8_h(pv);
-                        *reinterpret_cast<uint4 *>(out + IMG_P + sw128_off(r, 2 * q4 + 1)) = pack8_h(pv + 8);
+                    for (int e = 0; e < 16; ++e) {
+                        const int i = 16 * cb + e;
+                        As[row * TP + i] = row > i ? b * d[e] : 0.f;
                     }
+                } else {
+                    const int r = row - 64;
+                    float pv[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) pv[e] = (16 * cb + e) <= r ? d[e] : 0.f;
+                    *reinterpret_cast<uint4 *>(out + IMG_P + sw128_off(r, 2 * cb)) = pack8_h(pv);
+                    *reinterpret_cast<uint4 *>(out + IMG_P + sw128_off(r, 2 * cb + 1)) = pack8_h(pv + 8);
                 }
             }
         } else {
@@ -423,19 +471,22 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
 
         // ---- T = (I + A)^-1: 16x16 diagonal blocks, then block levels ---------
         float *Ts = reinterpret_cast<float *>(sm + S1_TS);
-        if (tid < 64) {
+        if (tid < 64) {   // column j of diagonal block R, by forward substitution
             const int R = tid >> 4, j = tid & 15;
+            const float *Ab = As + (16 * R) * TP + 16 * R;
             float t[16];
 #pragma unroll
             for (int m = 0; m < 16; ++m) t[m] = (m == j) ? 1.f : 0.f;
 #pragma unroll
             for (int m = 1; m < 16; ++m) {
                 if (m > j) {
-                    float s2 = 0.f;
+                    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                    for (int i2 = 0; i2 < m; ++i2)
-                        if (i2 >= j) s2 += As[(16 * R + m) * TP + 16 * R + i2] * t[i2];
-                    t[m] = -s2;
+                    for (int i2 = 0; i2 < m; i2 += 2) {
+                        if (i2 >= j) s0 += Ab[m * TP + i2] * t[i2];
+                        if (i2 + 1 < m && i2 + 1 >= j) s1 += Ab[m * TP + i2 + 1] * t[i2 + 1];
+                    }
+                    t[m] = -(s0 + s1);
                 }
             }
 #pragma unroll
@@ -443,83 +494,64 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         }
         __syncthreads();
         float *Ysc = reinterpret_cast<float *>(sm + S1_Y);
-        for (int d = 1; d < 4; ++d) {
-            const int nb = 4 - d;
-            for (int e = tid; e < nb * 256; e += K1_THREADS) {
-                const int bI = e >> 8, m = (e >> 4) & 15, nn = e & 15;
-                const int R = d + bI, I = R - d;
-                float s2 = 0.f;
-                for (int kx = 0; kx < 16 * d; ++kx)
-                    s2 += As[(16 * R + m) * TP + 16 * I + kx] * Ts[(16 * I + kx) * TP + 16 * I + nn];
-                Ysc[bI * 272 + m * 17 + nn] = s2;
-            }
-            __syncthreads();
-            for (int e = tid; e < nb * 256; e += K1_THREADS) {
-                const int bI = e >> 8, m = (e >> 4) & 15, nn = e & 15;
-                const int R = d + bI, I = R - d;
-                float s2 = 0.f;
-                for (int kx = 0; kx <= m; ++kx)
-                    s2 += Ts[(16 * R + m) * TP + 16 * R + kx] * Ysc[bI * 272 + kx * 17 + nn];
-                Ts[(16 * R + m) * TP + 16 * I + nn] = -s2;
-            }
-            __syncthreads();
-        }
+        inverse_level<1>(As, Ts, Ysc, tid);
+        inverse_level<2>(As, Ts, Ysc, tid);
+        inverse_level<3>(As, Ts, Ysc, tid);
         // T' = T Diag(beta) as an fp16 K-major SW128 image (row r, 64 columns)
         {
-            const int r = tid >> 2, i0 = (tid & 3) * 16;
+            const int r = tid >> 3, i0 = (tid & 7) * 8;
+            float tv[8];
 #pragma unroll
-            for (int hc = 0; hc < 2; ++hc) {
-                float tv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int i = i0 + hc * 8 + e;
-                    tv[e] = i <= r ? Ts[r * TP + i] * sB[i] : 0.f;
-                }
-                *reinterpret_cast<uint4 *>(sm + S1_TP + sw128_off(r, (i0 >> 3) + hc)) = pack8_h(tv);
+            for (int e = 0; e < 8; ++e) {
+                const int i = i0 + e;
+                tv[e] = i <= r ? Ts[r * TP + i] * sB[i] : 0.f;
             }
+            *reinterpret_cast<uint4 *>(sm + S1_TP + sw128_off(r, i0 >> 3)) = pack8_h(tv);
         }
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
 
-        // ---- W = T' (K e^g), U~ = T' V on tcgen05 (fp16, B operands MN-major) --
-        if (tid == 0) {
+        // ---- W = T' (K e^g), U~ = T' V on tcgen05 (fp16, B operands MN-major);
+        // warp 0 issues W, warp 1 issues U~
+        if (lane == 0 && warp < 2) {
             fence_after_sync();
-            const uint32_t tpa = smem_addr(sm + S1_TP), kga = smem_addr(sm + S1_KG16),
-                           va = smem_addr(sm + S1_V16);
+            const uint64_t dt = sdesc_k_sw128(smem_addr(sm + S1_TP));
+            const uint64_t db = sdesc(smem_addr(sm + (warp == 0 ? S1_KG16 : S1_V16)), 8192, 1024,
+                                      LAYOUT_SW128);
             const uint32_t id = idesc(64, 128, FMT_F16, FMT_F16, 0, 1);
+            const uint32_t col = warp == 0 ? W_COL : U_COL;
 #pragma unroll
-            for (int s2 = 0; s2 < 4; ++s2) {
-                const uint64_t a = sdesc_k_sw128(tpa + 32 * s2);
-                mma_f16(tmem + W_COL, a, sdesc(kga + 2048 * s2, 8192, 1024, LAYOUT_SW128), id, s2 > 0);
-                mma_f16(tmem + U_COL, a, sdesc(va + 2048 * s2, 8192, 1024, LAYOUT_SW128), id, s2 > 0);
-            }
+            for (int s2 = 0; s2 < 4; ++s2)
+                mma_f16(tmem + col, sdesc_add(dt, 32 * s2), sdesc_add(db, 2048 * s2), id, s2 > 0);
             mma_commit(&mbar[2]);
         }
         ok = __syncthreads_and(mbar_wait(&mbar[2], it & 1));
         fence_after_sync();
         if (!ok) break;
 
-        // ---- epilogue: W image and U~ slices (rows r = 16 w + lane, lane < 16)
-        if (warp < 4) {
-            const int r = 16 * warp + lane;
-            for (int cb = 0; cb < 8; ++cb) {
+        // ---- epilogue: warp = (quadrant q, 32-column block cb); rows 16q + lane
+        {
+            const int q = warp & 3, cb = warp >> 2;
+            const int r = 16 * q + lane;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int col = 32 * cb + 16 * hh;
                 float w[16], u[16];
-                tmem_ld16(tmem_at(tmem, warp, W_COL + 16 * cb), w);
-                tmem_ld16(tmem_at(tmem, warp, U_COL + 16 * cb), u);
+                tmem_ld16(tmem_at(tmem, q, W_COL + col), w);
+                tmem_ld16(tmem_at(tmem, q, U_COL + col), u);
                 tmem_wait_ld();
                 if (lane < 16) {
 #pragma unroll
                     for (int hc = 0; hc < 2; ++hc) {
-                        const int c0 = 16 * cb + 8 * hc;
+                        const int c0 = col + 8 * hc;
                         *reinterpret_cast<uint4 *>(out + IMG_W + rc_img_off(r, c0)) = pack8_h(w + 8 * hc);
                         *reinterpret_cast<uint4 *>(out + IMG_U + (c0 >> 5) * 4096 + r * 64 + (c0 & 31) * 2) =
                             pack8_h(u + 8 * hc);
                     }
                 }
             }
-        } else if (tid >= 128) {
-            reinterpret_cast<float *>(out + IMG_G)[tid - 128] = eL[tid - 128];
+            if (tid < 128) reinterpret_cast<float *>(out + IMG_G)[tid] = eL[tid];
         }
         fence_before_sync();
         __syncthreads();
@@ -533,15 +565,31 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
 // ------------------------------------------------------------------------------
 // K2: chain kernel
 // ------------------------------------------------------------------------------
+// One CTA of 128 threads per (sequence, head, block of 32 state columns);
+// thread t owns row t (a dk channel) of the fp32 state.  Per chunk:
+//   round 1: D_A + D_B = [W ; Q^] S   (M = 128: rows 0-63 W S, 64-127 Q^ S;
+//            K steps 0-3 into D_A by warp 0, 4-7 into D_B by warp 1)
+//   U = U~ - W S (fp16);
+//   round 2: D_S + D_S2 = Kbar^T U (warps 0 and 1, two K steps each),
+//            D_A += [0 ; P] U (warp 2; rows 64-127 then hold O - Q^S_B)
+//   S = Diag(e^gamma_last) S + D_S + D_S2.
+// A thread issuing tcgen05.mma is busy for ~90 cycles per instruction, so the
+// few MMAs on the state's critical path are spread over several issuing warps.
+// TMEM accumulators alternate between two sets so that the outputs of chunk
+// i are read while the MMAs of chunk i + 1 run.
 constexpr int K2_THREADS = 128;
-constexpr uint32_t S2_STAGE = 65536;                      // bytes per stage
-constexpr uint32_t S2_W = 0, S2_Q = 16384, S2_KT = 32768, S2_P = 49152, S2_U = 57344, S2_G = 61440;
+constexpr uint32_t S2_WQ = 0;          // [W ; Q^] K-major SW128, 2 atoms x 128 rows
+constexpr uint32_t S2_KB = 32768;      // Kbar [r][c] SW128 (MN-major A)
+constexpr uint32_t S2_PZ = 49152;      // [0 ; P] K-major SW128, 128 rows (rows 0-63 zero)
+constexpr uint32_t S2_U = 65536;       // U~ slice [64][32] fp16
+constexpr uint32_t S2_G = 69632;       // e^gamma_last [128] fp32
+constexpr uint32_t S2_STAGE = 70656;   // bytes per stage (multiple of 1024)
 constexpr uint32_t S2_SOP = 2 * S2_STAGE;                 // S fp16, K=128 x N=32, MN-major
 constexpr uint32_t S2_UOP = S2_SOP + 8192;                // U fp16, K=64 x N=32, MN-major
 constexpr uint32_t S2_MISC = S2_UOP + 4096;
 constexpr uint32_t S2_BYTES = S2_MISC + 256 + 1024;
-constexpr uint32_t S2_TX = 16384 * 3 + 8192 + 4096 + 512; // bytes landing per stage
-constexpr int D0_COL = 0, D1_COL = 32, D2_COL = 64;       // TMEM: W S, O, Kb^T U
+constexpr uint32_t S2_TX = 4 * 8192 + 16384 + 8192 + 4096 + 512;   // bytes landing per stage
+// TMEM set s (0, 1) at column 128 s: D_A +0, D_B +32, D_S +64, D_S2 +96
 
 struct K2Params {
     const float *S0;
@@ -558,8 +606,8 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + S2_MISC);   // [0..1] loads, [2] mma
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 3);
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + S2_MISC);   // [0..1] loads, [2] r1, [3] r2
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H;
@@ -589,7 +637,6 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     int64_t bos, eos;
     seq_bounds(p.cu, n, p.T, bos, eos);
 
-    // state row `tid` (dk index), DVS columns, fp32
     float S[DVS];
     {
         const float *src = (a == cb) ? p.S0 : p.S_T;
@@ -600,14 +647,20 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
             S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
         }
     }
-
+    // the zero half of [0 ; P] in both stages
+    for (int e = tid; e < 2 * 8192 / 16; e += K2_THREADS) {
+        const int st = e / 512, off = (e % 512) * 16;
+        *reinterpret_cast<uint4 *>(sm + st * S2_STAGE + S2_PZ + off) = make_uint4(0u, 0u, 0u, 0u);
+    }
     if (tid == 0) {
         mbar_init(&mbar[0], 1);
         mbar_init(&mbar[1], 1);
-        mbar_init(&mbar[2], 1);
+        mbar_init(&mbar[2], 2);   // round 1: two issuers
+        mbar_init(&mbar[3], 3);   // round 2: three issuers
         mbar_fence_init();
     }
-    if (warp == 0) tmem_alloc<128>(tmem_slot);
+    if (warp == 0) tmem_alloc<256>(tmem_slot);
+    fence_async_smem();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -618,10 +671,12 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
         uint8_t *dst = sm + stage * S2_STAGE;
         uint64_t *mb = &mbar[stage];
         mbar_arrive_expect_tx(mb, S2_TX);
-        bulk_g2s(dst + S2_W, src + IMG_W, 16384, mb);
-        bulk_g2s(dst + S2_Q, src + IMG_Q, 16384, mb);
-        bulk_g2s(dst + S2_KT, src + IMG_KT, 16384, mb);
-        bulk_g2s(dst + S2_P, src + IMG_P, 8192, mb);
+        bulk_g2s(dst + S2_WQ, src + IMG_W, 8192, mb);              // W, k 0-63
+        bulk_g2s(dst + S2_WQ + 8192, src + IMG_Q, 8192, mb);       // Q^, k 0-63
+        bulk_g2s(dst + S2_WQ + 16384, src + IMG_W + 8192, 8192, mb);
+        bulk_g2s(dst + S2_WQ + 24576, src + IMG_Q + 8192, 8192, mb);
+        bulk_g2s(dst + S2_KB, src + IMG_KT, 16384, mb);
+        bulk_g2s(dst + S2_PZ + 8192, src + IMG_P, 8192, mb);
         bulk_g2s(dst + S2_U, src + IMG_U + slice * 4096, 4096, mb);
         bulk_g2s(dst + S2_G, src + IMG_G, 512, mb);
     };
@@ -630,13 +685,47 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
         if (a + 1 < b) issue_loads(a + 1, 1);
     }
 
-    const uint32_t sop = smem_addr(sm + S2_SOP), uop = smem_addr(sm + S2_UOP);
-    const uint32_t id64 = idesc(64, DVS, FMT_F16, FMT_F16, 0, 1);
-    const uint32_t id128 = idesc(128, DVS, FMT_F16, FMT_F16, 1, 1);
+    const uint64_t d_sop = sdesc(smem_addr(sm + S2_SOP), 128, 2048, LAYOUT_NONE);
+    const uint64_t d_uop = sdesc(smem_addr(sm + S2_UOP), 128, 1024, LAYOUT_NONE);
+    const uint32_t id_wq = idesc(128, DVS, FMT_F16, FMT_F16, 0, 1);
+    const uint32_t id_kb = idesc(128, DVS, FMT_F16, FMT_F16, 1, 1);
+
+    // stores the O rows of a finished chunk (threads 64-127: row tid - 64)
+    auto store_o = [&](int set, int64_t t0, int L) {
+        if (warp >= 2) {
+            float oa[16], ob[16], pa[16], pb[16];
+            tmem_ld16(tmem_at(tmem, warp, 128 * set), oa);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 16), ob);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 32), pa);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 48), pb);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) { oa[j] += pa[j]; ob[j] += pb[j]; }
+            const int r = tid - 64;
+            if (r < L) {
+                __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * D + slice * DVS;
+#pragma unroll
+                for (int gq = 0; gq < DVS / 8; ++gq) {
+                    const float *src = gq < 2 ? oa + 8 * gq : ob + 8 * (gq - 2);
+                    __nv_bfloat162 b0 = __floats2bfloat162_rn(src[0], src[1]);
+                    __nv_bfloat162 b1 = __floats2bfloat162_rn(src[2], src[3]);
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(src[4], src[5]);
+                    __nv_bfloat162 b3 = __floats2bfloat162_rn(src[6], src[7]);
+                    *reinterpret_cast<uint4 *>(dst + 8 * gq) = make_uint4(
+                        *reinterpret_cast<uint32_t *>(&b0), *reinterpret_cast<uint32_t *>(&b1),
+                        *reinterpret_cast<uint32_t *>(&b2), *reinterpret_cast<uint32_t *>(&b3));
+                }
+            }
+        }
+    };
+
     bool ok = true;
-    for (int ch = a; ch < b && ok; ++ch) {
-        const int i = ch - a, stage = i & 1;
+    int64_t prev_t0 = 0;
+    int prev_L = 0;
+    for (int ch = a; ch < b; ++ch) {
+        const int i = ch - a, stage = i & 1, set = i & 1;
         uint8_t *st = sm + stage * S2_STAGE;
+        const uint32_t tset = tmem + 128 * set;
         const int64_t t0 = bos + (int64_t)(ch - cb) * C;
         const int L = (int)((eos - t0) < C ? (eos - t0) : C);
         ok = __syncthreads_and(mbar_wait(&mbar[stage], (i >> 1) & 1));
@@ -653,99 +742,90 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
-        if (tid == 0) {
+        if (lane == 0 && warp < 2) {      // round 1: warp w takes K atom w
             fence_after_sync();
-            const uint32_t wa = smem_addr(st + S2_W), qa = smem_addr(st + S2_Q);
+            const uint64_t dwq = sdesc_k_sw128(smem_addr(st + S2_WQ));
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t ko = (s >> 2) * 8192 + (s & 3) * 32;
-                const uint64_t bdesc = sdesc(sop + 256 * s, 128, 2048, LAYOUT_NONE);
-                mma_f16(tmem + D0_COL, sdesc_k_sw128(wa + ko), bdesc, id64, s > 0);
-                mma_f16(tmem + D1_COL, sdesc_k_sw128(qa + ko), bdesc, id64, s > 0);
-            }
+            for (int s = 0; s < 4; ++s)
+                mma_f16(tset + 32 * warp, sdesc_add(dwq, warp * 16384 + s * 32),
+                        sdesc_add(d_sop, 256 * (4 * warp + s)), id_wq, s > 0);
             mma_commit(&mbar[2]);
         }
-        ok = __syncthreads_and(mbar_wait(&mbar[2], 0));
+        if (i > 0) store_o(set ^ 1, prev_t0, prev_L);     // previous chunk's outputs
+        ok = __syncthreads_and(mbar_wait(&mbar[2], i & 1));
         fence_after_sync();
         if (!ok) break;
 
-        // U = U~ - W S for token row r (M = 64 layout: lanes 0-15 of each quadrant)
-        {
-            float ws0[16], ws1[16];
-            tmem_ld16(tmem_at(tmem, warp, D0_COL), ws0);
-            tmem_ld16(tmem_at(tmem, warp, D0_COL + 16), ws1);
+        // U = U~ - W S for token rows 0-63 (threads 0-63)
+        if (warp < 2) {
+            float w0[16], w1[16], x0[16], x1[16];
+            tmem_ld16(tmem_at(tmem, warp, 128 * set), w0);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 16), w1);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 32), x0);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 48), x1);
             tmem_wait_ld();
-            if (lane < 16) {
-                const int r = 16 * warp + lane;
-                const __half *ut = reinterpret_cast<const __half *>(st + S2_U) + r * DVS;
-                float u[DVS];
+            const int r = tid;
+            const __half *ut = reinterpret_cast<const __half *>(st + S2_U) + r * DVS;
+            float u[DVS];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    u[j] = __half2float(ut[j]) - ws0[j];
-                    u[16 + j] = __half2float(ut[16 + j]) - ws1[j];
-                }
+            for (int j = 0; j < 16; ++j) {
+                u[j] = __half2float(ut[j]) - (w0[j] + x0[j]);
+                u[16 + j] = __half2float(ut[16 + j]) - (w1[j] + x1[j]);
+            }
 #pragma unroll
-                for (int gq = 0; gq < DVS / 8; ++gq) {
-                    uint4 v4 = make_uint4(pack_h2(u[8 * gq + 0], u[8 * gq + 1]), pack_h2(u[8 * gq + 2], u[8 * gq + 3]),
-                                          pack_h2(u[8 * gq + 4], u[8 * gq + 5]), pack_h2(u[8 * gq + 6], u[8 * gq + 7]));
-                    *reinterpret_cast<uint4 *>(sm + S2_UOP + gq * 1024 + (r >> 3) * 128 + (r & 7) * 16) = v4;
-                }
+            for (int gq = 0; gq < DVS / 8; ++gq) {
+                uint4 v4 = make_uint4(pack_h2(u[8 * gq + 0], u[8 * gq + 1]), pack_h2(u[8 * gq + 2], u[8 * gq + 3]),
+                                      pack_h2(u[8 * gq + 4], u[8 * gq + 5]), pack_h2(u[8 * gq + 6], u[8 * gq + 7]));
+                *reinterpret_cast<uint4 *>(sm + S2_UOP + gq * 1024 + (r >> 3) * 128 + (r & 7) * 16) = v4;
             }
         }
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
-        if (tid == 0) {
+        if (lane == 0 && warp < 3) {      // round 2: warps 0-1 Kbar^T U halves, warp 2 P U
             fence_after_sync();
-            const uint32_t kta = smem_addr(st + S2_KT), pa = smem_addr(st + S2_P);
+            if (warp < 2) {
+                const uint64_t dkb = sdesc(smem_addr(st + S2_KB), 8192, 1024, LAYOUT_SW128);
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t bdesc = sdesc(uop + 256 * s, 128, 1024, LAYOUT_NONE);
-                mma_f16(tmem + D2_COL, sdesc(kta + 2048 * s, 8192, 1024, LAYOUT_SW128), bdesc, id128, s > 0);
-                mma_f16(tmem + D1_COL, sdesc_k_sw128(pa + 32 * s), bdesc, id64, 1);
+                for (int s = 0; s < 2; ++s) {
+                    const int ks = 2 * warp + s;
+                    mma_f16(tset + 64 + 32 * warp, sdesc_add(dkb, 2048 * ks),
+                            sdesc_add(d_uop, 256 * ks), id_kb, s > 0);
+                }
+            } else {
+                const uint64_t dpz = sdesc_k_sw128(smem_addr(st + S2_PZ));
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_f16(tset, sdesc_add(dpz, 32 * s), sdesc_add(d_uop, 256 * s), id_wq, 1);
             }
-            mma_commit(&mbar[2]);
+            mma_commit(&mbar[3]);
         }
-        ok = __syncthreads_and(mbar_wait(&mbar[2], 1));
+        ok = __syncthreads_and(mbar_wait(&mbar[3], i & 1));
         fence_after_sync();
         if (!ok) break;
 
-        // S = Diag(e^gamma_last) S + Kb^T U;  O rows -> o
+        // S = Diag(e^gamma_last) S + Kbar^T U
         {
-            float d2a[16], d2b[16], oa[16], ob[16];
-            tmem_ld16(tmem_at(tmem, warp, D2_COL), d2a);
-            tmem_ld16(tmem_at(tmem, warp, D2_COL + 16), d2b);
-            tmem_ld16(tmem_at(tmem, warp, D1_COL), oa);
-            tmem_ld16(tmem_at(tmem, warp, D1_COL + 16), ob);
+            float d2a[16], d2b[16], d3a[16], d3b[16];
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 64), d2a);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 80), d2b);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 96), d3a);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 112), d3b);
             tmem_wait_ld();
             const float gl = reinterpret_cast<const float *>(st + S2_G)[tid];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                S[j] = gl * S[j] + d2a[j];
-                S[16 + j] = gl * S[16 + j] + d2b[j];
-            }
-            if (lane < 16) {
-                const int r = 16 * warp + lane;
-                if (r < L) {
-                    __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * D + slice * DVS;
-#pragma unroll
-                    for (int gq = 0; gq < DVS / 8; ++gq) {
-                        const float *src = gq < 2 ? oa + 8 * gq : ob + 8 * (gq - 2);
-                        __nv_bfloat162 b0 = __floats2bfloat162_rn(src[0], src[1]);
-                        __nv_bfloat162 b1 = __floats2bfloat162_rn(src[2], src[3]);
-                        __nv_bfloat162 b2 = __floats2bfloat162_rn(src[4], src[5]);
-                        __nv_bfloat162 b3 = __floats2bfloat162_rn(src[6], src[7]);
-                        uint4 v4 = make_uint4(*reinterpret_cast<uint32_t *>(&b0), *reinterpret_cast<uint32_t *>(&b1),
-                                              *reinterpret_cast<uint32_t *>(&b2), *reinterpret_cast<uint32_t *>(&b3));
-                        *reinterpret_cast<uint4 *>(dst + 8 * gq) = v4;
-                    }
-                }
+                S[j] = gl * S[j] + (d2a[j] + d3a[j]);
+                S[16 + j] = gl * S[16 + j] + (d2b[j] + d3b[j]);
             }
         }
+        prev_t0 = t0;
+        prev_L = L;
         fence_before_sync();
         __syncthreads();   // every thread is done with this stage
         if (tid == 0 && ch + 2 < b) issue_loads(ch + 2, stage);
     }
+    if (ok) store_o((b - 1 - a) & 1, prev_t0, prev_L);
 
     if (!ok && tid == 0) ws_fail(ws_hdr, 2);
 #pragma unroll
@@ -753,7 +833,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
         *reinterpret_cast<float4 *>(p.S_T + sbase + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc<128>(tmem);
+    if (warp == 0) tmem_dealloc<256>(tmem);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {

@@ -41,6 +41,12 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
 __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
     return sdesc(saddr, 16, 1024, LAYOUT_SW128);
 }
+// The same descriptor moved by `bytes` (a multiple of 16): only the start
+// address field changes, and shared addresses stay below 2^18, so the sum
+// never carries out of that 14-bit field.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
+    return desc + (uint64_t)(bytes >> 4);
+}
 __host__ __device__ constexpr uint32_t idesc(uint32_t M, uint32_t N, uint32_t afmt,
                                              uint32_t bfmt, uint32_t a_mn, uint32_t b_mn,
                                              uint32_t neg_a = 0) {
