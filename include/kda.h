@@ -50,7 +50,9 @@ typedef enum kda_status {
     KDA_ERR_INVALID_ARG = 1,  /* null pointer, misalignment, bad size       */
     KDA_ERR_UNSUPPORTED = 2,  /* head size / chunk / dtype not compiled in   */
     KDA_ERR_CUDA = 3,         /* a CUDA launch or attribute call failed      */
-    KDA_ERR_TIMEOUT = 4       /* a bounded device wait gave up (see check) */
+    KDA_ERR_TIMEOUT = 4,      /* a bounded device wait gave up (see check) */
+    KDA_ERR_TOO_LARGE = 5     /* beyond the fixed scratch of the no-allocation
+                                 entry point                                  */
 } kda_status;
 
 typedef enum kda_dtype {
@@ -118,6 +120,45 @@ uint64_t kda_prefill_workspace_size(int32_t N, int64_t T_total, int32_t H,
  * KDA_ERR_CUDA if the stream reports an error, else KDA_OK.
  */
 kda_status kda_prefill_check(const void *workspace, void *stream);
+
+/*
+ * kda_prefill_chunked_noalloc -- kda_prefill_chunked for callers that cannot
+ * allocate device memory: same arguments, outputs and results, no workspace.
+ * (This entry point has no counterpart in the method's description; it exists
+ * for integration.)
+ *
+ * Some callers cannot call cudaMalloc or any allocating library routine: code
+ * running while a CUDA graph is being built by someone else's allocator, a
+ * host process whose device memory is owned by a framework, or plain-C
+ * callers that hold only the tensors they were handed.  This variant keeps
+ * its scratch in one fixed device array of kda_noalloc_scratch_bytes() bytes
+ * (64 MiB) inside the library, held by every GPU that loads the library
+ * until the process exits.  Long inputs are processed in as many windows of
+ * chunks as that array needs; the call is rejected with KDA_ERR_TOO_LARGE
+ * only when not even one chunk of all H heads (74,240 bytes each) plus the
+ * N + 1 sequence offsets fits.
+ *
+ * - The first call on a device looks up the array's device address with
+ *   cudaGetSymbolAddress while that device is current; make that first call
+ *   outside any stream capture.
+ * - Every call on a device shares the array and leaves its contents behind;
+ *   each call rewrites what it reads, so no clearing is needed, but calls that
+ *   overlap on the GPU (other streams, other host threads) race on it.
+ * - It calls no allocator: no cudaMalloc, cudaFree or allocating library
+ *   routine.  fp32 and d = 64 inputs need no scratch at all.
+ * - Its device-side timeout status is not reported; use kda_prefill_chunked
+ *   with kda_prefill_check where that status matters.
+ */
+kda_status kda_prefill_chunked_noalloc(const void *q, const void *k, const void *v,
+                                       const float *g, const float *beta,
+                                       const float *S0, const int32_t *cu_seqlens,
+                                       int32_t N, int64_t T_total, int32_t H,
+                                       int32_t dk, int32_t dv, int32_t dtype,
+                                       int32_t chunk, void *o, float *S_T,
+                                       void *stream);
+
+/* Size in bytes of the fixed scratch array behind the no-allocation entry. */
+uint64_t kda_noalloc_scratch_bytes(void);
 
 /*
  * kda_decode_step -- one token for each of B independent sequences; the

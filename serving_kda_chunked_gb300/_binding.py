@@ -22,6 +22,7 @@ KDA_ERR_INVALID_ARG = 1
 KDA_ERR_UNSUPPORTED = 2
 KDA_ERR_CUDA = 3
 KDA_ERR_TIMEOUT = 4
+KDA_ERR_TOO_LARGE = 5
 KDA_BF16 = 0
 KDA_FP32 = 1
 
@@ -57,6 +58,11 @@ def load() -> ctypes.CDLL:
         lib.kda_prefill_chunked.restype = ctypes.c_int
         lib.kda_prefill_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32, i32]
         lib.kda_prefill_workspace_size.restype = u64
+        lib.kda_prefill_chunked_noalloc.argtypes = [
+            vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, i32, vp, vp, vp]
+        lib.kda_prefill_chunked_noalloc.restype = ctypes.c_int
+        lib.kda_noalloc_scratch_bytes.argtypes = []
+        lib.kda_noalloc_scratch_bytes.restype = u64
         lib.kda_prefill_check.argtypes = [vp, vp]
         lib.kda_prefill_check.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [

@@ -56,6 +56,43 @@ kda_status kda_prefill_chunked(const void *q, const void *k, const void *v,
     return cuda_status(kda::launch_prefill_simt(a, (cudaStream_t)stream));
 }
 
+kda_status kda_prefill_chunked_noalloc(const void *q, const void *k, const void *v,
+                                       const float *g, const float *beta,
+                                       const float *S0, const int32_t *cu_seqlens,
+                                       int32_t N, int64_t T_total, int32_t H,
+                                       int32_t dk, int32_t dv, int32_t dtype,
+                                       int32_t chunk, void *o, float *S_T,
+                                       void *stream) {
+    if (N < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
+    if (dk <= 0 || dv <= 0 || chunk <= 0) return KDA_ERR_INVALID_ARG;
+    if (!head_ok(dk, dv) || chunk != 64) return KDA_ERR_UNSUPPORTED;
+    if (N == 0) return T_total == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens || !S_T) return KDA_ERR_INVALID_ARG;
+    if (T_total > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) ||
+        !aligned16(o) || !aligned16(S0) || !aligned16(S_T) || !aligned4(beta) ||
+        !aligned4(cu_seqlens))
+        return KDA_ERR_INVALID_ARG;
+    if ((int64_t)N * H * (dv / 32) > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+    const bool tensor_path = dtype == KDA_BF16 && dk == 128;
+    if (tensor_path) {
+        if (T_total / 64 + N > 0x3fffffffLL) return KDA_ERR_UNSUPPORTED;
+        if (kda::noalloc_window_chunks(N, H) < 1) return KDA_ERR_TOO_LARGE;
+    }
+
+    kda::PrefillArgs a;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S0 = S0;
+    a.cu_seqlens = cu_seqlens; a.o = o; a.S_T = S_T;
+    a.N = N; a.H = H; a.dk = dk; a.dv = dv; a.dtype = dtype; a.chunk = chunk;
+    a.T = T_total;
+    if (tensor_path)
+        return cuda_status(kda::launch_prefill_tc_noalloc(a, (cudaStream_t)stream));
+    return cuda_status(kda::launch_prefill_simt(a, (cudaStream_t)stream));
+}
+
+uint64_t kda_noalloc_scratch_bytes(void) { return (uint64_t)KDA_NOALLOC_SCRATCH_MIB << 20; }
+
 uint64_t kda_prefill_workspace_size(int32_t N, int64_t T_total, int32_t H, int32_t dk,
                                     int32_t dv, int32_t dtype, int32_t chunk) {
     if (N <= 0 || T_total < 0 || H <= 0 || !head_ok(dk, dv) || chunk != 64) return 0;
@@ -101,6 +138,8 @@ const char *kda_status_string(int32_t status) {
     case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: shape, chunk or dtype not supported";
     case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call failed";
     case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded device wait gave up";
+    case KDA_ERR_TOO_LARGE:
+        return "KDA_ERR_TOO_LARGE: N or H too large for the fixed scratch of the no-allocation entry point";
     default: return "KDA_ERR_UNKNOWN: unknown status";
     }
 }

@@ -32,6 +32,13 @@ cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, void *workspace, cudaStream_t stream);
 size_t prefill_tc_workspace_bytes(int32_t N, int64_t T, int32_t H);
 
+// Size of the fixed scratch array behind kda_prefill_chunked_noalloc.
+#define KDA_NOALLOC_SCRATCH_MIB 64
+// Chunks per window that fit that scratch for N sequences and H heads
+// (0: not even one chunk fits).
+int64_t noalloc_window_chunks(int32_t N, int32_t H);
+cudaError_t launch_prefill_tc_noalloc(const PrefillArgs &a, cudaStream_t stream);
+
 // ---- element access helpers ------------------------------------------------
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }

@@ -42,6 +42,8 @@
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 namespace kda {
 namespace {
 
@@ -882,7 +884,11 @@ size_t prefill_tc_workspace_bytes(int32_t N, int64_t T, int32_t H) {
     return (size_t)ws_images_offset(N) + (size_t)wch * (size_t)H * CH_STRIDE;
 }
 
-cudaError_t launch_prefill_tc(const PrefillArgs &a, void *workspace, cudaStream_t st) {
+namespace {
+
+// The prefill with windows of `window` chunks; `workspace` holds at least
+// ws_images_offset(N) + window * H * CH_STRIDE bytes.
+cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, cudaStream_t st) {
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -892,7 +898,6 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, void *workspace, cudaStream_
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
     int32_t *hdr = reinterpret_cast<int32_t *>(ws);
     const int64_t bound = (a.T + C - 1) / C + a.N;
     chunk_table_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.N, a.T, (int)bound, hdr,
@@ -909,8 +914,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, void *workspace, cudaStream_
             return cudaErrorInvalidValue;
     }
     p1.beta = a.beta; p1.cu = a.cu_seqlens; p1.ws = ws; p1.N = a.N; p1.H = a.H; p1.T = a.T;
-    for (int64_t w0 = 0; w0 < bound; w0 += WINDOW_CHUNKS) {
-        const int64_t w1 = w0 + WINDOW_CHUNKS;
+    for (int64_t w0 = 0; w0 < bound; w0 += window) {
+        const int64_t w1 = w0 + window;
         p1.w0 = (int)w0; p1.w1 = (int)w1;
         if (a.T > 0) {
             const int64_t tasks = (w1 - w0) * a.H;
@@ -927,6 +932,53 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, void *workspace, cudaStream_
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+// Fixed scratch for callers that cannot allocate device memory.  Every GPU
+// that loads this library holds it until the process exits; all calls of
+// the no-allocation entry point share it.
+constexpr size_t NOALLOC_BYTES = (size_t)KDA_NOALLOC_SCRATCH_MIB << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_BYTES];
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const PrefillArgs &a, void *workspace, cudaStream_t st) {
+    const int64_t bound = (a.T + C - 1) / C + a.N;
+    const int64_t window = bound < WINDOW_CHUNKS ? bound : WINDOW_CHUNKS;
+    return run_prefill_tc(a, static_cast<uint8_t *>(workspace), window, st);
+}
+
+int64_t noalloc_window_chunks(int32_t N, int32_t H) {
+    const uint64_t head = ws_images_offset(N);
+    if (head >= NOALLOC_BYTES) return 0;
+    const uint64_t w = (NOALLOC_BYTES - head) / ((uint64_t)H * CH_STRIDE);
+    return (int64_t)(w < (uint64_t)WINDOW_CHUNKS ? w : (uint64_t)WINDOW_CHUNKS);
+}
+
+cudaError_t launch_prefill_tc_noalloc(const PrefillArgs &a, cudaStream_t st) {
+    // device address of the scratch array, looked up once per device with
+    // that device current (host code cannot use the symbol itself)
+    static std::mutex mu;
+    static void *addr[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    void *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!addr[dev]) {
+            e = cudaGetSymbolAddress(&addr[dev], g_noalloc_scratch);
+            if (e != cudaSuccess) {
+                addr[dev] = nullptr;
+                return e;
+            }
+        }
+        ws = addr[dev];
+    }
+    const int64_t window = noalloc_window_chunks(a.N, a.H);
+    if (window < 1) return cudaErrorInvalidValue;
+    return run_prefill_tc(a, static_cast<uint8_t *>(ws), window, st);
 }
 
 }  // namespace kda
