@@ -185,13 +185,23 @@ def barrier(world):
 
 
 def max_over_ranks(world, x: float) -> float:
+    """Largest value over all ranks (the slowest rank's time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(world, units_per_rank: float, ms_this_rank: float) -> tuple[float, float]:
+    """Whole-job throughput of independent replicas: every rank processed
+    `units_per_rank`; the job took as long as its slowest rank.  Returns
+    (units per second over all ranks, slowest rank's ms)."""
+    ms = max_over_ranks(world, ms_this_rank)
+    return world * units_per_rank / (ms * 1e-3), ms
 
 
 def device_id_for_smi(local):
