@@ -182,6 +182,69 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v,
                            int32_t B, int32_t H, int32_t dk, int32_t dv,
                            int32_t dtype, void *o, void *stream);
 
+/*
+ * kda_decode_step_pooled -- one decode token for each of B sequences whose
+ * states live in a shared pool of P slots; slot slots[b] holds the state of
+ * sequence b and is updated in place.
+ *
+ *   q, k       [B, H, dk]         dtype
+ *   v          [B, H, dv]         dtype
+ *   g          [B, H, dk]         float32      log-gate, finite, <= 0
+ *   beta       [B, H]             float32
+ *   S_pool     [P, H, dk, dv]     float32      slots named in `slots` are
+ *                                              read and overwritten
+ *   slots      [B]                int32        device memory; a value outside
+ *                                              [0, P) skips that sequence:
+ *                                              its o row is zeroed and no
+ *                                              state is touched
+ *   o          [B, H, dv]         dtype
+ *
+ * This is the serving form of decode: a KDA state has a fixed size however
+ * long the context (the essay's section "선형 어텐션 (Linear Attention):
+ * 고정된 크기의 메모리"), so concurrent sessions can each own one slot of a
+ * preallocated pool instead of a growing KV cache (the explainer's section
+ * "한국 개발자에게 주는 시사점": the number of concurrent requests is set
+ * by how much cache memory is left).  The slots of the non-skipped sequences
+ * must be distinct (two sequences in one slot race).  Slot values are not
+ * read on the host.  B = 0 is a valid no-op.
+ */
+kda_status kda_decode_step_pooled(const void *q, const void *k, const void *v,
+                                  const float *g, const float *beta, float *S_pool,
+                                  const int32_t *slots, int32_t P, int32_t B, int32_t H,
+                                  int32_t dk, int32_t dv, int32_t dtype, void *o,
+                                  void *stream);
+
+/*
+ * kda_gdn_prefill_chunked, kda_gdn_decode_step -- the same two operations for
+ * Gated DeltaNet, whose gate is one scalar per head and token instead of one
+ * rate per channel.  The lineage essay's section "Gated DeltaNet: 이제는
+ * '망각'할 수 있습니다" gives its update (decay the old memory by alpha, then
+ * write the delta along k); its section "KDA: Kimi의 비법" states that KDA
+ * differs from it only in turning that scalar alpha into a per-channel
+ * vector.  So a Gated DeltaNet head is a KDA head whose dk gates are all equal,
+ * and these entry points run the KDA kernels reading one gate per head:
+ *
+ *   g   [T_total, H]   (prefill)   or   [B, H]   (decode)   float32, log of
+ *       alpha, finite, <= 0; 4-byte alignment suffices.
+ *
+ * Every other argument, the workspace (kda_prefill_workspace_size gives its
+ * size here too), the outputs, the status codes and kda_prefill_check are as
+ * for kda_prefill_chunked and kda_decode_step.
+ */
+kda_status kda_gdn_prefill_chunked(const void *q, const void *k, const void *v,
+                                   const float *g, const float *beta,
+                                   const float *S0, const int32_t *cu_seqlens,
+                                   int32_t N, int64_t T_total, int32_t H,
+                                   int32_t dk, int32_t dv, int32_t dtype,
+                                   int32_t chunk, void *o, float *S_T,
+                                   void *workspace, uint64_t workspace_bytes,
+                                   void *stream);
+
+kda_status kda_gdn_decode_step(const void *q, const void *k, const void *v,
+                               const float *g, const float *beta, float *S,
+                               int32_t B, int32_t H, int32_t dk, int32_t dv,
+                               int32_t dtype, void *o, void *stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char *kda_status_string(int32_t status);
 

@@ -144,3 +144,25 @@ def prefill(q, k, v, g, beta, S0, cu_seqlens, nthreads: int = 0):
 def decode_step(q, k, v, g, beta, S, nthreads: int = 0):
     """See :meth:`OracleLib.decode_step` (default library)."""
     return _load().decode_step(q, k, v, g, beta, S, nthreads)
+
+
+def gdn_prefill(q, k, v, g, beta, S0, cu_seqlens, nthreads: int = 0):
+    """Gated DeltaNet prefill: g is [T, H], one log-gate per head and token.
+
+    The lineage essay's section "KDA: Kimi의 비법" describes KDA as Gated
+    DeltaNet with its scalar alpha turned into a per-channel vector, so a
+    scalar gate is the per-channel gate with every channel equal: g is
+    broadcast over dk and the KDA recurrence runs unchanged.
+    """
+    g = _f64(g)
+    dk = tuple(q.shape)[-1]
+    gb = np.ascontiguousarray(np.broadcast_to(g[..., None], g.shape + (dk,)))
+    return prefill(q, k, v, gb, beta, S0, cu_seqlens, nthreads)
+
+
+def gdn_decode_step(q, k, v, g, beta, S, nthreads: int = 0):
+    """Gated DeltaNet decode step: g is [B, H] (see :func:`gdn_prefill`)."""
+    g = _f64(g)
+    dk = tuple(q.shape)[-1]
+    gb = np.ascontiguousarray(np.broadcast_to(g[..., None], g.shape + (dk,)))
+    return decode_step(q, k, v, gb, beta, S, nthreads)

@@ -56,6 +56,8 @@ def load() -> ctypes.CDLL:
             vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, i32,
             vp, vp, vp, u64, vp]
         lib.kda_prefill_chunked.restype = ctypes.c_int
+        lib.kda_gdn_prefill_chunked.argtypes = lib.kda_prefill_chunked.argtypes
+        lib.kda_gdn_prefill_chunked.restype = ctypes.c_int
         lib.kda_prefill_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32, i32]
         lib.kda_prefill_workspace_size.restype = u64
         lib.kda_prefill_chunked_noalloc.argtypes = [
@@ -68,6 +70,11 @@ def load() -> ctypes.CDLL:
         lib.kda_decode_step.argtypes = [
             vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]
         lib.kda_decode_step.restype = ctypes.c_int
+        lib.kda_gdn_decode_step.argtypes = lib.kda_decode_step.argtypes
+        lib.kda_gdn_decode_step.restype = ctypes.c_int
+        lib.kda_decode_step_pooled.argtypes = [
+            vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+        lib.kda_decode_step_pooled.restype = ctypes.c_int
         lib.kda_status_string.argtypes = [i32]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_abi_version.argtypes = []
@@ -119,17 +126,8 @@ def kda_prefill_check(workspace, stream=None) -> int:
     return int(load().kda_prefill_check(_ptr(workspace), _stream(stream)))
 
 
-def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, S0=None, *, chunk: int = 64,
-                        o=None, S_T=None, workspace=None, stream=None):
-    """Chunked KDA prefill over a packed batch (``kda_prefill_chunked`` in kda.h).
-
-    q, k [T, H, dk] and v [T, H, dv] in bf16 or fp32 (all the same); g
-    [T, H, dk] fp32 log-gates; beta [T, H] fp32; cu_seqlens [N+1] int32 on the
-    device; S0 [N, H, dk, dv] fp32 or None.  Returns (o, S_T); pass ``o`` /
-    ``S_T`` to write into existing buffers (``S_T`` may be ``S0``).
-    ``workspace``: a uint8 CUDA tensor of at least
-    ``kda_prefill_workspace_size(...)`` bytes; allocated here when omitted.
-    """
+def _prefill(fn, gate_shape, q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_T, workspace,
+             stream):
     _check_cuda("q", q)
     if q.dtype not in _DTYPE_CODE:
         raise ValueError("q must be bfloat16 or float32")
@@ -137,7 +135,7 @@ def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, S0=None, *, chunk: int = 6
     dv = v.shape[-1]
     _check_cuda("k", k, q.dtype, (T, H, dk))
     _check_cuda("v", v, q.dtype, (T, H, dv))
-    _check_cuda("g", g, torch.float32, (T, H, dk))
+    _check_cuda("g", g, torch.float32, gate_shape(T, H, dk))
     _check_cuda("beta", beta, torch.float32, (T, H))
     _check_cuda("cu_seqlens", cu_seqlens, torch.int32)
     N = cu_seqlens.shape[0] - 1
@@ -156,13 +154,58 @@ def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, S0=None, *, chunk: int = 6
     if workspace is not None:
         _check_cuda("workspace", workspace, torch.uint8)
         ws_bytes = workspace.numel()
-    st = load().kda_prefill_chunked(
+    st = getattr(load(), fn)(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
         N, T, H, dk, dv, _DTYPE_CODE[q.dtype], int(chunk), _ptr(o), _ptr(S_T),
         _ptr(workspace), ws_bytes, _stream(stream))
     if st != KDA_OK:
-        raise KdaError("kda_prefill_chunked", st)
+        raise KdaError(fn, st)
     return o, S_T
+
+
+def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, S0=None, *, chunk: int = 64,
+                        o=None, S_T=None, workspace=None, stream=None):
+    """Chunked KDA prefill over a packed batch (``kda_prefill_chunked`` in kda.h).
+
+    q, k [T, H, dk] and v [T, H, dv] in bf16 or fp32 (all the same); g
+    [T, H, dk] fp32 log-gates; beta [T, H] fp32; cu_seqlens [N+1] int32 on the
+    device; S0 [N, H, dk, dv] fp32 or None.  Returns (o, S_T); pass ``o`` /
+    ``S_T`` to write into existing buffers (``S_T`` may be ``S0``).
+    ``workspace``: a uint8 CUDA tensor of at least
+    ``kda_prefill_workspace_size(...)`` bytes; allocated here when omitted.
+    """
+    return _prefill("kda_prefill_chunked", lambda T, H, dk: (T, H, dk), q, k, v, g, beta,
+                    cu_seqlens, S0, chunk, o, S_T, workspace, stream)
+
+
+def kda_gdn_prefill_chunked(q, k, v, g, beta, cu_seqlens, S0=None, *, chunk: int = 64,
+                            o=None, S_T=None, workspace=None, stream=None):
+    """Chunked Gated DeltaNet prefill (``kda_gdn_prefill_chunked`` in kda.h):
+    as ``kda_prefill_chunked`` with one log-gate per head, g [T, H] fp32."""
+    return _prefill("kda_gdn_prefill_chunked", lambda T, H, dk: (T, H), q, k, v, g, beta,
+                    cu_seqlens, S0, chunk, o, S_T, workspace, stream)
+
+
+def _decode(fn, gate_shape, q, k, v, g, beta, S, o, stream):
+    _check_cuda("q", q)
+    if q.dtype not in _DTYPE_CODE:
+        raise ValueError("q must be bfloat16 or float32")
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    _check_cuda("k", k, q.dtype, (B, H, dk))
+    _check_cuda("v", v, q.dtype, (B, H, dv))
+    _check_cuda("g", g, torch.float32, gate_shape(B, H, dk))
+    _check_cuda("beta", beta, torch.float32, (B, H))
+    _check_cuda("S", S, torch.float32, (B, H, dk, dv))
+    if o is None:
+        o = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
+    _check_cuda("o", o, q.dtype, (B, H, dv))
+    st = getattr(load(), fn)(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S), B, H, dk, dv,
+        _DTYPE_CODE[q.dtype], _ptr(o), _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(fn, st)
+    return o
 
 
 def kda_decode_step(q, k, v, g, beta, S, *, o=None, stream=None):
@@ -170,6 +213,24 @@ def kda_decode_step(q, k, v, g, beta, S, *, o=None, stream=None):
 
     q, k [B, H, dk], v [B, H, dv] (bf16 or fp32); g [B, H, dk] fp32; beta
     [B, H] fp32; S [B, H, dk, dv] fp32, updated in place.  Returns o.
+    """
+    return _decode("kda_decode_step", lambda B, H, dk: (B, H, dk), q, k, v, g, beta, S, o,
+                   stream)
+
+
+def kda_gdn_decode_step(q, k, v, g, beta, S, *, o=None, stream=None):
+    """One batched Gated DeltaNet decode step (``kda_gdn_decode_step`` in
+    kda.h): as ``kda_decode_step`` with one log-gate per head, g [B, H] fp32."""
+    return _decode("kda_gdn_decode_step", lambda B, H, dk: (B, H), q, k, v, g, beta, S, o,
+                   stream)
+
+
+def kda_decode_step_pooled(q, k, v, g, beta, S_pool, slots, *, o=None, stream=None):
+    """Batched decode over a pool of states (``kda_decode_step_pooled`` in kda.h).
+
+    S_pool [P, H, dk, dv] fp32; slots [B] int32 on the device (a value outside
+    [0, P) skips that sequence).  The named slots are updated in place.
+    Returns o [B, H, dv].
     """
     _check_cuda("q", q)
     if q.dtype not in _DTYPE_CODE:
@@ -180,13 +241,16 @@ def kda_decode_step(q, k, v, g, beta, S, *, o=None, stream=None):
     _check_cuda("v", v, q.dtype, (B, H, dv))
     _check_cuda("g", g, torch.float32, (B, H, dk))
     _check_cuda("beta", beta, torch.float32, (B, H))
-    _check_cuda("S", S, torch.float32, (B, H, dk, dv))
+    _check_cuda("S_pool", S_pool, torch.float32)
+    if S_pool.dim() != 4 or tuple(S_pool.shape[1:]) != (H, dk, dv):
+        raise ValueError("S_pool must have shape [P, %d, %d, %d]" % (H, dk, dv))
+    _check_cuda("slots", slots, torch.int32, (B,))
     if o is None:
         o = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
     _check_cuda("o", o, q.dtype, (B, H, dv))
-    st = load().kda_decode_step(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S), B, H, dk, dv,
-        _DTYPE_CODE[q.dtype], _ptr(o), _stream(stream))
+    st = load().kda_decode_step_pooled(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S_pool), _ptr(slots),
+        S_pool.shape[0], B, H, dk, dv, _DTYPE_CODE[q.dtype], _ptr(o), _stream(stream))
     if st != KDA_OK:
-        raise KdaError("kda_decode_step", st)
+        raise KdaError("kda_decode_step_pooled", st)
     return o

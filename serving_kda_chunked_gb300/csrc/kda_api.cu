@@ -14,18 +14,13 @@ kda_status cuda_status(cudaError_t e) {
     return KDA_ERR_CUDA;
 }
 
-}  // namespace
-
-extern "C" {
-
-kda_status kda_prefill_chunked(const void *q, const void *k, const void *v,
-                               const float *g, const float *beta,
-                               const float *S0, const int32_t *cu_seqlens,
-                               int32_t N, int64_t T_total, int32_t H,
-                               int32_t dk, int32_t dv, int32_t dtype,
-                               int32_t chunk, void *o, float *S_T,
-                               void *workspace, uint64_t workspace_bytes,
-                               void *stream) {
+// Shared by the per-channel (KDA) and per-head (Gated DeltaNet) entry points:
+// they differ only in the layout of g ([T, H, dk] vs [T, H]).
+kda_status prefill_impl(const void *q, const void *k, const void *v, const float *g,
+                        const float *beta, const float *S0, const int32_t *cu_seqlens,
+                        int32_t N, int64_t T_total, int32_t H, int32_t dk, int32_t dv,
+                        int32_t dtype, int32_t chunk, void *o, float *S_T, void *workspace,
+                        uint64_t workspace_bytes, bool scalar_gate, void *stream) {
     if (N < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
     if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
     if (dk <= 0 || dv <= 0 || chunk <= 0) return KDA_ERR_INVALID_ARG;
@@ -33,7 +28,8 @@ kda_status kda_prefill_chunked(const void *q, const void *k, const void *v,
     if (N == 0) return T_total == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
     if (!cu_seqlens || !S_T) return KDA_ERR_INVALID_ARG;
     if (T_total > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) ||
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) ||
+        !(scalar_gate ? aligned4(g) : aligned16(g)) ||
         !aligned16(o) || !aligned16(S0) || !aligned16(S_T) || !aligned4(beta) ||
         !aligned4(cu_seqlens))
         return KDA_ERR_INVALID_ARG;
@@ -51,9 +47,63 @@ kda_status kda_prefill_chunked(const void *q, const void *k, const void *v,
     a.cu_seqlens = cu_seqlens; a.o = o; a.S_T = S_T;
     a.N = N; a.H = H; a.dk = dk; a.dv = dv; a.dtype = dtype; a.chunk = chunk;
     a.T = T_total;
+    a.scalar_gate = scalar_gate;
     if (tensor_path)
         return cuda_status(kda::launch_prefill_tc(a, workspace, (cudaStream_t)stream));
     return cuda_status(kda::launch_prefill_simt(a, (cudaStream_t)stream));
+}
+
+kda_status decode_impl(const void *q, const void *k, const void *v, const float *g,
+                       const float *beta, float *S, const int32_t *slots, int32_t P,
+                       bool pooled, int32_t B, int32_t H, int32_t dk, int32_t dv, int32_t dtype,
+                       void *o, bool scalar_gate, void *stream) {
+    if (B < 0 || H <= 0 || (pooled && P <= 0)) return KDA_ERR_INVALID_ARG;
+    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
+    if (dk <= 0 || dv <= 0) return KDA_ERR_INVALID_ARG;
+    if (!head_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
+    if (B == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !S || !o || (pooled && !slots))
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) ||
+        !(scalar_gate ? aligned4(g) : aligned16(g)) ||
+        !aligned16(S) || !aligned16(o) || !aligned4(beta) || !aligned4(slots))
+        return KDA_ERR_INVALID_ARG;
+    if ((int64_t)B * H > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+
+    kda::DecodeArgs a;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S = S; a.o = o;
+    a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.dtype = dtype;
+    a.slots = pooled ? slots : nullptr; a.P = P;
+    a.scalar_gate = scalar_gate;
+    return cuda_status(kda::launch_decode(a, (cudaStream_t)stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_prefill_chunked(const void *q, const void *k, const void *v,
+                               const float *g, const float *beta,
+                               const float *S0, const int32_t *cu_seqlens,
+                               int32_t N, int64_t T_total, int32_t H,
+                               int32_t dk, int32_t dv, int32_t dtype,
+                               int32_t chunk, void *o, float *S_T,
+                               void *workspace, uint64_t workspace_bytes,
+                               void *stream) {
+    return prefill_impl(q, k, v, g, beta, S0, cu_seqlens, N, T_total, H, dk, dv, dtype, chunk,
+                        o, S_T, workspace, workspace_bytes, false, stream);
+}
+
+kda_status kda_gdn_prefill_chunked(const void *q, const void *k, const void *v,
+                                   const float *g, const float *beta,
+                                   const float *S0, const int32_t *cu_seqlens,
+                                   int32_t N, int64_t T_total, int32_t H,
+                                   int32_t dk, int32_t dv, int32_t dtype,
+                                   int32_t chunk, void *o, float *S_T,
+                                   void *workspace, uint64_t workspace_bytes,
+                                   void *stream) {
+    return prefill_impl(q, k, v, g, beta, S0, cu_seqlens, N, T_total, H, dk, dv, dtype, chunk,
+                        o, S_T, workspace, workspace_bytes, true, stream);
 }
 
 kda_status kda_prefill_chunked_noalloc(const void *q, const void *k, const void *v,
@@ -114,21 +164,25 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v,
                            const float *g, const float *beta, float *S,
                            int32_t B, int32_t H, int32_t dk, int32_t dv,
                            int32_t dtype, void *o, void *stream) {
-    if (B < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
-    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
-    if (dk <= 0 || dv <= 0) return KDA_ERR_INVALID_ARG;
-    if (!head_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
-    if (B == 0) return KDA_OK;
-    if (!q || !k || !v || !g || !beta || !S || !o) return KDA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) ||
-        !aligned16(S) || !aligned16(o) || !aligned4(beta))
-        return KDA_ERR_INVALID_ARG;
-    if ((int64_t)B * H > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+    return decode_impl(q, k, v, g, beta, S, nullptr, 0, false, B, H, dk, dv, dtype, o, false,
+                       stream);
+}
 
-    kda::DecodeArgs a;
-    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S = S; a.o = o;
-    a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.dtype = dtype;
-    return cuda_status(kda::launch_decode(a, (cudaStream_t)stream));
+kda_status kda_gdn_decode_step(const void *q, const void *k, const void *v,
+                               const float *g, const float *beta, float *S,
+                               int32_t B, int32_t H, int32_t dk, int32_t dv,
+                               int32_t dtype, void *o, void *stream) {
+    return decode_impl(q, k, v, g, beta, S, nullptr, 0, false, B, H, dk, dv, dtype, o, true,
+                       stream);
+}
+
+kda_status kda_decode_step_pooled(const void *q, const void *k, const void *v,
+                                  const float *g, const float *beta, float *S_pool,
+                                  const int32_t *slots, int32_t P, int32_t B, int32_t H,
+                                  int32_t dk, int32_t dv, int32_t dtype, void *o,
+                                  void *stream) {
+    return decode_impl(q, k, v, g, beta, S_pool, slots, P, true, B, H, dk, dv, dtype, o, false,
+                       stream);
 }
 
 const char *kda_status_string(int32_t status) {
@@ -144,6 +198,6 @@ const char *kda_status_string(int32_t status) {
     }
 }
 
-int32_t kda_abi_version(void) { return (2 << 16) | 0; }
+int32_t kda_abi_version(void) { return (2 << 16) | 1; }
 
 }  // extern "C"

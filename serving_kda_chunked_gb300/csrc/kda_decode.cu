@@ -28,20 +28,34 @@ struct DecodeShape {
     static constexpr int NT = GROUPS * LANES;    // threads per CTA
 };
 
-template <int D, int ROWS, typename Tin>
+// POOLED: the state of sequence b lives in slot slots[b] of a pool of P
+// states [P, H, D, D]; a slot outside [0, P) skips the sequence (its o row is
+// zeroed and no state is touched).
+template <int D, int ROWS, typename Tin, bool POOLED>
 __global__ void __launch_bounds__(DecodeShape<D, ROWS>::NT)
 decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
               const Tin *__restrict__ v, const float *__restrict__ g,
               const float *__restrict__ beta, float *__restrict__ S,
-              Tin *__restrict__ o) {
+              Tin *__restrict__ o, const int32_t *__restrict__ slots, int H, int P,
+              bool scalar_gate) {
     using Sh = DecodeShape<D, ROWS>;
     constexpr int LANES = Sh::LANES, GROUPS = Sh::GROUPS, NT = Sh::NT;
     const int tid = threadIdx.x;
     const int lane = tid % LANES;
     const int grp = tid / LANES;
     const int64_t bh = blockIdx.x;               // sequence * H + head
+    int64_t sidx = bh;                           // which state
+    if (POOLED) {
+        const int slot = slots[bh / H];
+        if (slot < 0 || slot >= P) {
+            for (int i = tid; i < LANES; i += NT)
+                store4(o + bh * D + 4 * i, make_float4(0.f, 0.f, 0.f, 0.f));
+            return;
+        }
+        sidx = (int64_t)slot * H + bh % H;
+    }
 
-    float4 *Sp = reinterpret_cast<float4 *>(S + bh * (int64_t)D * D);
+    float4 *Sp = reinterpret_cast<float4 *>(S + sidx * (int64_t)D * D);
     float4 s[ROWS];
 #pragma unroll
     for (int r = 0; r < ROWS; ++r)
@@ -56,7 +70,7 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     for (int i = tid; i < D; i += NT) {
         sk[i] = to_f32(k[vb + i]);
         sq[i] = to_f32(q[vb + i]);
-        sa[i] = expf(g[vb + i]);
+        sa[i] = expf(scalar_gate ? g[bh] : g[vb + i]);
     }
     for (int i = tid; i < LANES; i += NT)
         sv4[i] = load4(v + vb + 4 * i);
@@ -113,23 +127,28 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     }
 }
 
-template <int D, int ROWS, typename Tin>
+template <int D, int ROWS, typename Tin, bool POOLED>
 cudaError_t launch(const DecodeArgs &a, cudaStream_t st) {
     const int64_t units = (int64_t)a.B * a.H;
-    decode_kernel<D, ROWS, Tin><<<(unsigned)units, DecodeShape<D, ROWS>::NT, 0, st>>>(
+    decode_kernel<D, ROWS, Tin, POOLED><<<(unsigned)units, DecodeShape<D, ROWS>::NT, 0, st>>>(
         (const Tin *)a.q, (const Tin *)a.k, (const Tin *)a.v, a.g, a.beta, a.S,
-        (Tin *)a.o);
+        (Tin *)a.o, a.slots, a.H, a.P, a.scalar_gate);
     return cudaGetLastError();
+}
+
+template <bool POOLED>
+cudaError_t dispatch(const DecodeArgs &a, cudaStream_t st) {
+    if ((int64_t)a.B * a.H == 0) return cudaSuccess;
+    const bool bf = a.dtype == 0;
+    if (a.dk == 128)
+        return bf ? launch<128, 16, __nv_bfloat16, POOLED>(a, st) : launch<128, 16, float, POOLED>(a, st);
+    return bf ? launch<64, 16, __nv_bfloat16, POOLED>(a, st) : launch<64, 16, float, POOLED>(a, st);
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st) {
-    if ((int64_t)a.B * a.H == 0) return cudaSuccess;
-    const bool bf = a.dtype == 0;
-    if (a.dk == 128)
-        return bf ? launch<128, 16, __nv_bfloat16>(a, st) : launch<128, 16, float>(a, st);
-    return bf ? launch<64, 16, __nv_bfloat16>(a, st) : launch<64, 16, float>(a, st);
+    return a.slots ? dispatch<true>(a, st) : dispatch<false>(a, st);
 }
 
 }  // namespace kda

@@ -16,6 +16,7 @@ struct PrefillArgs {
     float *S_T;
     int32_t N, H, dk, dv, dtype, chunk;
     int64_t T;
+    bool scalar_gate = false;   // g is [T, H] (one rate per head) instead of [T, H, dk]
 };
 
 // Arguments of one decode call after host validation.
@@ -25,6 +26,9 @@ struct DecodeArgs {
     float *S;
     void *o;
     int32_t B, H, dk, dv, dtype;
+    const int32_t *slots = nullptr;   // pooled decode: state slot of each sequence
+    int32_t P = 0;                    // pooled decode: number of slots
+    bool scalar_gate = false;         // g is [B, H] instead of [B, H, dk]
 };
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);

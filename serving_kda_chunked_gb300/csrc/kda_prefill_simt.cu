@@ -45,7 +45,7 @@ prefill_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                     const Tin *__restrict__ v, const float *__restrict__ g,
                     const float *__restrict__ beta, const float *S0,
                     const int32_t *__restrict__ cu, Tin *__restrict__ o,
-                    float *S_T, int H, int64_t T, int n_slices) {
+                    float *S_T, int H, int64_t T, int n_slices, bool scalar_gate) {
     using Sm = SimtSmem<DK, DVS>;
     constexpr int KP = Sm::KP, CP = Sm::CP;
     constexpr int DV = DK;
@@ -86,7 +86,7 @@ prefill_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                 const int64_t off = ((c0 + r) * H + h) * DK + c;
                 kv = to_f32(k[off]);
                 qv = to_f32(q[off]);
-                gv = g[off];
+                gv = scalar_gate ? g[(c0 + r) * H + h] : g[off];
             }
             sK[r * KP + c] = kv;
             sQ[r * KP + c] = qv;
@@ -213,7 +213,7 @@ cudaError_t launch(const PrefillArgs &a, cudaStream_t st) {
     const int64_t units = (int64_t)a.N * a.H * n_slices;
     kern<<<(unsigned)units, NT, Sm::bytes, st>>>(
         (const Tin *)a.q, (const Tin *)a.k, (const Tin *)a.v, a.g, a.beta, a.S0,
-        a.cu_seqlens, (Tin *)a.o, a.S_T, a.H, a.T, n_slices);
+        a.cu_seqlens, (Tin *)a.o, a.S_T, a.H, a.T, n_slices, a.scalar_gate);
     return cudaGetLastError();
 }
 

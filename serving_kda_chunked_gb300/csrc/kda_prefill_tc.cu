@@ -171,13 +171,15 @@ constexpr int TP = 65;                                // padded fp32 row stride
 constexpr float RANGE_LIMIT = 80.f;                   // e^80 stays inside fp32
 
 struct K1Params {
-    CUtensorMap tm_q, tm_k, tm_v, tm_g;   // 3D maps over [T][H][128]
+    CUtensorMap tm_q, tm_k, tm_v, tm_g;   // 3D maps over [T][H][128] (tm_g unused for scalar gates)
+    const float *g;                       // scalar gates [T][H] (when scalar_gate)
     const float *beta;
     const int32_t *cu;
     uint8_t *ws;
     int N, H;
     int64_t T;
     int w0, w1;
+    int scalar_gate;
 };
 
 __device__ __forceinline__ void tma_load_3d(uint8_t *dst, const CUtensorMap *map, int c0, int c1,
@@ -244,7 +246,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
     float *eL = gL + 128;                                  // [128] e^gamma_last
     float *sB = eL + 128;                                  // [64] beta
     float *tot = sB + 64;                                  // [4][128] segment totals
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(tot + 512);   // [0] TMA, [1] A/P, [2] W/U
+    float *sGs = tot + 512;                                // [64] scalar gates (scalar_gate)
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(sGs + 64);   // [0] TMA, [1] A/P, [2] W/U
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 3);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -282,11 +285,11 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         int h, L;
         int64_t t0;
         task_pos(task, h, t0, L);
-        mbar_arrive_expect_tx(&mbar[0], 3 * 16384 + 32768);
+        mbar_arrive_expect_tx(&mbar[0], 3 * 16384 + (p.scalar_gate ? 0 : 32768));
         tma_load_3d(sm + S1_STG_K, &p.tm_k, 0, h, (int)t0, &mbar[0]);
         tma_load_3d(sm + S1_STG_Q, &p.tm_q, 0, h, (int)t0, &mbar[0]);
         tma_load_3d(sm + S1_STG_V, &p.tm_v, 0, h, (int)t0, &mbar[0]);
-        tma_load_3d(sm + S1_STG_G, &p.tm_g, 0, h, (int)t0, &mbar[0]);
+        if (!p.scalar_gate) tma_load_3d(sm + S1_STG_G, &p.tm_g, 0, h, (int)t0, &mbar[0]);
     };
     if (tid == 0 && (int)blockIdx.x < ntask) issue_tma(blockIdx.x);
 
@@ -297,7 +300,10 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         int64_t t0;
         task_pos(task, h, t0, L);
         uint8_t *out = img_base + (uint64_t)task * CH_STRIDE;
-        if (tid < C) sB[tid] = tid < L ? p.beta[(t0 + tid) * H + h] : 0.f;
+        if (tid < C) {
+            sB[tid] = tid < L ? p.beta[(t0 + tid) * H + h] : 0.f;
+            if (p.scalar_gate) sGs[tid] = tid < L ? p.g[(t0 + tid) * H + h] : 0.f;
+        }
         ok = __syncthreads_and(mbar_wait(&mbar[0], it & 1));
         if (!ok) break;
 
@@ -311,7 +317,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int r = 16 * sg + j;
-                acc += r < L ? G[r * 128 + c] : 0.f;
+                acc += r < L ? (p.scalar_gate ? sGs[r] : G[r * 128 + c]) : 0.f;
                 v[j] = acc;
             }
             tot[sg * 128 + c] = acc;
@@ -909,10 +915,13 @@ cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, cu
     if (a.T > 0) {
         if (!token_map(&p1.tm_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.H, a.T) ||
             !token_map(&p1.tm_k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.H, a.T) ||
-            !token_map(&p1.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.H, a.T) ||
+            !token_map(&p1.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.H, a.T))
+            return cudaErrorInvalidValue;
+        if (!a.scalar_gate &&
             !token_map(&p1.tm_g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.H, a.T))
             return cudaErrorInvalidValue;
     }
+    p1.g = a.g; p1.scalar_gate = a.scalar_gate ? 1 : 0;
     p1.beta = a.beta; p1.cu = a.cu_seqlens; p1.ws = ws; p1.N = a.N; p1.H = a.H; p1.T = a.T;
     for (int64_t w0 = 0; w0 < bound; w0 += window) {
         const int64_t w1 = w0 + window;

@@ -56,22 +56,22 @@ def test_status_strings(lib):
 P = 0x10000  # a 16-byte aligned stand-in address; never dereferenced here
 
 
-def _prefill(lib, **kw):
+def _prefill(lib, fn="kda_prefill_chunked", **kw):
     a = dict(q=P, k=P, v=P, g=P, beta=P, S0=None, cu=P, N=1, T=64, H=2, dk=128,
              dv=128, dtype=0, chunk=64, o=P, S_T=P, ws=None, ws_bytes=0)
     a.update(kw)
     vp = ctypes.c_void_p
-    return lib.kda_prefill_chunked(
+    return getattr(lib, fn)(
         vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]),
         vp(a["S0"]), vp(a["cu"]), a["N"], a["T"], a["H"], a["dk"], a["dv"],
         a["dtype"], a["chunk"], vp(a["o"]), vp(a["S_T"]), vp(a["ws"]), a["ws_bytes"], None)
 
 
-def _decode(lib, **kw):
+def _decode(lib, fn="kda_decode_step", **kw):
     a = dict(q=P, k=P, v=P, g=P, beta=P, S=P, B=4, H=2, dk=128, dv=128, dtype=0, o=P)
     a.update(kw)
     vp = ctypes.c_void_p
-    return lib.kda_decode_step(
+    return getattr(lib, fn)(
         vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), vp(a["S"]),
         a["B"], a["H"], a["dk"], a["dv"], a["dtype"], vp(a["o"]), None)
 
@@ -117,6 +117,53 @@ def test_prefill_host_validation(lib, kw, expect):
 ])
 def test_decode_host_validation(lib, kw, expect):
     assert _decode(lib, **kw) == expect
+
+
+def _decode_pooled(lib, **kw):
+    a = dict(q=P, k=P, v=P, g=P, beta=P, S=P, slots=P, Pn=8, B=4, H=2, dk=128, dv=128,
+             dtype=0, o=P)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.kda_decode_step_pooled(
+        vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), vp(a["S"]),
+        vp(a["slots"]), a["Pn"], a["B"], a["H"], a["dk"], a["dv"], a["dtype"], vp(a["o"]), None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(Pn=0), kda.KDA_ERR_INVALID_ARG),
+    (dict(slots=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(slots=P + 2), kda.KDA_ERR_INVALID_ARG),
+    (dict(S=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(dk=64, dv=128), kda.KDA_ERR_UNSUPPORTED),
+    (dict(B=0), kda.KDA_OK),
+])
+def test_decode_pooled_host_validation(lib, kw, expect):
+    assert _decode_pooled(lib, **kw) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(H=0), kda.KDA_ERR_INVALID_ARG),
+    (dict(dtype=7), kda.KDA_ERR_INVALID_ARG),
+    (dict(dk=96, dv=96), kda.KDA_ERR_UNSUPPORTED),
+    (dict(g=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(g=P + 2), kda.KDA_ERR_INVALID_ARG),     # one gate per head: 4-byte alignment
+    (dict(q=P + 4), kda.KDA_ERR_INVALID_ARG),
+    (dict(ws=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(N=0, T=0), kda.KDA_OK),
+])
+def test_gdn_prefill_host_validation(lib, kw, expect):
+    assert _prefill(lib, fn="kda_gdn_prefill_chunked", **kw) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(B=-1), kda.KDA_ERR_INVALID_ARG),
+    (dict(g=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(g=P + 1), kda.KDA_ERR_INVALID_ARG),
+    (dict(dk=32, dv=32), kda.KDA_ERR_UNSUPPORTED),
+    (dict(B=0), kda.KDA_OK),
+])
+def test_gdn_decode_host_validation(lib, kw, expect):
+    assert _decode(lib, fn="kda_gdn_decode_step", **kw) == expect
 
 
 def test_workspace_size_query(lib):

@@ -378,3 +378,57 @@ def test_rejects_bad_offsets():
         oracle.prefill(q, k, v, g, beta, S0, [0, 7])
     with pytest.raises(ValueError):
         oracle.prefill(q, k, v, g, beta, np.zeros((2, 1, 4, 4)), [0, 4, 2])
+
+
+# ---------------------------------------------------------------------------
+# Gated DeltaNet (one gate per head): "Gated DeltaNet" section of the essay
+# ---------------------------------------------------------------------------
+def test_gdn_prefill_follows_the_scalar_gated_rule():
+    """gdn_prefill with g [T, H] matches S_t = a_t S_{t-1} + k_t delta_t^T,
+    delta_t = b_t (v_t - (a_t S_{t-1})^T k_t), written out per step in its
+    'decay the old memory, then write the delta' order, over two sequences."""
+    rng = np.random.default_rng(21)
+    T, H, dk, dv = 11, 2, 5, 4
+    q, k, v, _, beta, S0 = _rand_case(rng, T, H, dk, dv, N=2)
+    g = -np.abs(rng.standard_normal((T, H)))
+    cu = [0, 4, T]
+    o, S_T, _ = oracle.gdn_prefill(q, k, v, g, beta, S0, cu)
+    for n in range(2):
+        for h in range(H):
+            S = S0[n, h].copy()
+            for t in range(cu[n], cu[n + 1]):
+                a, b, kt = math.exp(g[t, h]), beta[t, h], k[t, h]
+                delta = b * (v[t, h] - (a * S).T @ kt)
+                S = a * S + np.outer(kt, delta)
+                np.testing.assert_allclose(o[t, h], S.T @ q[t, h], rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(S_T[n, h], S, rtol=1e-12, atol=1e-12)
+
+
+def test_gdn_cumulative_decay():
+    """With no writes (beta = 0) a value stored at the start is read at step t
+    through the product of the gates a_1 ... a_t, one number for the whole
+    head (the essay's cumulative-decay statement for Gated DeltaNet)."""
+    rng = np.random.default_rng(22)
+    T, H, dk, dv = 9, 3, 4, 6
+    q, k, v, _, beta, S0 = _rand_case(rng, T, H, dk, dv)
+    beta[:] = 0.0
+    g = -np.abs(rng.standard_normal((T, H)))
+    o, S_T, _ = oracle.gdn_prefill(q, k, v, g, beta, S0, [0, T])
+    cum = np.cumsum(g, axis=0)
+    for h in range(H):
+        for t in range(T):
+            np.testing.assert_allclose(o[t, h], math.exp(cum[t, h]) * (S0[0, h].T @ q[t, h]),
+                                       rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(S_T[0, h], math.exp(cum[-1, h]) * S0[0, h],
+                                   rtol=1e-12, atol=1e-14)
+
+
+def test_gdn_decode_matches_gdn_prefill_step():
+    rng = np.random.default_rng(23)
+    B, H, dk, dv = 3, 2, 4, 5
+    q, k, v, _, beta, S0 = _rand_case(rng, B, H, dk, dv, N=B)
+    g = -np.abs(rng.standard_normal((B, H)))
+    o_d, S_d = oracle.gdn_decode_step(q[:, :, :], k, v, g, beta, S0)
+    o_p, S_p, _ = oracle.gdn_prefill(q, k, v, g, beta, S0, list(range(B + 1)))
+    np.testing.assert_allclose(o_d, o_p, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(S_d, S_p, rtol=1e-13, atol=1e-14)

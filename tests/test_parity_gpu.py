@@ -262,3 +262,122 @@ def test_corrupt_offsets_stay_in_bounds():
     assert_close("o", o, o_ref, 2e-3)
     assert_close("S_T", S_T, S_ref, 2e-3)
     assert torch.all(S_T[2] == 0)
+
+
+# ---------------------------------------------------------------------------
+# decode over a state-slot pool
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_decode_pooled_slots(dtype):
+    """Sequences name their state slot in a pool; untouched slots stay
+    bit-identical, a slot outside the pool skips its sequence (o row = 0)."""
+    P, B, H, d, steps = 12, 7, 3, 128, 4
+    cfg = ki.DecodeConfig("pool", B=B, H=H, d=d, steps=steps, dtype=dtype)
+    inp = ki.decode_inputs(cfg, device=DEV, seed=11)
+    gen = torch.Generator(device="cpu").manual_seed(5)
+    pool = (torch.randn((P, H, d, d), generator=gen) * 0.05).to(DEV)
+    ref = pool.double().cpu().numpy()
+    tol = TOL[DT[dtype]]
+    for s in range(steps):
+        perm = torch.randperm(P, generator=gen)[:B].to(torch.int32)
+        perm[3] = -1 if s % 2 == 0 else P + 2          # a skipped sequence
+        slots = perm.to(DEV)
+        before = pool.clone()
+        o = kda.kda_decode_step_pooled(inp["q"][s], inp["k"][s], inp["v"][s], inp["g"][s],
+                                       inp["beta"][s], pool, slots)
+        torch.cuda.synchronize()
+        live = [b for b in range(B) if 0 <= int(perm[b]) < P]
+        idx = [int(perm[b]) for b in live]
+        o_ref, S_new = oracle.decode_step(inp["q"][s][live], inp["k"][s][live], inp["v"][s][live],
+                                          inp["g"][s][live], inp["beta"][s][live], ref[idx])
+        ref[idx] = S_new
+        assert_close("o", o[live], o_ref, tol)
+        assert_close("pool slots", pool[idx], S_new, tol)
+        assert torch.all(o[3] == 0)
+        untouched = [p for p in range(P) if p not in idx]
+        assert torch.equal(pool[untouched], before[untouched])
+
+
+# ---------------------------------------------------------------------------
+# strong gates: the pairwise intra-chunk path of the tensor-core kernel
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_prefill_strong_gates(dtype):
+    """gate scale 8: a chunk's cumulative log-gate reaches hundreds, beyond
+    the range where exp(gamma) and exp(-gamma) factor safely, so the
+    intra-chunk products are formed pair by pair."""
+    lengths = [64, 1, 190, 77]
+    cfg = ki.PrefillConfig("strong", H=2, d=128, dtype=dtype, n_seqs=len(lengths),
+                           s0_std=0.3, gate_scale=8.0)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=17, lengths=lengths)
+    assert float(inp["g"].sum(0).min()) < -500.0
+    o, S_T = _run_prefill(inp)
+    o_ref, S_ref = _oracle_prefill(inp)
+    assert_close("o", o, o_ref, TOL[DT[dtype]])
+    assert_close("S_T", S_T, S_ref, TOL[DT[dtype]])
+
+
+# ---------------------------------------------------------------------------
+# Gated DeltaNet: one gate per head and token
+# ---------------------------------------------------------------------------
+def _head_gate(g):
+    """One log-gate per (token, head): the first channel of the per-channel draw."""
+    return g[..., 0].contiguous()
+
+
+def _gdn_case(inp):
+    gh = _head_gate(inp["g"])
+    o, S_T = kda.kda_gdn_prefill_chunked(inp["q"], inp["k"], inp["v"], gh, inp["beta"],
+                                         inp["cu_seqlens"], inp["S0"])
+    torch.cuda.synchronize()
+    o_ref, S_ref, _ = oracle.gdn_prefill(inp["q"], inp["k"], inp["v"], gh, inp["beta"],
+                                         inp["S0"], inp["cu_seqlens"])
+    return o, S_T, o_ref, S_ref
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_gdn_prefill_ragged(d, dtype):
+    lengths = [1, 63, 0, 64, 65, 200, 130, 7]
+    cfg = ki.PrefillConfig("ragged", H=3, d=d, dtype=dtype, n_seqs=len(lengths), s0_std=0.3)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=13, lengths=lengths)
+    o, S_T, o_ref, S_ref = _gdn_case(inp)
+    assert_close("o", o, o_ref, TOL[DT[dtype]])
+    assert_close("S_T", S_T, S_ref, TOL[DT[dtype]])
+    assert torch.equal(S_T[2], inp["S0"][2])
+
+
+def test_gdn_prefill_single_sequence_workload():
+    """B=1, H=32, T=8192, d=128, bf16 with one gate per head: checked in full."""
+    inp = ki.prefill_inputs("single", device=DEV, seed=14)
+    o, S_T, o_ref, S_ref = _gdn_case(inp)
+    assert_close("o", o, o_ref, 2e-3)
+    assert_close("S_T", S_T, S_ref, 2e-3)
+
+
+def test_gdn_prefill_strong_gates():
+    lengths = [64, 190, 77]
+    cfg = ki.PrefillConfig("strong", H=2, d=128, dtype="bf16", n_seqs=len(lengths),
+                           s0_std=0.3, gate_scale=8.0)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=18, lengths=lengths)
+    o, S_T, o_ref, S_ref = _gdn_case(inp)
+    assert_close("o", o, o_ref, 2e-3)
+    assert_close("S_T", S_T, S_ref, 2e-3)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_gdn_decode_multi_step(d, dtype):
+    cfg = ki.DecodeConfig("t", B=5, H=3, d=d, steps=10, dtype=dtype)
+    inp = ki.decode_inputs(cfg, device=DEV, seed=19)
+    S = inp["S0"].clone()
+    S_ref = inp["S0"].double().cpu().numpy()
+    for s in range(cfg.steps):
+        gh = _head_gate(inp["g"][s])
+        o = kda.kda_gdn_decode_step(inp["q"][s], inp["k"][s], inp["v"][s], gh,
+                                    inp["beta"][s], S)
+        o_ref, S_ref = oracle.gdn_decode_step(inp["q"][s], inp["k"][s], inp["v"][s], gh,
+                                              inp["beta"][s], S_ref)
+        torch.cuda.synchronize()
+        assert_close("o step %d" % s, o, o_ref, TOL[DT[dtype]])
+        assert_close("S step %d" % s, S, S_ref, TOL[DT[dtype]])
