@@ -27,10 +27,10 @@
 //    then K^T U and P U, each a tcgen05 round trip.  Operand images arrive
 //    with bulk async copies, double buffered.
 //
-// Gate factors inside a chunk use a reference point per 16-row block
-// (e^(gamma_r - gamma_ref) and e^(gamma_ref - gamma_i)), so no factor exceeds
-// e^(sum of |g| over 16 tokens): results stay finite while every channel's
-// log-gate sum over any 16 consecutive tokens is above about -80.
+// Gate factors inside a chunk are referenced to the chunk start (K e^gamma,
+// K e^-gamma), which stays inside fp32 while every channel's log-gate sum over
+// the chunk is above -80; a chunk beyond that forms A and P pair by pair with
+// e^(gamma_r - gamma_i) <= 1 instead, so any gate strength gives finite results.
 //
 // Operand precision (chosen with a CPU emulation against the fp64 oracle):
 // A and P use tf32 operands (the gated factors need fp32 range); every other
@@ -141,18 +141,23 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 // ------------------------------------------------------------------------------
 // One CTA per SM walks (chunk, head) tasks.  Per task:
 //   1. TMA brings k, q, v (bf16) and g (fp32) rows [t0, t0 + 64) of head h
-//      into staging (issued one task ahead).
+//      into staging, issued during the previous task: k, q and g once its
+//      MMA operands are formed, v once its fp16 images are.
 //   2. Per-channel cumulative log-gate (in place), e^gamma_last, range check.
 //   3. Element-wise prep, 8 channels of one row per unit: tf32 operands
-//      [K e^g ; Q e^g] and K e^-g for A / P, fp16 K e^g and V for W / U~, and
-//      the Q^ and Kbar images written straight to the workspace.
+//      [K e^g ; Q e^g] and K e^-g for A / P.
 //   4. One M = 128 tf32 MMA: rows 0-63 give A / beta, rows 64-127 give P.
 //      A chunk whose decay exceeds e^80 on some channel would overflow those
 //      factors, so it takes an exact pairwise CUDA-core path instead.
-//   5. T = (I + A)^-1 on CUDA cores (fp32; 16 x 16 diagonal blocks, then
-//      three block levels), T' = T Diag(beta) as fp16.
-//   6. W = T' (K e^g), U~ = T' V on tcgen05 (fp16), stored to the workspace.
+//      While that MMA runs, the fp16 images (K e^g and V for W / U~, the Q^
+//      and Kbar workspace images) are formed from the tf32 operands, and the
+//      previous task's W and U~ leave TMEM for the workspace.
+//   5. T = (I + A)^-1 on CUDA cores (fp32, 16 x 16 blocks, register-tiled
+//      block forward substitution), T' = T Diag(beta) as fp16.
+//   6. W = T' (K e^g), U~ = T' V on tcgen05 (fp16); they stay in TMEM until
+//      the next task's A/P MMA is running.
 constexpr int K1_THREADS = 512;
+constexpr int K1_ISSUER0 = 12;  // warps 12-15 issue the A/P MMAs
 constexpr uint32_t S1_STG_K = 0, S1_STG_Q = 16384, S1_STG_V = 32768;  // bf16 [64][128]
 constexpr uint32_t S1_STG_G = 49152;                                  // fp32 [64][128]
 constexpr uint32_t S1_OPA = 81920;    // tf32 [K e^g ; Q e^g]: 4 atoms x 128 rows x 128 B
@@ -162,12 +167,15 @@ constexpr uint32_t S1_V16 = 196608;   // fp16 V, same layout
 constexpr uint32_t S1_TP = 212992;    // fp16 T', K-major SW128 [r][i]
 constexpr uint32_t S1_MISC = 221184;
 constexpr uint32_t S1_BYTES = S1_MISC + 4096 + 1024;
-// after the A/P MMA has completed the operand area is reused:
-constexpr uint32_t S1_AS = S1_OPA;            // A  fp32 [64][TP]
-constexpr uint32_t S1_TS = S1_OPA + 17408;    // T  fp32 [64][TP]
-constexpr uint32_t S1_Y = S1_OPA + 34816;     // [3][16][17] fp32 scratch
+// after the A/P MMA has completed the operand area is reused by the inverse:
+constexpr int LD = 68;                          // fp32 row stride of the 64 x 64 tiles
+constexpr uint32_t TILE_BYTES = 64 * LD * 4;    // 17,408
+constexpr uint32_t S1_AS = S1_OPA;                   // A    fp32 [64][LD]
+constexpr uint32_t S1_TS = S1_OPA + TILE_BYTES;      // T    fp32 [64][LD]
+constexpr uint32_t S1_TT = S1_OPA + 2 * TILE_BYTES;  // T_RR transposed (diagonal blocks)
+constexpr uint32_t S1_FT = S1_OPA + 3 * TILE_BYTES;  // F = T_RR A_RJ, transposed
+static_assert(S1_FT + TILE_BYTES <= S1_KG16, "inverse scratch overlaps the fp16 operands");
 constexpr int AP_COL = 0, W_COL = 256, U_COL = 384;  // TMEM: 4 A/P partials of 64, W, U~
-constexpr int TP = 65;                                // padded fp32 row stride
 constexpr float RANGE_LIMIT = 80.f;                   // e^80 stays inside fp32
 
 struct K1Params {
@@ -202,40 +210,98 @@ __device__ __forceinline__ uint32_t rc_img_off(int r, int c0) {
     return (uint32_t)(c0 >> 6) * 8192u + sw128_off(r, (c0 & 63) >> 3);
 }
 
-// One level of the blocked unit-lower-triangular inverse: for every block
-// (R, I = R - d),  T_RI = -T_RR * sum_{J=I}^{R-1} A_RJ T_JI  (16 x 16 blocks).
-template <int d>
-__device__ __forceinline__ void inverse_level(const float *As, float *Ts, float *Ysc, int tid) {
-    constexpr int nb = 4 - d;
-    for (int e = tid; e < nb * 256; e += K1_THREADS) {
-        const int bI = e >> 8, m = (e >> 4) & 15, nn = e & 15;
-        const int R = d + bI, I = R - d;
-        const float *arow = As + (16 * R + m) * TP + 16 * I;
-        const float *tcol = Ts + (16 * I) * TP + 16 * I + nn;
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+// acc[2][4] += X[m0..m0+1][k] Y[k][n0..n0+3] over k = 0..15, with X read
+// transposed (Xt[k][m]) and Y row-major, both with row stride LD.
+__device__ __forceinline__ void mm16_2x4(float (&acc)[2][4], const float *Xt, const float *Y) {
 #pragma unroll
-        for (int kx = 0; kx < 16 * d; kx += 4) {
-            s0 += arow[kx] * tcol[kx * TP];
-            s1 += arow[kx + 1] * tcol[(kx + 1) * TP];
-            s2 += arow[kx + 2] * tcol[(kx + 2) * TP];
-            s3 += arow[kx + 3] * tcol[(kx + 3) * TP];
-        }
-        Ysc[bI * 272 + m * 17 + nn] = (s0 + s1) + (s2 + s3);
+    for (int k = 0; k < 16; ++k) {
+        const float2 x = *reinterpret_cast<const float2 *>(Xt + k * LD);
+        const float4 y = *reinterpret_cast<const float4 *>(Y + k * LD);
+        acc[0][0] = fmaf(x.x, y.x, acc[0][0]); acc[0][1] = fmaf(x.x, y.y, acc[0][1]);
+        acc[0][2] = fmaf(x.x, y.z, acc[0][2]); acc[0][3] = fmaf(x.x, y.w, acc[0][3]);
+        acc[1][0] = fmaf(x.y, y.x, acc[1][0]); acc[1][1] = fmaf(x.y, y.y, acc[1][1]);
+        acc[1][2] = fmaf(x.y, y.z, acc[1][2]); acc[1][3] = fmaf(x.y, y.w, acc[1][3]);
     }
-    __syncthreads();
-    for (int e = tid; e < nb * 256; e += K1_THREADS) {
-        const int bI = e >> 8, m = (e >> 4) & 15, nn = e & 15;
-        const int R = d + bI, I = R - d;
-        const float *trow = Ts + (16 * R + m) * TP + 16 * R;
-        float s0 = 0.f, s1 = 0.f;
+}
+
+// fp16 of x at (row r, column i) of the K-major 128B-swizzled T' image
+__device__ __forceinline__ void tp_store1(uint8_t *img, int r, int i, float x) {
+    *reinterpret_cast<__half *>(img + sw128_off(r, i >> 3) + (i & 7) * 2) = __float2half_rn(x);
+}
+
+// T = (I + A)^-1 for the strictly lower 64 x 64 A (row-major, stride LD) in
+// 16 x 16 blocks, fp32 on CUDA cores, and the fp16 image of T' = T Diag(beta).
+// With T_RR the inverses of the diagonal blocks of I + A and F_RJ = T_RR A_RJ
+// (J < R), block forward substitution gives T_RI = -sum_{J=I}^{R-1} F_RJ T_JI
+// for I < R.  Six warps each own one off-diagonal block of T (2 x 4 outputs
+// per lane, partial sums kept in registers) and add one term per pass, so the
+// whole inverse is: diagonal blocks | F | three passes.  Run by warps 0-5
+// only (named barrier 1), leaving the other warps free.  The image's blocks
+// above the diagonal are not written (they hold zeros).
+constexpr int INV_THREADS = 192;
+__device__ __forceinline__ void invert_unit_lower(const float *As, float *Ts, float *Tt, float *Ft,
+                                                  const float *sB, uint8_t *tp_img, int tid) {
+    const int warp = tid >> 5, lane = tid & 31;
+    // diagonal blocks: thread (R, column j) by forward substitution in registers
+    if (tid < 64) {
+        const int R = tid >> 4, j = tid & 15;
+        const float *Ab = As + (16 * R) * LD + 16 * R;
+        float x[16];
 #pragma unroll
-        for (int kx = 0; kx < 16; kx += 2) {
-            if (kx <= m) s0 += trow[kx] * Ysc[bI * 272 + kx * 17 + nn];
-            if (kx + 1 <= m) s1 += trow[kx + 1] * Ysc[bI * 272 + (kx + 1) * 17 + nn];
+        for (int m = 0; m < 16; ++m) x[m] = (m == j) ? 1.f : 0.f;
+#pragma unroll
+        for (int i = 0; i < 15; ++i) {
+            const float xi = x[i];
+#pragma unroll
+            for (int r = i + 1; r < 16; ++r) x[r] = fmaf(-Ab[r * LD + i], xi, x[r]);
         }
-        Ts[(16 * R + m) * TP + 16 * I + nn] = -(s0 + s1);
+        const float bj = sB[16 * R + j];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            Ts[(16 * R + m) * LD + 16 * R + j] = x[m];
+            tp_store1(tp_img, 16 * R + m, 16 * R + j, x[m] * bj);
+        }
+        float4 *trow = reinterpret_cast<float4 *>(Tt + (16 * R + j) * LD + 16 * R);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+            trow[q4] = make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
     }
-    __syncthreads();
+    bar_sync(1, INV_THREADS);
+
+    // warp w owns block (R, I): (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
+    const int R = warp < 3 ? warp + 1 : (warp < 5 ? warp - 1 : 3);
+    const int I = warp < 3 ? warp : (warp < 5 ? warp - 3 : 0);
+    const int m0 = 2 * (lane >> 2), n0 = 4 * (lane & 3);
+    {   // F_RI = T_RR A_RI, stored transposed
+        float f[2][4] = {};
+        mm16_2x4(f, Tt + (16 * R) * LD + 16 * R + m0, As + (16 * R) * LD + 16 * I + n0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<float2 *>(Ft + (16 * I + n0 + e) * LD + 16 * R + m0) =
+                make_float2(f[0][e], f[1][e]);
+    }
+    bar_sync(1, INV_THREADS);
+    float acc[2][4] = {};
+#pragma unroll
+    for (int pass = 0; pass < 3; ++pass) {
+        const int J = I + pass;
+        if (J < R) {
+            mm16_2x4(acc, Ft + (16 * J) * LD + 16 * R + m0, Ts + (16 * J) * LD + 16 * I + n0);
+            if (J == R - 1) {
+                const float4 b4 = *reinterpret_cast<const float4 *>(sB + 16 * I + n0);
+#pragma unroll
+                for (int a = 0; a < 2; ++a) {
+                    const int r = 16 * R + m0 + a, i = 16 * I + n0;
+                    *reinterpret_cast<float4 *>(Ts + r * LD + i) =
+                        make_float4(-acc[a][0], -acc[a][1], -acc[a][2], -acc[a][3]);
+                    *reinterpret_cast<uint2 *>(tp_img + sw128_off(r, i >> 3) + (i & 7) * 2) =
+                        make_uint2(pack_h2(-acc[a][0] * b4.x, -acc[a][1] * b4.y),
+                                   pack_h2(-acc[a][2] * b4.z, -acc[a][3] * b4.w));
+                }
+            }
+        }
+        if (pass < 2) bar_sync(1, INV_THREADS);
+    }
 }
 
 __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_constant__ K1Params p) {
@@ -267,45 +333,142 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    // T' is lower triangular: the blocks above its diagonal stay zero (the
+    // inverse rewrites only the diagonal and lower blocks)
+    for (int e = tid; e < 64 * 8; e += K1_THREADS) {
+        const int r = e >> 3, ch = e & 7;
+        if (ch >= 2 * ((r >> 4) + 1))
+            *reinterpret_cast<uint4 *>(sm + S1_TP + sw128_off(r, ch)) = make_uint4(0, 0, 0, 0);
+    }
 
     const int total = chunk_base[p.N];
     const int c_end = min(p.w1, total);
     const int ntask = (c_end > p.w0 ? c_end - p.w0 : 0) * H;
+    const int stride = gridDim.x;
 
-    auto task_pos = [&](int task, int &h, int64_t &t0, int &L) {
-        const int ch = p.w0 + task / H;
-        h = task % H;
-        const int n = find_seq(chunk_base, p.N, ch);
-        int64_t bos, eos;
-        seq_bounds(p.cu, n, p.T, bos, eos);
-        t0 = bos + (int64_t)(ch - chunk_base[n]) * C;
-        L = (int)((eos - t0) < C ? (eos - t0) : C);
+    struct Pos { int h, L; int64_t t0; };
+    // A task's position in two steps: fetch issues the offset-table loads,
+    // finish is their first use (placed a phase later, so that the loads'
+    // latency is hidden).  Together they give the sequence bounds clamped into
+    // [0, T] (as seq_bounds does) and the chunk's first token and length.
+    struct PosRaw { int ch, h; int32_t c0, c1, cb; };
+    auto pos_fetch = [&](int task) {
+        PosRaw r{-1, 0, 0, 0, 0};
+        if (task >= ntask) return r;
+        r.ch = p.w0 + task / H;
+        r.h = task % H;
+        const int n = find_seq(chunk_base, p.N, r.ch);
+        r.c0 = p.cu[n];
+        r.c1 = p.cu[n + 1];
+        r.cb = chunk_base[n];
+        return r;
     };
-    auto issue_tma = [&](int task) {
-        int h, L;
-        int64_t t0;
-        task_pos(task, h, t0, L);
-        mbar_arrive_expect_tx(&mbar[0], 3 * 16384 + (p.scalar_gate ? 0 : 32768));
-        tma_load_3d(sm + S1_STG_K, &p.tm_k, 0, h, (int)t0, &mbar[0]);
-        tma_load_3d(sm + S1_STG_Q, &p.tm_q, 0, h, (int)t0, &mbar[0]);
-        tma_load_3d(sm + S1_STG_V, &p.tm_v, 0, h, (int)t0, &mbar[0]);
-        if (!p.scalar_gate) tma_load_3d(sm + S1_STG_G, &p.tm_g, 0, h, (int)t0, &mbar[0]);
+    auto pos_finish = [&](const PosRaw &r) {
+        Pos q{0, 0, 0};
+        if (r.ch < 0) return q;
+        int64_t bos = r.c0, eos = r.c1;
+        bos = bos < 0 ? 0 : (bos > p.T ? p.T : bos);
+        eos = eos < bos ? bos : (eos > p.T ? p.T : eos);
+        q.h = r.h;
+        q.t0 = bos + (int64_t)(r.ch - r.cb) * C;
+        q.L = (int)((eos - q.t0) < C ? (eos - q.t0) : C);
+        return q;
     };
-    if (tid == 0 && (int)blockIdx.x < ntask) issue_tma(blockIdx.x);
+    auto task_pos = [&](int task) { return pos_finish(pos_fetch(task)); };
+    // beta (and the scalar gate) of row `tid` of a task, read ahead into registers
+    auto row_params = [&](const Pos &q, int task, float &b, float &gs) {
+        b = 0.f; gs = 0.f;
+        if (tid < C && task < ntask && tid < q.L) {
+            b = p.beta[(q.t0 + tid) * H + q.h];
+            if (p.scalar_gate) gs = p.g[(q.t0 + tid) * H + q.h];
+        }
+    };
+    constexpr uint32_t TILE_BF16 = 16384, TILE_G = 32768;
+    auto expect_tma = [&]() {
+        mbar_arrive_expect_tx(&mbar[0], 3 * TILE_BF16 + (p.scalar_gate ? 0 : TILE_G));
+    };
+    auto tma_kqg = [&](const Pos &q) {
+        tma_load_3d(sm + S1_STG_K, &p.tm_k, 0, q.h, (int)q.t0, &mbar[0]);
+        tma_load_3d(sm + S1_STG_Q, &p.tm_q, 0, q.h, (int)q.t0, &mbar[0]);
+        if (!p.scalar_gate) tma_load_3d(sm + S1_STG_G, &p.tm_g, 0, q.h, (int)q.t0, &mbar[0]);
+    };
+    auto tma_v = [&](const Pos &q) {
+        tma_load_3d(sm + S1_STG_V, &p.tm_v, 0, q.h, (int)q.t0, &mbar[0]);
+    };
+    // W and U~ of a finished task: TMEM -> fp16 workspace images.  Row r of
+    // the M = 64 accumulators sits in lane r % 16 of quadrant r / 16; a warp
+    // reads its own quadrant.
+    auto store_wu_cols = [&](uint8_t *dst, int q, int col) {   // 16 columns
+        const int r = 16 * q + lane;
+        float w[16], u[16];
+        tmem_ld16(tmem_at(tmem, q, W_COL + col), w);
+        tmem_ld16(tmem_at(tmem, q, U_COL + col), u);
+        tmem_wait_ld();
+        if (lane < 16) {
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {
+                const int c0 = col + 8 * hc;
+                *reinterpret_cast<uint4 *>(dst + IMG_W + rc_img_off(r, c0)) = pack8_h(w + 8 * hc);
+                *reinterpret_cast<uint4 *>(dst + IMG_U + (c0 >> 5) * 4096 + r * 64 + (c0 & 31) * 2) =
+                    pack8_h(u + 8 * hc);
+            }
+        }
+    };
+    auto store_wu = [&](uint8_t *dst) {        // all 16 warps: 32 columns each
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) store_wu_cols(dst, warp & 3, 32 * (warp >> 2) + 16 * hh);
+    };
+    // The same, split so that the TMEM loads' latency overlaps other work:
+    // round hh (0, 1) of warp w covers columns 32 (w / 4) + 16 hh.
+    auto drain_issue = [&](int hh, float (&w)[16], float (&u)[16]) {
+        const int col = 32 * (warp >> 2) + 16 * hh;
+        tmem_ld16(tmem_at(tmem, warp & 3, W_COL + col), w);
+        tmem_ld16(tmem_at(tmem, warp & 3, U_COL + col), u);
+    };
+    auto drain_finish = [&](uint8_t *dst, int hh, float (&w)[16], float (&u)[16]) {
+        tmem_wait_ld();
+        reg_fence(w);
+        reg_fence(u);
+        const int col = 32 * (warp >> 2) + 16 * hh;
+        const int r = 16 * (warp & 3) + lane;
+        if (lane < 16) {
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {
+                const int c0 = col + 8 * hc;
+                *reinterpret_cast<uint4 *>(dst + IMG_W + rc_img_off(r, c0)) = pack8_h(w + 8 * hc);
+                *reinterpret_cast<uint4 *>(dst + IMG_U + (c0 >> 5) * 4096 + r * 64 + (c0 & 31) * 2) =
+                    pack8_h(u + 8 * hc);
+            }
+        }
+    };
+
+    // positions are resolved one task ahead of the one being loaded, so the
+    // offset-table lookups never sit on the critical path
+    int task = blockIdx.x;
+    Pos cur = task_pos(task), nxt = task_pos(task + stride);
+    float b_cur, gs_cur;
+    row_params(cur, task, b_cur, gs_cur);
+    uint32_t n_issued = 0, n_landed = 0;   // TMA phases (meaningful in thread 0, the issuer)
+    if (tid == 0 && task < ntask) { expect_tma(); tma_kqg(cur); tma_v(cur); n_issued = 1; }
 
     bool ok = true;
     uint32_t it = 0, ap_it = 0;
-    for (int task = blockIdx.x; task < ntask; task += gridDim.x, ++it) {
-        int h, L;
-        int64_t t0;
-        task_pos(task, h, t0, L);
+    uint8_t *out_prev = nullptr;
+    for (; task < ntask; task += stride, ++it) {
+        const int L = cur.L;
+        const int next = task + stride;
         uint8_t *out = img_base + (uint64_t)task * CH_STRIDE;
         if (tid < C) {
-            sB[tid] = tid < L ? p.beta[(t0 + tid) * H + h] : 0.f;
-            if (p.scalar_gate) sGs[tid] = tid < L ? p.g[(t0 + tid) * H + h] : 0.f;
+            sB[tid] = b_cur;
+            sGs[tid] = gs_cur;
         }
         ok = __syncthreads_and(mbar_wait(&mbar[0], it & 1));
         if (!ok) break;
+        ++n_landed;
+        // the previous task's W and U~ leave TMEM (this task's W/U MMA reuses
+        // the columns) in two rounds hidden behind the gate scan and the prep
+        float dw[16], du[16];
+        if (out_prev) drain_issue(0, dw, du);
 
         // ---- cumulative log-gate, in place (rows past the sequence: g = 0) ----
         // thread = (channel c, 16-row segment sg)
@@ -313,11 +476,17 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
             const int c = tid & 127, sg = tid >> 7;
             float *G = reinterpret_cast<float *>(sm + S1_STG_G);
             float v[16];
+            if (p.scalar_gate) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = sGs[16 * sg + j];
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = G[(16 * sg + j) * 128 + c];
+            }
             float acc = 0.f;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const int r = 16 * sg + j;
-                acc += r < L ? (p.scalar_gate ? sGs[r] : G[r * 128 + c]) : 0.f;
+                acc += 16 * sg + j < L ? v[j] : 0.f;
                 v[j] = acc;
             }
             tot[sg * 128 + c] = acc;
@@ -331,9 +500,15 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
                 eL[c] = __expf(acc + off);
             }
         }
+        if (out_prev) {
+            drain_finish(out_prev, 0, dw, du);
+            drain_issue(1, dw, du);
+        }
         const bool slow = __syncthreads_or(tid >= 384 && -gL[tid & 127] > RANGE_LIMIT);
 
         // ---- element-wise prep: unit = (row r, channels c0..c0+7) -------------
+        // tf32 operands [K e^g ; Q e^g] and K e^-g for A / P (not on the slow
+        // path), fp16 K e^g and V for W / U~, the Q^ and Kbar workspace images.
 #pragma unroll 1
         for (int jj = 0; jj < 2; ++jj) {
             const int u = tid + K1_THREADS * jj;
@@ -396,31 +571,41 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
                         make_float4(kh[4 * hc], kh[4 * hc + 1], kh[4 * hc + 2], kh[4 * hc + 3]);
                 }
             }
+            if (jj == 0 && out_prev) drain_finish(out_prev, 1, dw, du);
         }
+        if (tid < 128) reinterpret_cast<float *>(out + IMG_G)[tid] = eL[tid];
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
 
-        const int next = task + gridDim.x;
+        // ---- A and P: tf32 MMAs, M = 128 ([K e^g ; Q e^g]), N = 64 (K e^-g).
+        // Issuing one keeps its thread busy for a few hundred cycles, so the
+        // 16 K steps are spread over four issuers (warps 12-15, accumulator =
+        // channel atom); warp 12 then starts the next task's loads (every
+        // staging tile is consumed).  Meanwhile every thread resolves the
+        // task after next.
+        if (!slow && warp >= K1_ISSUER0 && lane == 0) {
+            const int atom = warp - K1_ISSUER0;
+            fence_after_sync();
+            const uint64_t da = sdesc_k_sw128(smem_addr(sm + S1_OPA));
+            const uint64_t db = sdesc_k_sw128(smem_addr(sm + S1_OPB));
+            const uint32_t id = idesc(128, 64, FMT_TF32, FMT_TF32, 0, 0);
+#pragma unroll
+            for (int s2 = 0; s2 < 4; ++s2) {   // 8 tf32 channels per step
+                const uint32_t wi = s2 * 32;
+                mma_tf32(tmem + AP_COL + 64 * atom, sdesc_add(da, atom * 16384 + wi),
+                         sdesc_add(db, atom * 8192 + wi), id, s2 > 0);
+            }
+            mma_commit(&mbar[1]);
+            if (atom == 0 && next < ntask) { expect_tma(); tma_kqg(nxt); tma_v(nxt); }
+        }
+        row_params(nxt, next, b_cur, gs_cur);              // consumed next task
+        const PosRaw nn_raw = pos_fetch(next + stride);    // finished after the W/U MMA
+
         float *As = reinterpret_cast<float *>(sm + S1_AS);
         if (!slow) {
-            // ---- A and P: tf32 MMAs, M = 128 ([K e^g ; Q e^g]), N = 64 (K e^-g).
-            // Issuing one tcgen05.mma occupies its thread for ~90 cycles, so the
-            // 16 K steps are spread over 4 issuing warps, one accumulator each.
-            if (lane == 0 && warp < 4) {
-                fence_after_sync();
-                const uint64_t da = sdesc_k_sw128(smem_addr(sm + S1_OPA));
-                const uint64_t db = sdesc_k_sw128(smem_addr(sm + S1_OPB));
-                const uint32_t id = idesc(128, 64, FMT_TF32, FMT_TF32, 0, 0);
-#pragma unroll
-                for (int s2 = 0; s2 < 4; ++s2) {   // channel atom `warp`, 8 tf32 per step
-                    const uint32_t wi = s2 * 32;
-                    mma_tf32(tmem + AP_COL + 64 * warp, sdesc_add(da, warp * 16384 + wi),
-                             sdesc_add(db, warp * 8192 + wi), id, s2 > 0);
-                }
-                mma_commit(&mbar[1]);
-                if (warp == 0 && next < ntask) issue_tma(next);   // staging is free
-            }
+            if (tid == 0 && next < ntask) ++n_issued;
+            fence_before_sync();
             ok = __syncthreads_and(mbar_wait(&mbar[1], ap_it & 1));
             ++ap_it;
             fence_after_sync();
@@ -438,10 +623,16 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
                 for (int e = 0; e < 16; ++e) d[e] = (d[e] + d1[e]) + (d2[e] + d3[e]);
                 if (row < 64) {
                     const float b = sB[row];
+                    float4 *arow = reinterpret_cast<float4 *>(As + row * LD + 16 * cb);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int i = 16 * cb + e;
-                        As[row * TP + i] = row > i ? b * d[e] : 0.f;
+                    for (int e4 = 0; e4 < 4; ++e4) {
+                        float a4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 16 * cb + 4 * e4 + e;
+                            a4[e] = row > i ? b * d[4 * e4 + e] : 0.f;
+                        }
+                        arow[e4] = make_float4(a4[0], a4[1], a4[2], a4[3]);
                     }
                 } else {
                     const int r = row - 64;
@@ -468,54 +659,24 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
                         pp += __bfloat162float(Qb[r * 128 + c]) * ki;
                     }
                 }
-                As[r * TP + i] = i < r ? sB[r] * a : 0.f;
+                As[r * LD + i] = i < r ? sB[r] * a : 0.f;
                 *reinterpret_cast<__half *>(out + IMG_P + sw128_off(r, i >> 3) + (i & 7) * 2) =
                     __float2half_rn(pp);
             }
+            fence_before_sync();
             __syncthreads();
-            if (tid == 0 && next < ntask) issue_tma(next);
+            if (tid == 0 && next < ntask) {   // staging is consumed
+                expect_tma(); tma_kqg(nxt); tma_v(nxt);
+                ++n_issued;
+            }
         }
         __syncthreads();
 
-        // ---- T = (I + A)^-1: 16x16 diagonal blocks, then block levels ---------
-        float *Ts = reinterpret_cast<float *>(sm + S1_TS);
-        if (tid < 64) {   // column j of diagonal block R, by forward substitution
-            const int R = tid >> 4, j = tid & 15;
-            const float *Ab = As + (16 * R) * TP + 16 * R;
-            float t[16];
-#pragma unroll
-            for (int m = 0; m < 16; ++m) t[m] = (m == j) ? 1.f : 0.f;
-#pragma unroll
-            for (int m = 1; m < 16; ++m) {
-                if (m > j) {
-                    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                    for (int i2 = 0; i2 < m; i2 += 2) {
-                        if (i2 >= j) s0 += Ab[m * TP + i2] * t[i2];
-                        if (i2 + 1 < m && i2 + 1 >= j) s1 += Ab[m * TP + i2 + 1] * t[i2 + 1];
-                    }
-                    t[m] = -(s0 + s1);
-                }
-            }
-#pragma unroll
-            for (int m = 0; m < 16; ++m) Ts[(16 * R + m) * TP + 16 * R + j] = t[m];
-        }
-        __syncthreads();
-        float *Ysc = reinterpret_cast<float *>(sm + S1_Y);
-        inverse_level<1>(As, Ts, Ysc, tid);
-        inverse_level<2>(As, Ts, Ysc, tid);
-        inverse_level<3>(As, Ts, Ysc, tid);
-        // T' = T Diag(beta) as an fp16 K-major SW128 image (row r, 64 columns)
-        {
-            const int r = tid >> 3, i0 = (tid & 7) * 8;
-            float tv[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int i = i0 + e;
-                tv[e] = i <= r ? Ts[r * TP + i] * sB[i] : 0.f;
-            }
-            *reinterpret_cast<uint4 *>(sm + S1_TP + sw128_off(r, i0 >> 3)) = pack8_h(tv);
-        }
+        // ---- T = (I + A)^-1 and the fp16 image of T' = T Diag(beta) (warps 0-5)
+        if (warp < 6)
+            invert_unit_lower(As, reinterpret_cast<float *>(sm + S1_TS),
+                              reinterpret_cast<float *>(sm + S1_TT),
+                              reinterpret_cast<float *>(sm + S1_FT), sB, sm + S1_TP, tid);
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
@@ -537,34 +698,18 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         ok = __syncthreads_and(mbar_wait(&mbar[2], it & 1));
         fence_after_sync();
         if (!ok) break;
-
-        // ---- epilogue: warp = (quadrant q, 32-column block cb); rows 16q + lane
-        {
-            const int q = warp & 3, cb = warp >> 2;
-            const int r = 16 * q + lane;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int col = 32 * cb + 16 * hh;
-                float w[16], u[16];
-                tmem_ld16(tmem_at(tmem, q, W_COL + col), w);
-                tmem_ld16(tmem_at(tmem, q, U_COL + col), u);
-                tmem_wait_ld();
-                if (lane < 16) {
-#pragma unroll
-                    for (int hc = 0; hc < 2; ++hc) {
-                        const int c0 = col + 8 * hc;
-                        *reinterpret_cast<uint4 *>(out + IMG_W + rc_img_off(r, c0)) = pack8_h(w + 8 * hc);
-                        *reinterpret_cast<uint4 *>(out + IMG_U + (c0 >> 5) * 4096 + r * 64 + (c0 & 31) * 2) =
-                            pack8_h(u + 8 * hc);
-                    }
-                }
-            }
-            if (tid < 128) reinterpret_cast<float *>(out + IMG_G)[tid] = eL[tid];
-        }
-        fence_before_sync();
-        __syncthreads();
+        out_prev = out;   // its W and U~ leave TMEM while the next task's A/P MMA runs
+        cur = nxt;
+        nxt = pos_finish(nn_raw);
     }
-    if (!ok && tid == 0) ws_fail(ws_hdr, 1);
+    if (ok && out_prev) store_wu(out_prev);
+    if (!ok) {
+        if (tid == 0) {
+            ws_fail(ws_hdr, 1);
+            // let copies still in flight land before the CTA's shared memory is released
+            if (n_issued > n_landed) mbar_wait(&mbar[0], (n_issued - 1) & 1, 1u << 20);
+        }
+    }
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc<512>(tmem);

@@ -112,6 +112,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// Registers filled by tcgen05.ld are defined only after tcgen05.wait::ld.
+// Passing them through an empty volatile asm after the wait stops the
+// compiler from moving their uses above it when the load was issued early.
+template <int N>
+__device__ __forceinline__ void reg_fence(float (&v)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i]));
+}
 // TMEM address of (lane quadrant base of this warp, column).
 __device__ __forceinline__ uint32_t tmem_at(uint32_t base, int warp, int col) {
     return base + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)col;

@@ -28,10 +28,29 @@ def _lib():
     kda.load()
 
 
+def _checked(fn):
+    """A prefill entry point with an explicit workspace whose device status
+    (a bounded wait that gave up) is checked after the call."""
+    def call(q, k, v, g, beta, cu_seqlens, S0=None, **kw):
+        T, H, dk = q.shape
+        need = kda.kda_prefill_workspace_size(cu_seqlens.shape[0] - 1, T, H, dk, v.shape[-1],
+                                              q.dtype)
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device) if need else None
+        out = fn(q, k, v, g, beta, cu_seqlens, S0, workspace=ws, **kw)
+        st = kda.kda_prefill_check(ws)
+        assert st == kda.KDA_OK, kda.status_string(st)
+        return out
+    return call
+
+
+prefill = _checked(kda.kda_prefill_chunked)
+gdn_prefill = _checked(kda.kda_gdn_prefill_chunked)
+
+
 def _run_prefill(inp, chunk=64, S0=None):
     S0 = inp["S0"] if S0 is None else S0
-    o, S_T = kda.kda_prefill_chunked(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
-                                     inp["cu_seqlens"], S0, chunk=chunk)
+    o, S_T = prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                     inp["cu_seqlens"], S0, chunk=chunk)
     torch.cuda.synchronize()
     return o, S_T
 
@@ -159,7 +178,7 @@ def test_prefill_long_context_workload():
     o_full, S_full = _run_prefill(inp)
     pre = {key: inp[key][:P] for key in ("q", "k", "v", "g", "beta")}
     pre["cu_seqlens"] = torch.tensor([0, P], dtype=torch.int32, device=DEV)
-    o_pre, S_pre = kda.kda_prefill_chunked(pre["q"], pre["k"], pre["v"], pre["g"],
+    o_pre, S_pre = prefill(pre["q"], pre["k"], pre["v"], pre["g"],
                                            pre["beta"], pre["cu_seqlens"], None)
     torch.cuda.synchronize()
     # (iii)
@@ -186,9 +205,9 @@ def test_resume_from_state_is_exact_on_chunk_boundaries():
     cu1 = torch.tensor([0, T1], dtype=torch.int32, device=DEV)
     cu2 = torch.tensor([0, 640 - T1], dtype=torch.int32, device=DEV)
     sl = lambda x, a, b: x[a:b].contiguous()
-    o1, S1 = kda.kda_prefill_chunked(*(sl(inp[n], 0, T1) for n in ("q", "k", "v", "g", "beta")),
+    o1, S1 = prefill(*(sl(inp[n], 0, T1) for n in ("q", "k", "v", "g", "beta")),
                                      cu1, inp["S0"])
-    o2, S2 = kda.kda_prefill_chunked(*(sl(inp[n], T1, 640) for n in ("q", "k", "v", "g", "beta")),
+    o2, S2 = prefill(*(sl(inp[n], T1, 640) for n in ("q", "k", "v", "g", "beta")),
                                      cu2, S1)
     torch.cuda.synchronize()
     assert torch.equal(torch.cat([o1, o2]), o)
@@ -200,7 +219,7 @@ def test_prefill_then_decode_matches_longer_prefill():
     inp = ki.prefill_inputs(cfg, device=DEV, seed=6)
     n_dec, T0 = 8, 192
     cu0 = torch.tensor([0, T0], dtype=torch.int32, device=DEV)
-    _, S = kda.kda_prefill_chunked(*(inp[n][:T0].contiguous() for n in ("q", "k", "v", "g", "beta")),
+    _, S = prefill(*(inp[n][:T0].contiguous() for n in ("q", "k", "v", "g", "beta")),
                                    cu0, inp["S0"])
     outs = []
     for t in range(T0, T0 + n_dec):
@@ -220,7 +239,7 @@ def test_state_in_place_alias_and_determinism():
     o_b, S_b = _run_prefill(inp)
     assert torch.equal(o_a, o_b) and torch.equal(S_a, S_b)
     S_io = inp["S0"].clone()
-    o_c, S_c = kda.kda_prefill_chunked(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+    o_c, S_c = prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
                                        inp["cu_seqlens"], S_io, S_T=S_io)
     torch.cuda.synchronize()
     assert S_c.data_ptr() == S_io.data_ptr()
@@ -235,7 +254,7 @@ def test_outputs_stay_inside_their_buffers():
     T, G = sum(lengths), 16
     o_buf = torch.full((T + 2 * G, 2, 128), 7.0, dtype=torch.bfloat16, device=DEV)
     s_buf = torch.full((2 + 2, 2, 128, 128), -3.0, dtype=torch.float32, device=DEV)
-    o, S_T = kda.kda_prefill_chunked(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+    o, S_T = prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
                                      inp["cu_seqlens"], inp["S0"], o=o_buf[G:G + T],
                                      S_T=s_buf[1:3])
     torch.cuda.synchronize()
@@ -254,7 +273,7 @@ def test_corrupt_offsets_stay_in_bounds():
     inp = ki.prefill_inputs(cfg, device=DEV, seed=9)
     cu = torch.tensor([0, 60, 1000, 5], dtype=torch.int32, device=DEV)
     S0 = torch.zeros((3, 2, 64, 64), device=DEV)
-    o, S_T = kda.kda_prefill_chunked(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+    o, S_T = prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
                                      cu, S0)
     torch.cuda.synchronize()
     o_ref, S_ref, _ = oracle.prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
@@ -327,7 +346,7 @@ def _head_gate(g):
 
 def _gdn_case(inp):
     gh = _head_gate(inp["g"])
-    o, S_T = kda.kda_gdn_prefill_chunked(inp["q"], inp["k"], inp["v"], gh, inp["beta"],
+    o, S_T = gdn_prefill(inp["q"], inp["k"], inp["v"], gh, inp["beta"],
                                          inp["cu_seqlens"], inp["S0"])
     torch.cuda.synchronize()
     o_ref, S_ref, _ = oracle.gdn_prefill(inp["q"], inp["k"], inp["v"], gh, inp["beta"],
