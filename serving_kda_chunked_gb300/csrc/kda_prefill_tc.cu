@@ -465,10 +465,6 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         ok = __syncthreads_and(mbar_wait(&mbar[0], it & 1));
         if (!ok) break;
         ++n_landed;
-        // the previous task's W and U~ leave TMEM (this task's W/U MMA reuses
-        // the columns) in two rounds hidden behind the gate scan and the prep
-        float dw[16], du[16];
-        if (out_prev) drain_issue(0, dw, du);
 
         // ---- cumulative log-gate, in place (rows past the sequence: g = 0) ----
         // thread = (channel c, 16-row segment sg)
@@ -500,11 +496,16 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
                 eL[c] = __expf(acc + off);
             }
         }
-        if (out_prev) {
-            drain_finish(out_prev, 0, dw, du);
-            drain_issue(1, dw, du);
-        }
+        // The previous task's W/U MMA ran under the scan; it must be done before
+        // the prep rewrites its B operands and before its results leave TMEM
+        // (this task's W/U MMA reuses the columns), in two rounds hidden behind
+        // the prep.
+        ok = __syncthreads_and(it == 0 || mbar_wait(&mbar[2], (it - 1) & 1));
+        fence_after_sync();
+        if (!ok) break;
         const bool slow = __syncthreads_or(tid >= 384 && -gL[tid & 127] > RANGE_LIMIT);
+        float dw[16], du[16];
+        if (out_prev) drain_issue(0, dw, du);
 
         // ---- element-wise prep: unit = (row r, channels c0..c0+7) -------------
         // tf32 operands [K e^g ; Q e^g] and K e^-g for A / P (not on the slow
@@ -571,8 +572,12 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
                         make_float4(kh[4 * hc], kh[4 * hc + 1], kh[4 * hc + 2], kh[4 * hc + 3]);
                 }
             }
-            if (jj == 0 && out_prev) drain_finish(out_prev, 1, dw, du);
+            if (jj == 0 && out_prev) {
+                drain_finish(out_prev, 0, dw, du);
+                drain_issue(1, dw, du);
+            }
         }
+        if (out_prev) drain_finish(out_prev, 1, dw, du);
         if (tid < 128) reinterpret_cast<float *>(out + IMG_G)[tid] = eL[tid];
         fence_async_smem();
         fence_before_sync();
@@ -693,22 +698,24 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
 #pragma unroll
             for (int s2 = 0; s2 < 4; ++s2)
                 mma_f16(tmem + col, sdesc_add(dt, 32 * s2), sdesc_add(db, 2048 * s2), id, s2 > 0);
-            mma_commit(&mbar[2]);
+            mma_commit(&mbar[2]);   // waited for after the next task's gate scan
         }
-        ok = __syncthreads_and(mbar_wait(&mbar[2], it & 1));
-        fence_after_sync();
-        if (!ok) break;
-        out_prev = out;   // its W and U~ leave TMEM while the next task's A/P MMA runs
+        out_prev = out;
         cur = nxt;
         nxt = pos_finish(nn_raw);
     }
-    if (ok && out_prev) store_wu(out_prev);
-    if (!ok) {
-        if (tid == 0) {
-            ws_fail(ws_hdr, 1);
-            // let copies still in flight land before the CTA's shared memory is released
-            if (n_issued > n_landed) mbar_wait(&mbar[0], (n_issued - 1) & 1, 1u << 20);
-        }
+    // the last W/U MMA, then its results
+    if (ok && it > 0) {
+        ok = __syncthreads_and(mbar_wait(&mbar[2], (it - 1) & 1));
+        fence_after_sync();
+        if (ok) store_wu(out_prev);
+    }
+    if (!ok && tid == 0) {
+        ws_fail(ws_hdr, 1);
+        // let copies and MMAs still in flight finish before the CTA's shared
+        // memory and TMEM are released (bounded waits)
+        if (n_issued > n_landed) mbar_wait(&mbar[0], (n_issued - 1) & 1, 1u << 20);
+        if (it > 0) mbar_wait(&mbar[2], (it - 1) & 1, 1u << 20);
     }
     fence_before_sync();
     __syncthreads();
