@@ -996,6 +996,292 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     if (warp == 0) tmem_dealloc<256>(tmem);
 }
 
+// ------------------------------------------------------------------------------
+// K2, wide form: one CTA of 512 threads per (sequence, head), for batches
+// with more chains than the GPU runs at once.  Warpgroup s (warps 4s..4s+3)
+// owns state columns 32s..32s+31; its thread t (0..127) holds row t (a dk
+// channel) of those columns in fp32 registers.  Every MMA spans the whole
+// state (N = 128), so one SM carries a whole head.  Per chunk:
+//   round 1: A_s + B_s = [W ; Q^] S   (M = 128, K = dk, split in halves over
+//            two issuers; rows 0-63 W S, 64-127 Q^ S)
+//   U = U~ - W S (fp16)                (rows 0-63: warps 0-1 of every warpgroup)
+//   round 2: B_s' = Kbar^T U           (M = 128, K = 64; first issuer)
+//            A_s += [0 ; P] U          (second issuer; rows 64-127 of A_s + B_s
+//                                       then hold O)
+//   S = Diag(e^gamma_last) S + B_s'.
+// TMEM holds two 128-column accumulators per set; chunk c uses set s = c % 2
+// for round 1 and the other set's B (whose previous contents, the last
+// chunk's outputs, have left TMEM during round 1) for Kbar^T U.  Operand
+// images arrive with bulk async copies, double buffered; a stage is reloaded
+// once the next chunk's round 1 is issued, when its last reader (the P U MMA)
+// has long finished.
+constexpr int K2W_THREADS = 512;
+constexpr uint32_t S2W_WQ = 0;          // [W ; Q^] K-major SW128, 2 atoms x 128 rows
+constexpr uint32_t S2W_KB = 32768;      // Kbar [r][c] SW128 (MN-major A)
+constexpr uint32_t S2W_PZ = 49152;      // [0 ; P] K-major SW128, 128 rows (rows 0-63 zero)
+constexpr uint32_t S2W_U = 65536;       // U~ [4 column blocks][64][32] fp16
+constexpr uint32_t S2W_G = 81920;       // e^gamma_last [128] fp32
+constexpr uint32_t S2W_STAGE = 82944;   // bytes per stage (multiple of 1024)
+constexpr uint32_t S2W_SOP = 2 * S2W_STAGE;                 // S fp16, K = 128 x N = 128, MN-major
+constexpr uint32_t S2W_UOP = S2W_SOP + 32768;               // U fp16, K = 64 x N = 128, MN-major
+constexpr uint32_t S2W_MISC = S2W_UOP + 16384;
+constexpr uint32_t S2W_BYTES = S2W_MISC + 256 + 1024;
+constexpr uint32_t S2W_TX = 4 * 8192 + 16384 + 8192 + 16384 + 512;   // bytes landing per stage
+// TMEM set s (0, 1) at column 256 s: A_s +0, B_s +128
+
+__global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    // [0..1] loads, [2] round 1 (two issuers), [3] round 2 state, [4] round 2 outputs
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + S2W_MISC);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 5);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wg = warp >> 2, wq = warp & 3;   // column block, TMEM lane quadrant
+    const int row = 32 * wq + lane;            // state row (dk channel) / TMEM lane
+    const int col0 = 32 * wg;                  // first state column of this thread
+    const int H = p.H;
+    const int h = blockIdx.x % H;
+    const int n = blockIdx.x / H;
+    int32_t *ws_hdr = reinterpret_cast<int32_t *>(p.ws);
+    const int32_t *chunk_base = reinterpret_cast<const int32_t *>(p.ws + WS_HEADER);
+    const uint8_t *img_base = p.ws + ws_images_offset(p.N);
+
+    const int cb = chunk_base[n], ce = chunk_base[n + 1];
+    const int a = max(cb, p.w0), b = min(ce, p.w1);
+    const int64_t sbase = ((int64_t)n * H + h) * D * D + (int64_t)row * D + col0;
+    if (cb == ce) {                       // empty sequence: pass the state through
+        if (p.w0 == 0) {
+            for (int j = 0; j < 32; j += 4) {
+                float4 x = p.S0 ? *reinterpret_cast<const float4 *>(p.S0 + sbase + j)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4 *>(p.S_T + sbase + j) = x;
+            }
+        }
+        return;
+    }
+    if (a >= b) return;                   // no chunk of this sequence in the window
+
+    int64_t bos, eos;
+    seq_bounds(p.cu, n, p.T, bos, eos);
+
+    float S[32];
+    {
+        const float *src = (a == cb) ? p.S0 : p.S_T;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            float4 x = src ? *reinterpret_cast<const float4 *>(src + sbase + j)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
+        }
+    }
+    // the zero half of [0 ; P] in both stages
+    for (int e = tid; e < 2 * 8192 / 16; e += K2W_THREADS) {
+        const int st = e / 512, off = (e % 512) * 16;
+        *reinterpret_cast<uint4 *>(sm + st * S2W_STAGE + S2W_PZ + off) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (tid == 0) {
+        for (int j = 0; j < 5; ++j) mbar_init(&mbar[j], j == 2 ? 2 : 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc<512>(tmem_slot);
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    auto issue_loads = [&](int ch, int stage) {
+        const uint8_t *src = img_base + ((uint64_t)(ch - p.w0) * H + h) * CH_STRIDE;
+        uint8_t *dst = sm + stage * S2W_STAGE;
+        uint64_t *mb = &mbar[stage];
+        mbar_arrive_expect_tx(mb, S2W_TX);
+        bulk_g2s(dst + S2W_WQ, src + IMG_W, 8192, mb);              // W, k 0-63
+        bulk_g2s(dst + S2W_WQ + 8192, src + IMG_Q, 8192, mb);       // Q^, k 0-63
+        bulk_g2s(dst + S2W_WQ + 16384, src + IMG_W + 8192, 8192, mb);
+        bulk_g2s(dst + S2W_WQ + 24576, src + IMG_Q + 8192, 8192, mb);
+        bulk_g2s(dst + S2W_KB, src + IMG_KT, 16384, mb);
+        bulk_g2s(dst + S2W_PZ + 8192, src + IMG_P, 8192, mb);
+        bulk_g2s(dst + S2W_U, src + IMG_U, 16384, mb);
+        bulk_g2s(dst + S2W_G, src + IMG_G, 512, mb);
+    };
+    if (tid == 0) {
+        issue_loads(a, 0);
+        if (a + 1 < b) issue_loads(a + 1, 1);
+    }
+    // chunk a + 1 is loaded up front; chunk c + 1 for c > a is loaded during
+    // chunk c (see round 1)
+
+    const uint64_t d_sop = sdesc(smem_addr(sm + S2W_SOP), 128, 2048, LAYOUT_NONE);
+    const uint64_t d_uop = sdesc(smem_addr(sm + S2W_UOP), 128, 1024, LAYOUT_NONE);
+    const uint32_t id_wq = idesc(128, 128, FMT_F16, FMT_F16, 0, 1);
+    const uint32_t id_kb = idesc(128, 128, FMT_F16, FMT_F16, 1, 1);
+
+    // O rows of a finished chunk (TMEM lanes 64-127: warps 2-3 of each group)
+    auto store_o = [&](int set, uint32_t phase, int64_t t0, int L) {
+        if (wq >= 2) {
+            const bool done = mbar_wait(&mbar[4], phase & 1);
+            fence_after_sync();
+            float oa[16], ob[16], pa[16], pb[16];
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + col0), oa);
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + col0 + 16), ob);
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + 128 + col0), pa);
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + 128 + col0 + 16), pb);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) { oa[j] += pa[j]; ob[j] += pb[j]; }
+            const int r = row - 64;
+            if (done && r < L) {
+                __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * D + col0;
+#pragma unroll
+                for (int gq = 0; gq < 4; ++gq) {
+                    const float *src = gq < 2 ? oa + 8 * gq : ob + 8 * (gq - 2);
+                    __nv_bfloat162 b0 = __floats2bfloat162_rn(src[0], src[1]);
+                    __nv_bfloat162 b1 = __floats2bfloat162_rn(src[2], src[3]);
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(src[4], src[5]);
+                    __nv_bfloat162 b3 = __floats2bfloat162_rn(src[6], src[7]);
+                    *reinterpret_cast<uint4 *>(dst + 8 * gq) = make_uint4(
+                        *reinterpret_cast<uint32_t *>(&b0), *reinterpret_cast<uint32_t *>(&b1),
+                        *reinterpret_cast<uint32_t *>(&b2), *reinterpret_cast<uint32_t *>(&b3));
+                }
+            }
+            return done;
+        }
+        return true;
+    };
+
+    bool ok = true;
+    int64_t prev_t0 = 0;
+    int prev_L = 0;
+    for (int ch = a; ch < b; ++ch) {
+        const int i = ch - a, stage = i & 1, set = i & 1;
+        uint8_t *st = sm + stage * S2W_STAGE;
+        const uint32_t acc_a = tmem + 256 * set, acc_b = acc_a + 128;   // round 1
+        const uint32_t acc_s = tmem + 256 * (set ^ 1) + 128;              // Kbar^T U
+        const int64_t t0 = bos + (int64_t)(ch - cb) * C;
+        const int L = (int)((eos - t0) < C ? (eos - t0) : C);
+        ok = __syncthreads_and(mbar_wait(&mbar[stage], (i >> 1) & 1));
+        if (!ok) break;
+
+        // S (fp16) -> B operand [K = dk][N = 128], MN-major, no swizzle:
+        // core matrix (8 K rows x 8 N) at (n/8) * 2048 + (k/8) * 128
+#pragma unroll
+        for (int gq = 0; gq < 4; ++gq) {
+            uint4 v4 = make_uint4(pack_h2(S[8 * gq + 0], S[8 * gq + 1]), pack_h2(S[8 * gq + 2], S[8 * gq + 3]),
+                                  pack_h2(S[8 * gq + 4], S[8 * gq + 5]), pack_h2(S[8 * gq + 6], S[8 * gq + 7]));
+            *reinterpret_cast<uint4 *>(sm + S2W_SOP + (4 * wg + gq) * 2048 + (row >> 3) * 128 + (row & 7) * 16) = v4;
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        if (lane == 0 && warp < 2) {      // round 1: warp w takes K atom w
+            fence_after_sync();
+            const uint64_t dwq = sdesc_k_sw128(smem_addr(st + S2W_WQ));
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4)
+                mma_f16(warp == 0 ? acc_a : acc_b, sdesc_add(dwq, warp * 16384 + s4 * 32),
+                        sdesc_add(d_sop, 256 * (4 * warp + s4)), id_wq, s4 > 0);
+            mma_commit(&mbar[2]);
+            // the previous chunk's P U MMA was the last reader of the other
+            // stage: reload it with the chunk after next
+            if (warp == 0 && i > 0 && ch + 1 < b) {
+                if (mbar_wait(&mbar[4], (i - 1) & 1)) issue_loads(ch + 1, stage ^ 1);
+                else ws_fail(ws_hdr, 2);
+            }
+        }
+        bool o_ok = true;
+        if (i > 0) o_ok = store_o(set ^ 1, (uint32_t)(i - 1), prev_t0, prev_L);
+        ok = __syncthreads_and(mbar_wait(&mbar[2], i & 1) && o_ok);
+        fence_after_sync();
+        if (!ok) break;
+
+        // U = U~ - W S for token rows 0-63 (warps 0-1 of each group)
+        if (wq < 2) {
+            float w0[16], w1[16], x0[16], x1[16];
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + col0), w0);
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + col0 + 16), w1);
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + 128 + col0), x0);
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + 128 + col0 + 16), x1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) { w0[j] += x0[j]; w1[j] += x1[j]; }
+            const int r = row;
+            const uint4 *ut = reinterpret_cast<const uint4 *>(st + S2W_U + wg * 4096 + r * 64);
+            float u[32];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const uint4 x = ut[q4];
+                const __half2 *h2 = reinterpret_cast<const __half2 *>(&x);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(h2[e]);
+                    const int j = 8 * q4 + 2 * e;
+                    const float wa = j < 16 ? w0[j] : w1[j - 16];
+                    const float wb = j + 1 < 16 ? w0[j + 1] : w1[j - 15];
+                    u[j] = f.x - wa;
+                    u[j + 1] = f.y - wb;
+                }
+            }
+#pragma unroll
+            for (int gq = 0; gq < 4; ++gq) {
+                uint4 v4 = make_uint4(pack_h2(u[8 * gq + 0], u[8 * gq + 1]), pack_h2(u[8 * gq + 2], u[8 * gq + 3]),
+                                      pack_h2(u[8 * gq + 4], u[8 * gq + 5]), pack_h2(u[8 * gq + 6], u[8 * gq + 7]));
+                *reinterpret_cast<uint4 *>(sm + S2W_UOP + (4 * wg + gq) * 1024 + (r >> 3) * 128 + (r & 7) * 16) = v4;
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        if (lane == 0 && warp < 2) {      // round 2: warp 0 Kbar^T U, warp 1 [0 ; P] U
+            fence_after_sync();
+            if (warp == 0) {
+                const uint64_t dkb = sdesc(smem_addr(st + S2W_KB), 8192, 1024, LAYOUT_SW128);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(acc_s, sdesc_add(dkb, 2048 * ks), sdesc_add(d_uop, 256 * ks), id_kb, ks > 0);
+                mma_commit(&mbar[3]);
+            } else {
+                const uint64_t dpz = sdesc_k_sw128(smem_addr(st + S2W_PZ));
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(acc_a, sdesc_add(dpz, 32 * ks), sdesc_add(d_uop, 256 * ks), id_wq, 1);
+                mma_commit(&mbar[4]);
+            }
+        }
+        ok = __syncthreads_and(mbar_wait(&mbar[3], i & 1));
+        fence_after_sync();
+        if (!ok) break;
+
+        // S = Diag(e^gamma_last) S + Kbar^T U
+        {
+            float da[16], db[16];
+            tmem_ld16(tmem_at(tmem, wq, 256 * (set ^ 1) + 128 + col0), da);
+            tmem_ld16(tmem_at(tmem, wq, 256 * (set ^ 1) + 128 + col0 + 16), db);
+            tmem_wait_ld();
+            const float gl = reinterpret_cast<const float *>(st + S2W_G)[row];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                S[j] = gl * S[j] + da[j];
+                S[16 + j] = gl * S[16 + j] + db[j];
+            }
+        }
+        prev_t0 = t0;
+        prev_L = L;
+        fence_before_sync();
+        __syncthreads();   // every thread is done with this stage's images
+    }
+    if (ok) ok = __syncthreads_and(store_o((b - 1 - a) & 1, (uint32_t)(b - 1 - a), prev_t0, prev_L));
+
+    if (!ok && tid == 0) ws_fail(ws_hdr, 2);
+#pragma unroll
+    for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4 *>(p.S_T + sbase + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc<512>(tmem);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -1054,6 +1340,9 @@ cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, cu
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S2_BYTES);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(chain_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)S2W_BYTES);
+        if (e != cudaSuccess) return e;
         attr_done = true;
     }
     int32_t *hdr = reinterpret_cast<int32_t *>(ws);
@@ -1088,7 +1377,15 @@ cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, cu
         K2Params p2;
         p2.S0 = a.S0; p2.S_T = a.S_T; p2.o = (__nv_bfloat16 *)a.o; p2.cu = a.cu_seqlens;
         p2.ws = ws; p2.N = a.N; p2.H = a.H; p2.T = a.T; p2.w0 = (int)w0; p2.w1 = (int)w1;
-        chain_kernel<<<(unsigned)((int64_t)a.N * a.H * NSLICE), K2_THREADS, S2_BYTES, st>>>(p2);
+        // A chain is latency-bound: one (sequence, head, 32-column slice) per
+        // SM finishes soonest when all slices run at once; with more than two
+        // waves of slices, one CTA per (sequence, head) carrying all four
+        // slices gets through about twice the chains per SM.
+        const int64_t slices = (int64_t)a.N * a.H * NSLICE;
+        if (slices > 2 * (int64_t)nsm)
+            chain_wide_kernel<<<(unsigned)((int64_t)a.N * a.H), K2W_THREADS, S2W_BYTES, st>>>(p2);
+        else
+            chain_kernel<<<(unsigned)slices, K2_THREADS, S2_BYTES, st>>>(p2);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -400,3 +400,40 @@ def test_gdn_decode_multi_step(d, dtype):
         torch.cuda.synchronize()
         assert_close("o step %d" % s, o, o_ref, TOL[DT[dtype]])
         assert_close("S step %d" % s, S, S_ref, TOL[DT[dtype]])
+
+
+# ---------------------------------------------------------------------------
+# many sequences (the one-CTA-per-head chain form) and degenerate gates
+# ---------------------------------------------------------------------------
+def test_prefill_many_short_sequences():
+    """120 packed sequences of 0-200 tokens, H=4: 1,920 state slices, more than
+    two waves, so the chain runs one CTA per (sequence, head)."""
+    gen = torch.Generator(device="cpu").manual_seed(31)
+    lengths = torch.randint(0, 201, (120,), generator=gen).tolist()
+    lengths[5] = 0
+    lengths[6] = 64
+    lengths[7] = 1
+    cfg = ki.PrefillConfig("many", H=4, d=128, dtype="bf16", n_seqs=len(lengths), s0_std=0.2)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=32, lengths=lengths)
+    o, S_T = _run_prefill(inp)
+    o_ref, S_ref = _oracle_prefill(inp)
+    assert_close("o", o, o_ref, 2e-3)
+    assert_close("S_T", S_T, S_ref, 2e-3)
+    assert torch.equal(S_T[5], inp["S0"][5])
+
+
+@pytest.mark.parametrize("case", ["beta0", "gate0"])
+def test_prefill_degenerate_gates(case):
+    """beta = 0: nothing is written, the state only decays (o_t = S_t^T q_t with
+    S_t = Diag(e^gamma_t) S0).  g = 0: no decay, the plain delta rule."""
+    lengths = [150, 64, 9]
+    cfg = ki.PrefillConfig("degen", H=2, d=128, dtype="bf16", n_seqs=len(lengths), s0_std=0.3)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=33, lengths=lengths)
+    if case == "beta0":
+        inp["beta"].zero_()
+    else:
+        inp["g"].zero_()
+    o, S_T = _run_prefill(inp)
+    o_ref, S_ref = _oracle_prefill(inp)
+    assert_close("o", o, o_ref, 2e-3)
+    assert_close("S_T", S_T, S_ref, 2e-3)
