@@ -760,7 +760,19 @@ struct K2Params {
     int N, H;
     int64_t T;
     int w0, w1;
+    // chunk-affine scan of one sequence (N = 1), see segment_launch_plan
+    int nseg;          // 0: off; else the window's chunks in nseg segments
+    int seg_len;       // chunks per segment
+    int phase;         // 0: segment maps (and segment 0 itself), 1: segments 1..nseg-1
+    float *smaps;      // [H][nseg][3][128][128] fp32: M_s, B_s, start state of segment s
 };
+
+// Roles of a chain CTA in a segment launch.
+enum : int { SEG_FULL = 0, SEG_B = 1, SEG_M = 2 };
+constexpr int SMAP_M = 0, SMAP_B = 1, SMAP_START = 2;
+__host__ __device__ inline float *smap(float *smaps, int nseg, int h, int s, int which) {
+    return smaps + ((((size_t)h * nseg + s) * 3 + which) << 14);   // 128 x 128 each
+}
 
 __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -772,17 +784,49 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H;
     const int unit = blockIdx.x;
-    const int slice = unit % NSLICE;
-    const int h = (unit / NSLICE) % H;
-    const int n = unit / (NSLICE * H);
+    int slice = unit % NSLICE;
+    int h = (unit / NSLICE) % H;
+    int n = unit / (NSLICE * H);
     int32_t *ws_hdr = reinterpret_cast<int32_t *>(p.ws);
     const int32_t *chunk_base = reinterpret_cast<const int32_t *>(p.ws + WS_HEADER);
     const uint8_t *img_base = p.ws + ws_images_offset(p.N);
 
+    // A segment launch (one sequence): phase 0 runs, per head, segment 0
+    // itself (slices 0-3) and, for each later segment, its state
+    // contribution from a zero start (B) and its homogeneous map from an
+    // identity start with U~ = 0 (M), four slices each; phase 1 runs
+    // segments 1.. from their start states.
+    int role = SEG_FULL, seg = 0;
+    if (p.nseg) {
+        n = 0;
+        if (p.phase == 0) {
+            const int per_head = 4 + 8 * (p.nseg - 1);
+            h = unit / per_head;
+            const int r = unit % per_head;
+            if (r < 4) {
+                slice = r;
+            } else {
+                seg = 1 + (r - 4) / 8;
+                role = ((r - 4) % 8) < 4 ? SEG_B : SEG_M;
+                slice = (r - 4) % 4;
+            }
+        } else {
+            const int per_head = 4 * (p.nseg - 1);
+            h = unit / per_head;
+            seg = 1 + (unit % per_head) / 4;
+            slice = unit % 4;
+        }
+    }
+
     const int cb = chunk_base[n], ce = chunk_base[n + 1];
-    const int a = max(cb, p.w0), b = min(ce, p.w1);
+    int a = max(cb, p.w0), b = min(ce, p.w1);
+    if (p.nseg) {
+        const int sa = a + seg * p.seg_len;
+        b = min(b, sa + p.seg_len);
+        a = sa;
+    }
     const int64_t sbase = ((int64_t)n * H + h) * D * D + (int64_t)tid * D + slice * DVS;
-    if (cb == ce) {                       // empty sequence: pass the state through
+    if (cb == ce && !p.nseg) {            // empty sequence: pass the state through
         if (p.w0 == 0) {
             for (int j = 0; j < DVS; j += 4) {
                 float4 x = p.S0 ? *reinterpret_cast<const float4 *>(p.S0 + sbase + j)
@@ -792,21 +836,36 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
         }
         return;
     }
-    if (a >= b) return;                   // no chunk of this sequence in the window
+    // no chunk of this sequence in the window (a segment launch still runs an
+    // empty segment: it maps its start state to itself)
+    if (a >= b && !p.nseg) return;
 
     int64_t bos, eos;
     seq_bounds(p.cu, n, p.T, bos, eos);
 
     float S[DVS];
-    {
+    if (role == SEG_M) {          // identity columns slice*32 .. slice*32+31
+#pragma unroll
+        for (int j = 0; j < DVS; ++j) S[j] = (tid == slice * DVS + j) ? 1.f : 0.f;
+    } else if (role == SEG_B) {
+#pragma unroll
+        for (int j = 0; j < DVS; ++j) S[j] = 0.f;
+    } else {
         const float *src = (a == cb) ? p.S0 : p.S_T;
+        int64_t off = sbase;
+        if (p.nseg && seg > 0) {  // the start state the combine step produced
+            src = smap(p.smaps, p.nseg, h, seg, SMAP_START);
+            off = (int64_t)tid * D + slice * DVS;
+        }
 #pragma unroll
         for (int j = 0; j < DVS; j += 4) {
-            float4 x = src ? *reinterpret_cast<const float4 *>(src + sbase + j)
+            float4 x = src ? *reinterpret_cast<const float4 *>(src + off + j)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
             S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
         }
     }
+    const bool write_o = role == SEG_FULL;
+    const float u_scale = role == SEG_M ? 0.f : 1.f;   // the homogeneous map drops U~
     // the zero half of [0 ; P] in both stages
     for (int e = tid; e < 2 * 8192 / 16; e += K2_THREADS) {
         const int st = e / 512, off = (e % 512) * 16;
@@ -840,7 +899,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
         bulk_g2s(dst + S2_U, src + IMG_U + slice * 4096, 4096, mb);
         bulk_g2s(dst + S2_G, src + IMG_G, 512, mb);
     };
-    if (tid == 0) {
+    if (tid == 0 && a < b) {
         issue_loads(a, 0);
         if (a + 1 < b) issue_loads(a + 1, 1);
     }
@@ -911,7 +970,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
                         sdesc_add(d_sop, 256 * (4 * warp + s)), id_wq, s > 0);
             mma_commit(&mbar[2]);
         }
-        if (i > 0) store_o(set ^ 1, prev_t0, prev_L);     // previous chunk's outputs
+        if (i > 0 && write_o) store_o(set ^ 1, prev_t0, prev_L);   // previous chunk's outputs
         ok = __syncthreads_and(mbar_wait(&mbar[2], i & 1));
         fence_after_sync();
         if (!ok) break;
@@ -929,8 +988,8 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
             float u[DVS];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                u[j] = __half2float(ut[j]) - (w0[j] + x0[j]);
-                u[16 + j] = __half2float(ut[16 + j]) - (w1[j] + x1[j]);
+                u[j] = u_scale * __half2float(ut[j]) - (w0[j] + x0[j]);
+                u[16 + j] = u_scale * __half2float(ut[16 + j]) - (w1[j] + x1[j]);
             }
 #pragma unroll
             for (int gq = 0; gq < DVS / 8; ++gq) {
@@ -985,15 +1044,80 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
         __syncthreads();   // every thread is done with this stage
         if (tid == 0 && ch + 2 < b) issue_loads(ch + 2, stage);
     }
-    if (ok) store_o((b - 1 - a) & 1, prev_t0, prev_L);
+    if (ok && write_o && a < b) store_o((b - 1 - a) & 1, prev_t0, prev_L);
 
     if (!ok && tid == 0) ws_fail(ws_hdr, 2);
+    // final state: S_T, or (segment launch) the segment's map, contribution
+    // or end state for the combine step; the last segment writes S_T
+    float *dst = nullptr;
+    if (!p.nseg || (p.phase == 1 && seg == p.nseg - 1))
+        dst = p.S_T + sbase;
+    else if (p.phase == 0)   // segment 0 ends in its B slot
+        dst = smap(p.smaps, p.nseg, h, seg, role == SEG_M ? SMAP_M : SMAP_B) + (int64_t)tid * D +
+              slice * DVS;
+    if (dst) {
 #pragma unroll
-    for (int j = 0; j < DVS; j += 4)
-        *reinterpret_cast<float4 *>(p.S_T + sbase + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        for (int j = 0; j < DVS; j += 4)
+            *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc<256>(tmem);
+}
+
+// Chunk-affine scan, combine step: a segment maps its start state S to
+// M_s S + B_s, so the start states follow in order from segment 0's end
+// state (stored in its B slot).  One CTA per (head, 32-column slice), fp32 on
+// CUDA cores: thread (row t, group of 8 columns); M_s is staged transposed in
+// shared memory (rows padded to 129 floats) so that a warp reads consecutive
+// rows of one column, and the slice of S is broadcast from shared memory
+// (rows of 40 floats, so that a thread's 8 columns are two 16-byte loads).
+constexpr int COMB_THREADS = 512;
+constexpr int SSH_LD = 40;
+constexpr uint32_t COMB_BYTES = (128 * 129 + 128 * SSH_LD) * sizeof(float);
+__global__ void __launch_bounds__(COMB_THREADS) segment_combine_kernel(float *smaps, int nseg) {
+    extern __shared__ float csm[];
+    float *Mt = csm;                  // [k][t] = M_s[t][k], row stride 129
+    float *Ssh = csm + 128 * 129;     // [k][j], row stride SSH_LD (16-byte aligned rows)
+    const int h = blockIdx.x / NSLICE, slice = blockIdx.x % NSLICE;
+    const int tid = threadIdx.x, t = tid & 127, g = tid >> 7;
+    const int64_t off = (int64_t)t * D + slice * DVS + 8 * g;
+    float S[8];
+    const float *e0 = smap(smaps, nseg, h, 0, SMAP_B) + off;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) S[j] = e0[j];
+    for (int sg = 1; sg < nseg; ++sg) {
+        float *start = smap(smaps, nseg, h, sg, SMAP_START) + off;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) start[j] = S[j];
+        if (sg == nseg - 1) break;
+        __syncthreads();   // the previous step is done with Mt and Ssh
+        const float4 *M4 = reinterpret_cast<const float4 *>(smap(smaps, nseg, h, sg, SMAP_M));
+        for (int e = tid; e < 128 * 32; e += COMB_THREADS) {
+            const int row = e >> 5, k4 = (e & 31) * 4;
+            const float4 m = M4[e];
+            Mt[(k4 + 0) * 129 + row] = m.x;
+            Mt[(k4 + 1) * 129 + row] = m.y;
+            Mt[(k4 + 2) * 129 + row] = m.z;
+            Mt[(k4 + 3) * 129 + row] = m.w;
+        }
+        *reinterpret_cast<float4 *>(Ssh + t * SSH_LD + 8 * g) = make_float4(S[0], S[1], S[2], S[3]);
+        *reinterpret_cast<float4 *>(Ssh + t * SSH_LD + 8 * g + 4) = make_float4(S[4], S[5], S[6], S[7]);
+        __syncthreads();
+        const float *Bv = smap(smaps, nseg, h, sg, SMAP_B) + off;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) S[j] = Bv[j];
+#pragma unroll 4
+        for (int k = 0; k < D; ++k) {
+            const float m = Mt[k * 129 + t];
+            const float4 s0 = *reinterpret_cast<const float4 *>(Ssh + k * SSH_LD + 8 * g);
+            const float4 s1 = *reinterpret_cast<const float4 *>(Ssh + k * SSH_LD + 8 * g + 4);
+            S[0] = fmaf(m, s0.x, S[0]); S[1] = fmaf(m, s0.y, S[1]);
+            S[2] = fmaf(m, s0.z, S[2]); S[3] = fmaf(m, s0.w, S[3]);
+            S[4] = fmaf(m, s1.x, S[4]); S[5] = fmaf(m, s1.y, S[5]);
+            S[6] = fmaf(m, s1.z, S[6]); S[7] = fmaf(m, s1.w, S[7]);
+        }
+    }
 }
 
 // ------------------------------------------------------------------------------
@@ -1322,17 +1446,55 @@ int sm_count() {
 
 }  // namespace
 
+namespace {
+
+// Chunk-affine scan plan for one sequence of `chunks` chunks and H heads.
+// The state chain of a (head, 32-column slice) is latency-bound, so when the
+// 4 H slice chains leave most SMs idle, the chunks are cut into segments:
+// phase 0 runs 4 + 8 (nseg - 1) chains per head, each over one segment (the
+// segment maps), a short combine step chains their start states, and phase 1
+// reruns segments 1.. (4 (nseg - 1) chains per head) for their outputs.  The
+// chain latency falls from `chunks` steps to about 2 chunks / nseg.  nseg is
+// held to (8 nseg - 4) H <= 128 so that phase 0 runs in one wave, and
+// segments keep at least 16 chunks; with fewer than 4 segments it is off.
+struct SegPlan { int nseg, seg_len; };
+SegPlan segment_plan(int32_t N, int32_t H, int64_t chunks) {
+    SegPlan pl{0, 0};
+    if (N != 1 || H <= 0) return pl;
+    const int64_t gmax = (128 / H + 4) / 8;
+    if (gmax < 4 || chunks < 4 * 16) return pl;
+    int64_t seg_len = (chunks + gmax - 1) / gmax;
+    if (seg_len < 16) seg_len = 16;
+    const int64_t nseg = (chunks + seg_len - 1) / seg_len;
+    if (nseg < 4) return pl;
+    pl.nseg = (int)nseg;
+    pl.seg_len = (int)seg_len;
+    return pl;
+}
+
+// bytes of segment maps for a window of `wch` chunks (0 when the scan is off)
+size_t smaps_bytes(int32_t N, int32_t H, int64_t wch) {
+    const SegPlan pl = segment_plan(N, H, wch);
+    return pl.nseg ? (size_t)H * pl.nseg * 3 * (D * D * sizeof(float)) : 0;
+}
+
+}  // namespace
+
 size_t prefill_tc_workspace_bytes(int32_t N, int64_t T, int32_t H) {
     const int64_t bound = (T + C - 1) / C + N;
     const int64_t wch = bound < WINDOW_CHUNKS ? bound : WINDOW_CHUNKS;
-    return (size_t)ws_images_offset(N) + (size_t)wch * (size_t)H * CH_STRIDE;
+    const size_t images = (size_t)ws_images_offset(N) + (size_t)wch * (size_t)H * CH_STRIDE;
+    const size_t maps = smaps_bytes(N, H, wch);
+    return maps ? ((images + 255) & ~(size_t)255) + maps : images;
 }
 
 namespace {
 
 // The prefill with windows of `window` chunks; `workspace` holds at least
-// ws_images_offset(N) + window * H * CH_STRIDE bytes.
-cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, cudaStream_t st) {
+// ws_images_offset(N) + window * H * CH_STRIDE bytes, plus (when `scan`) the
+// segment maps of the chunk-affine scan behind them.
+cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, bool scan,
+                           cudaStream_t st) {
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1343,7 +1505,15 @@ cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, cu
         e = cudaFuncSetAttribute(chain_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)S2W_BYTES);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(segment_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)COMB_BYTES);
+        if (e != cudaSuccess) return e;
         attr_done = true;
+    }
+    float *smaps = nullptr;
+    if (scan) {
+        const size_t images = (size_t)ws_images_offset(a.N) + (size_t)window * (size_t)a.H * CH_STRIDE;
+        smaps = reinterpret_cast<float *>(ws + ((images + 255) & ~(size_t)255));
     }
     int32_t *hdr = reinterpret_cast<int32_t *>(ws);
     const int64_t bound = (a.T + C - 1) / C + a.N;
@@ -1377,6 +1547,20 @@ cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, cu
         K2Params p2;
         p2.S0 = a.S0; p2.S_T = a.S_T; p2.o = (__nv_bfloat16 *)a.o; p2.cu = a.cu_seqlens;
         p2.ws = ws; p2.N = a.N; p2.H = a.H; p2.T = a.T; p2.w0 = (int)w0; p2.w1 = (int)w1;
+        p2.nseg = 0; p2.seg_len = 0; p2.phase = 0; p2.smaps = smaps;
+        const int64_t wch = (bound - w0) < window ? (bound - w0) : window;
+        const SegPlan pl = smaps ? segment_plan(a.N, a.H, wch) : SegPlan{0, 0};
+        if (pl.nseg) {            // chunk-affine scan over this window
+            p2.nseg = pl.nseg; p2.seg_len = pl.seg_len; p2.phase = 0;
+            chain_kernel<<<(unsigned)(a.H * (4 + 8 * (pl.nseg - 1))), K2_THREADS, S2_BYTES, st>>>(p2);
+            segment_combine_kernel<<<(unsigned)(a.H * NSLICE), COMB_THREADS, COMB_BYTES, st>>>(
+                smaps, pl.nseg);
+            p2.phase = 1;
+            chain_kernel<<<(unsigned)(a.H * 4 * (pl.nseg - 1)), K2_THREADS, S2_BYTES, st>>>(p2);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+            continue;
+        }
         // A chain is latency-bound: one (sequence, head, 32-column slice) per
         // SM finishes soonest when all slices run at once; with more than two
         // waves of slices, one CTA per (sequence, head) carrying all four
@@ -1403,7 +1587,8 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_BYTES];
 cudaError_t launch_prefill_tc(const PrefillArgs &a, void *workspace, cudaStream_t st) {
     const int64_t bound = (a.T + C - 1) / C + a.N;
     const int64_t window = bound < WINDOW_CHUNKS ? bound : WINDOW_CHUNKS;
-    return run_prefill_tc(a, static_cast<uint8_t *>(workspace), window, st);
+    return run_prefill_tc(a, static_cast<uint8_t *>(workspace), window,
+                          smaps_bytes(a.N, a.H, window) > 0, st);
 }
 
 int64_t noalloc_window_chunks(int32_t N, int32_t H) {
@@ -1436,7 +1621,7 @@ cudaError_t launch_prefill_tc_noalloc(const PrefillArgs &a, cudaStream_t st) {
     }
     const int64_t window = noalloc_window_chunks(a.N, a.H);
     if (window < 1) return cudaErrorInvalidValue;
-    return run_prefill_tc(a, static_cast<uint8_t *>(ws), window, st);
+    return run_prefill_tc(a, static_cast<uint8_t *>(ws), window, false, st);
 }
 
 }  // namespace kda

@@ -173,6 +173,11 @@ def test_workspace_size_query(lib):
     # long inputs are processed in windows of 2048 chunks
     big = kda.kda_prefill_workspace_size(1, 1 << 20, 32, 128, 128, kda.KDA_BF16)
     assert big == 1024 + 2048 * 32 * 74240
+    # one sequence with few heads adds the chunk-affine scan's segment maps:
+    # H=2, 129 chunks -> 8 segments, 3 fp32 128x128 matrices each per head
+    small = kda.kda_prefill_workspace_size(1, 8192, 2, 128, 128, kda.KDA_BF16)
+    images = 1024 + (8192 // 64 + 1) * 2 * 74240
+    assert small == ((images + 255) // 256) * 256 + 2 * 8 * 3 * 65536
     assert kda.kda_prefill_workspace_size(1, 8192, 32, 128, 128, kda.KDA_FP32) == 0
     assert kda.kda_prefill_workspace_size(1, 8192, 32, 64, 64, kda.KDA_BF16) == 0
     assert kda.kda_prefill_workspace_size(1, 8192, 32, 96, 96, kda.KDA_BF16) == 0

@@ -437,3 +437,29 @@ def test_prefill_degenerate_gates(case):
     o_ref, S_ref = _oracle_prefill(inp)
     assert_close("o", o, o_ref, 2e-3)
     assert_close("S_T", S_T, S_ref, 2e-3)
+
+
+# ---------------------------------------------------------------------------
+# chunk-affine scan: one long sequence with few heads, chunks cut into
+# segments whose maps are chained (phase 0 / combine / phase 1)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("H,T", [(2, 8192 + 37), (1, 20000)])
+def test_prefill_segment_scan(H, T):
+    cfg = ki.PrefillConfig("scan", H=H, d=128, dtype="bf16", T=T, s0_std=0.1)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=41)
+    o, S_T = _run_prefill(inp)
+    o_ref, S_ref = _oracle_prefill(inp)
+    assert_close("o", o, o_ref, 2e-3)
+    assert_close("S_T", S_T, S_ref, 2e-3)
+
+
+def test_prefill_segment_scan_two_windows():
+    """H=1, 140,000 tokens: 2,188 chunks, two windows of segments, the state
+    carried from the first window's last segment into the second."""
+    cfg = ki.PrefillConfig("scan2", H=1, d=128, dtype="bf16", T=140000, s0_std=0.1,
+                           gate_scale=0.1)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=42)
+    o, S_T = _run_prefill(inp)
+    o_ref, S_ref = _oracle_prefill(inp)
+    assert_close("o", o, o_ref, 2e-3)
+    assert_close("S_T", S_T, S_ref, 2e-3)
