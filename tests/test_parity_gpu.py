@@ -463,3 +463,12 @@ def test_prefill_segment_scan_two_windows():
     o_ref, S_ref = _oracle_prefill(inp)
     assert_close("o", o, o_ref, 2e-3)
     assert_close("S_T", S_T, S_ref, 2e-3)
+
+
+def test_gdn_prefill_segment_scan():
+    """One sequence, two heads, one gate per head: the chunk-affine scan path."""
+    cfg = ki.PrefillConfig("gdnscan", H=2, d=128, dtype="bf16", T=5000, s0_std=0.1)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=43)
+    o, S_T, o_ref, S_ref = _gdn_case(inp)
+    assert_close("o", o, o_ref, 2e-3)
+    assert_close("S_T", S_T, S_ref, 2e-3)
