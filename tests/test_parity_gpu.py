@@ -472,3 +472,46 @@ def test_gdn_prefill_segment_scan():
     o, S_T, o_ref, S_ref = _gdn_case(inp)
     assert_close("o", o, o_ref, 2e-3)
     assert_close("S_T", S_T, S_ref, 2e-3)
+
+
+# ---------------------------------------------------------------------------
+# CUDA graphs: both calls enqueue only kernels on the caller's stream, so a
+# captured graph replays them exactly
+# ---------------------------------------------------------------------------
+def test_prefill_and_decode_replay_in_a_cuda_graph():
+    cfg = ki.PrefillConfig("graph", H=4, d=128, dtype="bf16", T=700, s0_std=0.1)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=51)
+    dcfg = ki.DecodeConfig("graphd", B=3, H=4, d=128, steps=2, dtype="bf16")
+    dec = ki.decode_inputs(dcfg, device=DEV, seed=52)
+    T, H, d = inp["q"].shape
+    ws = torch.empty(kda.kda_prefill_workspace_size(1, T, H, d, d, torch.bfloat16),
+                     dtype=torch.uint8, device=DEV)
+    o = torch.empty_like(inp["v"])
+    S_T = torch.empty_like(inp["S0"])
+    S_dec = dec["S0"].clone()
+    o_dec = torch.empty_like(dec["v"][0])
+
+    def work():
+        kda.kda_prefill_chunked(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                inp["cu_seqlens"], inp["S0"], o=o, S_T=S_T, workspace=ws)
+        kda.kda_decode_step(dec["q"][0], dec["k"][0], dec["v"][0], dec["g"][0], dec["beta"][0],
+                            S_dec, o=o_dec)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        work()                                  # eager, on the capture stream
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    o_ref, S_ref, od_ref, Sd_ref = o.clone(), S_T.clone(), o_dec.clone(), S_dec.clone()
+
+    S_dec.copy_(dec["S0"])
+    o.zero_(); S_T.zero_(); o_dec.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        work()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert kda.kda_prefill_check(ws) == kda.KDA_OK
+    assert torch.equal(o, o_ref) and torch.equal(S_T, S_ref)
+    assert torch.equal(o_dec, od_ref) and torch.equal(S_dec, Sd_ref)
