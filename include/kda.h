@@ -245,6 +245,14 @@ kda_status kda_gdn_decode_step(const void *q, const void *k, const void *v,
                                int32_t B, int32_t H, int32_t dk, int32_t dv,
                                int32_t dtype, void *o, void *stream);
 
+/* Gated DeltaNet decode over a state-slot pool: kda_decode_step_pooled with
+ * one log-gate per head, g [B, H] float32 (4-byte alignment suffices). */
+kda_status kda_gdn_decode_step_pooled(const void *q, const void *k, const void *v,
+                                      const float *g, const float *beta, float *S_pool,
+                                      const int32_t *slots, int32_t P, int32_t B, int32_t H,
+                                      int32_t dk, int32_t dv, int32_t dtype, void *o,
+                                      void *stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char *kda_status_string(int32_t status);
 

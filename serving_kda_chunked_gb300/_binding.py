@@ -75,6 +75,8 @@ def load() -> ctypes.CDLL:
         lib.kda_decode_step_pooled.argtypes = [
             vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
         lib.kda_decode_step_pooled.restype = ctypes.c_int
+        lib.kda_gdn_decode_step_pooled.argtypes = lib.kda_decode_step_pooled.argtypes
+        lib.kda_gdn_decode_step_pooled.restype = ctypes.c_int
         lib.kda_status_string.argtypes = [i32]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_abi_version.argtypes = []
@@ -225,13 +227,7 @@ def kda_gdn_decode_step(q, k, v, g, beta, S, *, o=None, stream=None):
                    stream)
 
 
-def kda_decode_step_pooled(q, k, v, g, beta, S_pool, slots, *, o=None, stream=None):
-    """Batched decode over a pool of states (``kda_decode_step_pooled`` in kda.h).
-
-    S_pool [P, H, dk, dv] fp32; slots [B] int32 on the device (a value outside
-    [0, P) skips that sequence).  The named slots are updated in place.
-    Returns o [B, H, dv].
-    """
+def _decode_pooled(fn, gate_shape, q, k, v, g, beta, S_pool, slots, o, stream):
     _check_cuda("q", q)
     if q.dtype not in _DTYPE_CODE:
         raise ValueError("q must be bfloat16 or float32")
@@ -239,7 +235,7 @@ def kda_decode_step_pooled(q, k, v, g, beta, S_pool, slots, *, o=None, stream=No
     dv = v.shape[-1]
     _check_cuda("k", k, q.dtype, (B, H, dk))
     _check_cuda("v", v, q.dtype, (B, H, dv))
-    _check_cuda("g", g, torch.float32, (B, H, dk))
+    _check_cuda("g", g, torch.float32, gate_shape(B, H, dk))
     _check_cuda("beta", beta, torch.float32, (B, H))
     _check_cuda("S_pool", S_pool, torch.float32)
     if S_pool.dim() != 4 or tuple(S_pool.shape[1:]) != (H, dk, dv):
@@ -248,9 +244,27 @@ def kda_decode_step_pooled(q, k, v, g, beta, S_pool, slots, *, o=None, stream=No
     if o is None:
         o = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
     _check_cuda("o", o, q.dtype, (B, H, dv))
-    st = load().kda_decode_step_pooled(
+    st = getattr(load(), fn)(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S_pool), _ptr(slots),
         S_pool.shape[0], B, H, dk, dv, _DTYPE_CODE[q.dtype], _ptr(o), _stream(stream))
     if st != KDA_OK:
-        raise KdaError("kda_decode_step_pooled", st)
+        raise KdaError(fn, st)
     return o
+
+
+def kda_decode_step_pooled(q, k, v, g, beta, S_pool, slots, *, o=None, stream=None):
+    """Batched decode over a pool of states (``kda_decode_step_pooled`` in kda.h).
+
+    S_pool [P, H, dk, dv] fp32; slots [B] int32 on the device (a value outside
+    [0, P) skips that sequence).  The named slots are updated in place.
+    Returns o [B, H, dv].
+    """
+    return _decode_pooled("kda_decode_step_pooled", lambda B, H, dk: (B, H, dk), q, k, v, g,
+                          beta, S_pool, slots, o, stream)
+
+
+def kda_gdn_decode_step_pooled(q, k, v, g, beta, S_pool, slots, *, o=None, stream=None):
+    """Gated DeltaNet decode over a pool of states (``kda_gdn_decode_step_pooled``
+    in kda.h): as ``kda_decode_step_pooled`` with g [B, H] fp32."""
+    return _decode_pooled("kda_gdn_decode_step_pooled", lambda B, H, dk: (B, H), q, k, v, g,
+                          beta, S_pool, slots, o, stream)

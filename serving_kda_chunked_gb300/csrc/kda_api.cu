@@ -185,6 +185,15 @@ kda_status kda_decode_step_pooled(const void *q, const void *k, const void *v,
                        stream);
 }
 
+kda_status kda_gdn_decode_step_pooled(const void *q, const void *k, const void *v,
+                                      const float *g, const float *beta, float *S_pool,
+                                      const int32_t *slots, int32_t P, int32_t B, int32_t H,
+                                      int32_t dk, int32_t dv, int32_t dtype, void *o,
+                                      void *stream) {
+    return decode_impl(q, k, v, g, beta, S_pool, slots, P, true, B, H, dk, dv, dtype, o, true,
+                       stream);
+}
+
 const char *kda_status_string(int32_t status) {
     switch (status) {
     case KDA_OK: return "KDA_OK";

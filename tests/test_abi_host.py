@@ -119,12 +119,12 @@ def test_decode_host_validation(lib, kw, expect):
     assert _decode(lib, **kw) == expect
 
 
-def _decode_pooled(lib, **kw):
+def _decode_pooled(lib, fn="kda_decode_step_pooled", **kw):
     a = dict(q=P, k=P, v=P, g=P, beta=P, S=P, slots=P, Pn=8, B=4, H=2, dk=128, dv=128,
              dtype=0, o=P)
     a.update(kw)
     vp = ctypes.c_void_p
-    return lib.kda_decode_step_pooled(
+    return getattr(lib, fn)(
         vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), vp(a["S"]),
         vp(a["slots"]), a["Pn"], a["B"], a["H"], a["dk"], a["dv"], a["dtype"], vp(a["o"]), None)
 
@@ -139,6 +139,8 @@ def _decode_pooled(lib, **kw):
 ])
 def test_decode_pooled_host_validation(lib, kw, expect):
     assert _decode_pooled(lib, **kw) == expect
+    if "dk" not in kw:   # the per-head-gate form validates the same way (g: 4-byte alignment)
+        assert _decode_pooled(lib, fn="kda_gdn_decode_step_pooled", **kw) == expect
 
 
 @pytest.mark.parametrize("kw,expect", [

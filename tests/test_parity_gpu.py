@@ -515,3 +515,33 @@ def test_prefill_and_decode_replay_in_a_cuda_graph():
     assert kda.kda_prefill_check(ws) == kda.KDA_OK
     assert torch.equal(o, o_ref) and torch.equal(S_T, S_ref)
     assert torch.equal(o_dec, od_ref) and torch.equal(S_dec, Sd_ref)
+
+
+def test_gdn_decode_pooled_slots():
+    """Per-head gates over a state-slot pool."""
+    P, B, H, d = 9, 5, 2, 128
+    cfg = ki.DecodeConfig("gpool", B=B, H=H, d=d, steps=2, dtype="bf16")
+    inp = ki.decode_inputs(cfg, device=DEV, seed=53)
+    gen = torch.Generator(device="cpu").manual_seed(54)
+    pool = (torch.randn((P, H, d, d), generator=gen) * 0.05).to(DEV)
+    ref = pool.double().cpu().numpy()
+    for s in range(2):
+        perm = torch.randperm(P, generator=gen)[:B].to(torch.int32)
+        perm[1] = -3
+        slots = perm.to(DEV)
+        before = pool.clone()
+        gh = _head_gate(inp["g"][s])
+        o = kda.kda_gdn_decode_step_pooled(inp["q"][s], inp["k"][s], inp["v"][s], gh,
+                                           inp["beta"][s], pool, slots)
+        torch.cuda.synchronize()
+        live = [b for b in range(B) if 0 <= int(perm[b]) < P]
+        idx = [int(perm[b]) for b in live]
+        o_ref, S_new = oracle.gdn_decode_step(inp["q"][s][live], inp["k"][s][live],
+                                              inp["v"][s][live], gh[live], inp["beta"][s][live],
+                                              ref[idx])
+        ref[idx] = S_new
+        assert_close("o", o[live], o_ref, 2e-3)
+        assert_close("pool slots", pool[idx], S_new, 2e-3)
+        assert torch.all(o[1] == 0)
+        untouched = [p for p in range(P) if p not in idx]
+        assert torch.equal(pool[untouched], before[untouched])
