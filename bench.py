@@ -60,19 +60,29 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def source_digest(sources: list[str]) -> str:
+    """sha256 of the sources' code with comments and blank lines removed, so
+    that only a change of code (not of its comments) invalidates a profile."""
+    h = hashlib.sha256()
+    for s in sources:
+        with open(os.path.join(ROOT, s)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        lines = [ln.rstrip() for ln in text.splitlines()]
+        h.update("\n".join(ln for ln in lines if ln.strip()).encode())
+    return h.hexdigest()
+
+
 def kernel_traffic(kernel: str, sources: list[str]):
     """Per-launch DRAM bytes from the committed ncu summary of ``kernel``, or
-    None when there is none or when the kernel's sources changed since."""
+    None when there is none or when the kernel's code changed since."""
     path = os.path.join(ROOT, "profiles", "%s.md" % kernel)
     if not os.path.exists(path):
         return None
-    h = hashlib.sha256()
-    for s in sources:
-        with open(os.path.join(ROOT, s), "rb") as f:
-            h.update(f.read())
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+source_sha256:\s*([0-9a-f]{64})", text)
-    if not m or m.group(2) != h.hexdigest():
+    if not m or m.group(2) != source_digest(sources):
         return None
     return float(m.group(1))
 

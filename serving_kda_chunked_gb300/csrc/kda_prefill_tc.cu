@@ -25,7 +25,10 @@
 //  * chain_kernel (K2) walks the chunks of one (sequence, head, block of 32
 //    state columns) in order with the fp32 state in registers: W S and Q^ S,
 //    then K^T U and P U, each a tcgen05 round trip.  Operand images arrive
-//    with bulk async copies, double buffered.
+//    with bulk async copies, double buffered.  chain_wide_kernel is the same
+//    walk for all 128 columns in one CTA (for batches with many chains); for
+//    one sequence with few heads, the chunk-affine scan runs the slice chains
+//    over segments and chains the segments' maps (segment_combine_kernel).
 //
 // Gate factors inside a chunk are referenced to the chunk start (K e^gamma,
 // K e^-gamma), which stays inside fp32 while every channel's log-gate sum over
@@ -139,23 +142,25 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 // ------------------------------------------------------------------------------
 // K1: intra-chunk kernel
 // ------------------------------------------------------------------------------
-// One CTA per SM walks (chunk, head) tasks.  Per task:
+// One CTA per SM walks (chunk, head) tasks, chunk-major.  Per task:
 //   1. TMA brings k, q, v (bf16) and g (fp32) rows [t0, t0 + 64) of head h
-//      into staging, issued during the previous task: k, q and g once its
-//      MMA operands are formed, v once its fp16 images are.
-//   2. Per-channel cumulative log-gate (in place), e^gamma_last, range check.
+//      into staging; issued during the previous task, as soon as its prep
+//      has consumed the staging tiles.
+//   2. Per-channel cumulative log-gate (in place), e^gamma_last, range check;
+//      the previous task's W/U MMA finishes underneath.
 //   3. Element-wise prep, 8 channels of one row per unit: tf32 operands
-//      [K e^g ; Q e^g] and K e^-g for A / P.
-//   4. One M = 128 tf32 MMA: rows 0-63 give A / beta, rows 64-127 give P.
-//      A chunk whose decay exceeds e^80 on some channel would overflow those
-//      factors, so it takes an exact pairwise CUDA-core path instead.
-//      While that MMA runs, the fp16 images (K e^g and V for W / U~, the Q^
-//      and Kbar workspace images) are formed from the tf32 operands, and the
-//      previous task's W and U~ leave TMEM for the workspace.
-//   5. T = (I + A)^-1 on CUDA cores (fp32, 16 x 16 blocks, register-tiled
-//      block forward substitution), T' = T Diag(beta) as fp16.
-//   6. W = T' (K e^g), U~ = T' V on tcgen05 (fp16); they stay in TMEM until
-//      the next task's A/P MMA is running.
+//      [K e^g ; Q e^g] and K e^-g for A / P, fp16 K e^g and V for W / U~, the
+//      Q^ and Kbar workspace images; the previous task's W and U~ leave TMEM
+//      for the workspace in two rounds hidden behind it.
+//   4. One M = 128 tf32 MMA group (warps 12-15 issue one channel atom each):
+//      rows 0-63 give A / beta, rows 64-127 give P.  A chunk whose decay
+//      exceeds e^80 on some channel would overflow those factors, so it takes
+//      an exact pairwise CUDA-core path instead.
+//   5. T = (I + A)^-1 on CUDA cores by warps 0-5 (fp32, 16 x 16 blocks,
+//      register-tiled block forward substitution), written as the fp16 image
+//      of T' = T Diag(beta).
+//   6. W = T' (K e^g), U~ = T' V on tcgen05 (fp16), waited for in step 2 of
+//      the next task.
 constexpr int K1_THREADS = 512;
 constexpr int K1_ISSUER0 = 12;  // warps 12-15 issue the A/P MMAs
 constexpr uint32_t S1_STG_K = 0, S1_STG_Q = 16384, S1_STG_V = 32768;  // bf16 [64][128]
