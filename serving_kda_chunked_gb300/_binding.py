@@ -165,6 +165,44 @@ def _prefill(fn, gate_shape, q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_T, wo
     return o, S_T
 
 
+def kda_noalloc_scratch_bytes() -> int:
+    """Size of the fixed device scratch behind ``kda_prefill_chunked_noalloc``."""
+    return int(load().kda_noalloc_scratch_bytes())
+
+
+def kda_prefill_chunked_noalloc(q, k, v, g, beta, cu_seqlens, S0=None, *, chunk: int = 64,
+                                o=None, S_T=None, stream=None):
+    """``kda_prefill_chunked`` without a workspace (``kda_prefill_chunked_noalloc``
+    in kda.h): scratch lives in a fixed device array inside the library; calls
+    that overlap on the GPU must not share it.  Outputs as ``kda_prefill_chunked``
+    (pass ``o`` / ``S_T`` to keep the call free of allocation)."""
+    _check_cuda("q", q)
+    if q.dtype not in _DTYPE_CODE:
+        raise ValueError("q must be bfloat16 or float32")
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    _check_cuda("k", k, q.dtype, (T, H, dk))
+    _check_cuda("v", v, q.dtype, (T, H, dv))
+    _check_cuda("g", g, torch.float32, (T, H, dk))
+    _check_cuda("beta", beta, torch.float32, (T, H))
+    _check_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    N = cu_seqlens.shape[0] - 1
+    if S0 is not None:
+        _check_cuda("S0", S0, torch.float32, (N, H, dk, dv))
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
+    _check_cuda("o", o, q.dtype, (T, H, dv))
+    if S_T is None:
+        S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    _check_cuda("S_T", S_T, torch.float32, (N, H, dk, dv))
+    st = load().kda_prefill_chunked_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
+        N, T, H, dk, dv, _DTYPE_CODE[q.dtype], int(chunk), _ptr(o), _ptr(S_T), _stream(stream))
+    if st != KDA_OK:
+        raise KdaError("kda_prefill_chunked_noalloc", st)
+    return o, S_T
+
+
 def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, S0=None, *, chunk: int = 64,
                         o=None, S_T=None, workspace=None, stream=None):
     """Chunked KDA prefill over a packed batch (``kda_prefill_chunked`` in kda.h).

@@ -185,8 +185,15 @@ def test_workspace_size_query(lib):
     assert kda.kda_prefill_workspace_size(1, 8192, 32, 96, 96, kda.KDA_BF16) == 0
 
 
+def test_noalloc_scratch_size(lib):
+    assert kda.kda_noalloc_scratch_bytes() == 64 << 20
+
+
 def test_binding_rejects_host_tensors(lib):
     import torch
     q = torch.zeros(4, 2, 64)
     with pytest.raises(ValueError, match="CUDA"):
         kda.kda_decode_step(q, q, q, q, torch.zeros(4, 2), torch.zeros(4, 2, 64, 64))
+    with pytest.raises(ValueError, match="CUDA"):
+        kda.kda_prefill_chunked_noalloc(q, q, q, q, torch.zeros(4, 2),
+                                        torch.zeros(2, dtype=torch.int32))

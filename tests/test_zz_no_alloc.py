@@ -84,3 +84,17 @@ def test_noalloc_rejects_what_does_not_fit(lib):
                                          _stream())
     assert st == kda.KDA_ERR_TOO_LARGE
     assert "no-allocation" in kda.status_string(st)
+
+
+def test_noalloc_through_the_python_binding():
+    """The binding's wrapper of the no-allocation entry point gives the same
+    outputs as the regular call, into caller buffers."""
+    cfg = ki.PrefillConfig("na_py", H=4, d=128, dtype="bf16", T=1000, s0_std=0.1)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=61)
+    args = (inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["cu_seqlens"], inp["S0"])
+    o_ref, S_ref = kda.kda_prefill_chunked(*args)
+    o = torch.empty_like(o_ref)
+    S_T = torch.empty_like(S_ref)
+    kda.kda_prefill_chunked_noalloc(*args, o=o, S_T=S_T)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(S_T, S_ref)
