@@ -60,6 +60,11 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+PREFILL_SOURCES = ["serving_kda_chunked_gb300/csrc/%s" % f for f in (
+    "kda_prefill_tc.cuh", "kda_prefill_intra.cu", "kda_prefill_chain.cu", "kda_prefill_tc.cu",
+    "kda_tc.cuh")]
+
+
 def source_digest(sources: list[str]) -> str:
     """sha256 of the sources' code with comments and blank lines removed, so
     that only a change of code (not of its comments) invalidates a profile."""
@@ -423,9 +428,7 @@ def run_ours(args):
     achieved = bytes_launch / launch_s / 1e9
     flops_launch = T_PREFILL * PREFILL_FLOPS_PER_TOKEN
     tflops = flops_launch / launch_s / 1e12
-    traffic = kernel_traffic("prefill_tc_single_T8192",
-                             ["serving_kda_chunked_gb300/csrc/kda_prefill_tc.cu",
-                              "serving_kda_chunked_gb300/csrc/kda_tc.cuh"])
+    traffic = kernel_traffic("prefill_tc_single_T8192", PREFILL_SOURCES)
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "traffic": traffic,

@@ -1,0 +1,640 @@
+// kda_prefill_chain.cu -- the state chain of the tensor-core prefill: the
+// slice form, the combine step of the chunk-affine scan and the wide form
+// (layouts and the method overview in kda_prefill_tc.cuh).
+#include "kda_prefill_tc.cuh"
+
+namespace kda {
+namespace tcp {
+
+// ------------------------------------------------------------------------------
+// K2: chain kernel
+// ------------------------------------------------------------------------------
+// One CTA of 128 threads per (sequence, head, block of 32 state columns);
+// thread t owns row t (a dk channel) of the fp32 state.  Per chunk:
+//   round 1: D_A + D_B = [W ; Q^] S   (M = 128: rows 0-63 W S, 64-127 Q^ S;
+//            K steps 0-3 into D_A by warp 0, 4-7 into D_B by warp 1)
+//   U = U~ - W S (fp16);
+//   round 2: D_S + D_S2 = Kbar^T U (warps 0 and 1, two K steps each),
+//            D_A += [0 ; P] U (warp 2; rows 64-127 then hold O - Q^S_B)
+//   S = Diag(e^gamma_last) S + D_S + D_S2.
+// A thread issuing tcgen05.mma is busy for ~90 cycles per instruction, so the
+// few MMAs on the state's critical path are spread over several issuing warps.
+// TMEM accumulators alternate between two sets so that the outputs of chunk
+// i are read while the MMAs of chunk i + 1 run.
+__global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + S2_MISC);   // [0..1] loads, [2] r1, [3] r2
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = p.H;
+    const int unit = blockIdx.x;
+    int slice = unit % NSLICE;
+    int h = (unit / NSLICE) % H;
+    int n = unit / (NSLICE * H);
+    int32_t *ws_hdr = reinterpret_cast<int32_t *>(p.ws);
+    const int32_t *chunk_base = reinterpret_cast<const int32_t *>(p.ws + WS_HEADER);
+    const uint8_t *img_base = p.ws + ws_images_offset(p.N);
+
+    // A segment launch (one sequence): phase 0 runs, per head, segment 0
+    // itself (slices 0-3) and, for each later segment, its state
+    // contribution from a zero start (B) and its homogeneous map from an
+    // identity start with U~ = 0 (M), four slices each; phase 1 runs
+    // segments 1.. from their start states.
+    int role = SEG_FULL, seg = 0;
+    if (p.nseg) {
+        n = 0;
+        if (p.phase == 0) {
+            const int per_head = 4 + 8 * (p.nseg - 1);
+            h = unit / per_head;
+            const int r = unit % per_head;
+            if (r < 4) {
+                slice = r;
+            } else {
+                seg = 1 + (r - 4) / 8;
+                role = ((r - 4) % 8) < 4 ? SEG_B : SEG_M;
+                slice = (r - 4) % 4;
+            }
+        } else {
+            const int per_head = 4 * (p.nseg - 1);
+            h = unit / per_head;
+            seg = 1 + (unit % per_head) / 4;
+            slice = unit % 4;
+        }
+    }
+
+    const int cb = chunk_base[n], ce = chunk_base[n + 1];
+    int a = max(cb, p.w0), b = min(ce, p.w1);
+    if (p.nseg) {
+        const int sa = a + seg * p.seg_len;
+        b = min(b, sa + p.seg_len);
+        a = sa;
+    }
+    const int64_t sbase = ((int64_t)n * H + h) * D * D + (int64_t)tid * D + slice * DVS;
+    if (cb == ce && !p.nseg) {            // empty sequence: pass the state through
+        if (p.w0 == 0) {
+            for (int j = 0; j < DVS; j += 4) {
+                float4 x = p.S0 ? *reinterpret_cast<const float4 *>(p.S0 + sbase + j)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4 *>(p.S_T + sbase + j) = x;
+            }
+        }
+        return;
+    }
+    // no chunk of this sequence in the window (a segment launch still runs an
+    // empty segment: it maps its start state to itself)
+    if (a >= b && !p.nseg) return;
+
+    int64_t bos, eos;
+    seq_bounds(p.cu, n, p.T, bos, eos);
+
+    float S[DVS];
+    if (role == SEG_M) {          // identity columns slice*32 .. slice*32+31
+#pragma unroll
+        for (int j = 0; j < DVS; ++j) S[j] = (tid == slice * DVS + j) ? 1.f : 0.f;
+    } else if (role == SEG_B) {
+#pragma unroll
+        for (int j = 0; j < DVS; ++j) S[j] = 0.f;
+    } else {
+        const float *src = (a == cb) ? p.S0 : p.S_T;
+        int64_t off = sbase;
+        if (p.nseg && seg > 0) {  // the start state the combine step produced
+            src = smap(p.smaps, p.nseg, h, seg, SMAP_START);
+            off = (int64_t)tid * D + slice * DVS;
+        }
+#pragma unroll
+        for (int j = 0; j < DVS; j += 4) {
+            float4 x = src ? *reinterpret_cast<const float4 *>(src + off + j)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
+        }
+    }
+    const bool write_o = role == SEG_FULL;
+    const float u_scale = role == SEG_M ? 0.f : 1.f;   // the homogeneous map drops U~
+    // the zero half of [0 ; P] in both stages
+    for (int e = tid; e < 2 * 8192 / 16; e += K2_THREADS) {
+        const int st = e / 512, off = (e % 512) * 16;
+        *reinterpret_cast<uint4 *>(sm + st * S2_STAGE + S2_PZ + off) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (tid == 0) {
+        mbar_init(&mbar[0], 1);
+        mbar_init(&mbar[1], 1);
+        mbar_init(&mbar[2], 2);   // round 1: two issuers
+        mbar_init(&mbar[3], 3);   // round 2: three issuers
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc<256>(tmem_slot);
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    auto issue_loads = [&](int ch, int stage) {
+        const uint8_t *src = img_base + ((uint64_t)(ch - p.w0) * H + h) * CH_STRIDE;
+        uint8_t *dst = sm + stage * S2_STAGE;
+        uint64_t *mb = &mbar[stage];
+        mbar_arrive_expect_tx(mb, S2_TX);
+        bulk_g2s(dst + S2_WQ, src + IMG_W, 8192, mb);              // W, k 0-63
+        bulk_g2s(dst + S2_WQ + 8192, src + IMG_Q, 8192, mb);       // Q^, k 0-63
+        bulk_g2s(dst + S2_WQ + 16384, src + IMG_W + 8192, 8192, mb);
+        bulk_g2s(dst + S2_WQ + 24576, src + IMG_Q + 8192, 8192, mb);
+        bulk_g2s(dst + S2_KB, src + IMG_KT, 16384, mb);
+        bulk_g2s(dst + S2_PZ + 8192, src + IMG_P, 8192, mb);
+        bulk_g2s(dst + S2_U, src + IMG_U + slice * 4096, 4096, mb);
+        bulk_g2s(dst + S2_G, src + IMG_G, 512, mb);
+    };
+    if (tid == 0 && a < b) {
+        issue_loads(a, 0);
+        if (a + 1 < b) issue_loads(a + 1, 1);
+    }
+
+    const uint64_t d_sop = sdesc(smem_addr(sm + S2_SOP), 128, 2048, LAYOUT_NONE);
+    const uint64_t d_uop = sdesc(smem_addr(sm + S2_UOP), 128, 1024, LAYOUT_NONE);
+    const uint32_t id_wq = idesc(128, DVS, FMT_F16, FMT_F16, 0, 1);
+    const uint32_t id_kb = idesc(128, DVS, FMT_F16, FMT_F16, 1, 1);
+
+    // stores the O rows of a finished chunk (threads 64-127: row tid - 64)
+    auto store_o = [&](int set, int64_t t0, int L) {
+        if (warp >= 2) {
+            float oa[16], ob[16], pa[16], pb[16];
+            tmem_ld16(tmem_at(tmem, warp, 128 * set), oa);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 16), ob);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 32), pa);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 48), pb);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) { oa[j] += pa[j]; ob[j] += pb[j]; }
+            const int r = tid - 64;
+            if (r < L) {
+                __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * D + slice * DVS;
+#pragma unroll
+                for (int gq = 0; gq < DVS / 8; ++gq) {
+                    const float *src = gq < 2 ? oa + 8 * gq : ob + 8 * (gq - 2);
+                    __nv_bfloat162 b0 = __floats2bfloat162_rn(src[0], src[1]);
+                    __nv_bfloat162 b1 = __floats2bfloat162_rn(src[2], src[3]);
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(src[4], src[5]);
+                    __nv_bfloat162 b3 = __floats2bfloat162_rn(src[6], src[7]);
+                    *reinterpret_cast<uint4 *>(dst + 8 * gq) = make_uint4(
+                        *reinterpret_cast<uint32_t *>(&b0), *reinterpret_cast<uint32_t *>(&b1),
+                        *reinterpret_cast<uint32_t *>(&b2), *reinterpret_cast<uint32_t *>(&b3));
+                }
+            }
+        }
+    };
+
+    bool ok = true;
+    int64_t prev_t0 = 0;
+    int prev_L = 0;
+    for (int ch = a; ch < b; ++ch) {
+        const int i = ch - a, stage = i & 1, set = i & 1;
+        uint8_t *st = sm + stage * S2_STAGE;
+        const uint32_t tset = tmem + 128 * set;
+        const int64_t t0 = bos + (int64_t)(ch - cb) * C;
+        const int L = (int)((eos - t0) < C ? (eos - t0) : C);
+        ok = __syncthreads_and(mbar_wait(&mbar[stage], (i >> 1) & 1));
+        if (!ok) break;
+
+        // S (fp16) -> B operand [K = dk][N = 32], MN-major, no swizzle:
+        // core matrix (8 K rows x 8 N) at (n/8) * 2048 + (k/8) * 128
+#pragma unroll
+        for (int gq = 0; gq < DVS / 8; ++gq) {
+            uint4 v4 = make_uint4(pack_h2(S[8 * gq + 0], S[8 * gq + 1]), pack_h2(S[8 * gq + 2], S[8 * gq + 3]),
+                                  pack_h2(S[8 * gq + 4], S[8 * gq + 5]), pack_h2(S[8 * gq + 6], S[8 * gq + 7]));
+            *reinterpret_cast<uint4 *>(sm + S2_SOP + gq * 2048 + (tid >> 3) * 128 + (tid & 7) * 16) = v4;
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        if (lane == 0 && warp < 2) {      // round 1: warp w takes K atom w
+            fence_after_sync();
+            const uint64_t dwq = sdesc_k_sw128(smem_addr(st + S2_WQ));
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_f16(tset + 32 * warp, sdesc_add(dwq, warp * 16384 + s * 32),
+                        sdesc_add(d_sop, 256 * (4 * warp + s)), id_wq, s > 0);
+            mma_commit(&mbar[2]);
+        }
+        if (i > 0 && write_o) store_o(set ^ 1, prev_t0, prev_L);   // previous chunk's outputs
+        ok = __syncthreads_and(mbar_wait(&mbar[2], i & 1));
+        fence_after_sync();
+        if (!ok) break;
+
+        // U = U~ - W S for token rows 0-63 (threads 0-63)
+        if (warp < 2) {
+            float w0[16], w1[16], x0[16], x1[16];
+            tmem_ld16(tmem_at(tmem, warp, 128 * set), w0);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 16), w1);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 32), x0);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 48), x1);
+            tmem_wait_ld();
+            const int r = tid;
+            const __half *ut = reinterpret_cast<const __half *>(st + S2_U) + r * DVS;
+            float u[DVS];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                u[j] = u_scale * __half2float(ut[j]) - (w0[j] + x0[j]);
+                u[16 + j] = u_scale * __half2float(ut[16 + j]) - (w1[j] + x1[j]);
+            }
+#pragma unroll
+            for (int gq = 0; gq < DVS / 8; ++gq) {
+                uint4 v4 = make_uint4(pack_h2(u[8 * gq + 0], u[8 * gq + 1]), pack_h2(u[8 * gq + 2], u[8 * gq + 3]),
+                                      pack_h2(u[8 * gq + 4], u[8 * gq + 5]), pack_h2(u[8 * gq + 6], u[8 * gq + 7]));
+                *reinterpret_cast<uint4 *>(sm + S2_UOP + gq * 1024 + (r >> 3) * 128 + (r & 7) * 16) = v4;
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        if (lane == 0 && warp < 3) {      // round 2: warps 0-1 Kbar^T U halves, warp 2 P U
+            fence_after_sync();
+            if (warp < 2) {
+                const uint64_t dkb = sdesc(smem_addr(st + S2_KB), 8192, 1024, LAYOUT_SW128);
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                    const int ks = 2 * warp + s;
+                    mma_f16(tset + 64 + 32 * warp, sdesc_add(dkb, 2048 * ks),
+                            sdesc_add(d_uop, 256 * ks), id_kb, s > 0);
+                }
+            } else {
+                const uint64_t dpz = sdesc_k_sw128(smem_addr(st + S2_PZ));
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_f16(tset, sdesc_add(dpz, 32 * s), sdesc_add(d_uop, 256 * s), id_wq, 1);
+            }
+            mma_commit(&mbar[3]);
+        }
+        ok = __syncthreads_and(mbar_wait(&mbar[3], i & 1));
+        fence_after_sync();
+        if (!ok) break;
+
+        // S = Diag(e^gamma_last) S + Kbar^T U
+        {
+            float d2a[16], d2b[16], d3a[16], d3b[16];
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 64), d2a);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 80), d2b);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 96), d3a);
+            tmem_ld16(tmem_at(tmem, warp, 128 * set + 112), d3b);
+            tmem_wait_ld();
+            const float gl = reinterpret_cast<const float *>(st + S2_G)[tid];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                S[j] = gl * S[j] + (d2a[j] + d3a[j]);
+                S[16 + j] = gl * S[16 + j] + (d2b[j] + d3b[j]);
+            }
+        }
+        prev_t0 = t0;
+        prev_L = L;
+        fence_before_sync();
+        __syncthreads();   // every thread is done with this stage
+        if (tid == 0 && ch + 2 < b) issue_loads(ch + 2, stage);
+    }
+    if (ok && write_o && a < b) store_o((b - 1 - a) & 1, prev_t0, prev_L);
+
+    if (!ok && tid == 0) ws_fail(ws_hdr, 2);
+    // final state: S_T, or (segment launch) the segment's map, contribution
+    // or end state for the combine step; the last segment writes S_T
+    float *dst = nullptr;
+    if (!p.nseg || (p.phase == 1 && seg == p.nseg - 1))
+        dst = p.S_T + sbase;
+    else if (p.phase == 0)   // segment 0 ends in its B slot
+        dst = smap(p.smaps, p.nseg, h, seg, role == SEG_M ? SMAP_M : SMAP_B) + (int64_t)tid * D +
+              slice * DVS;
+    if (dst) {
+#pragma unroll
+        for (int j = 0; j < DVS; j += 4)
+            *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc<256>(tmem);
+}
+
+// Chunk-affine scan, combine step: a segment maps its start state S to
+// M_s S + B_s, so the start states follow in order from segment 0's end
+// state (stored in its B slot).  One CTA per (head, 32-column slice), fp32 on
+// CUDA cores: thread (row t, group of 8 columns); M_s is staged transposed in
+// shared memory (rows padded to 129 floats) so that a warp reads consecutive
+// rows of one column, and the slice of S is broadcast from shared memory
+// (rows of 40 floats, so that a thread's 8 columns are two 16-byte loads).
+__global__ void __launch_bounds__(COMB_THREADS) segment_combine_kernel(float *smaps, int nseg) {
+    extern __shared__ float csm[];
+    float *Mt = csm;                  // [k][t] = M_s[t][k], row stride 129
+    float *Ssh = csm + 128 * 129;     // [k][j], row stride SSH_LD (16-byte aligned rows)
+    const int h = blockIdx.x / NSLICE, slice = blockIdx.x % NSLICE;
+    const int tid = threadIdx.x, t = tid & 127, g = tid >> 7;
+    const int64_t off = (int64_t)t * D + slice * DVS + 8 * g;
+    float S[8];
+    const float *e0 = smap(smaps, nseg, h, 0, SMAP_B) + off;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) S[j] = e0[j];
+    for (int sg = 1; sg < nseg; ++sg) {
+        float *start = smap(smaps, nseg, h, sg, SMAP_START) + off;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) start[j] = S[j];
+        if (sg == nseg - 1) break;
+        __syncthreads();   // the previous step is done with Mt and Ssh
+        const float4 *M4 = reinterpret_cast<const float4 *>(smap(smaps, nseg, h, sg, SMAP_M));
+        for (int e = tid; e < 128 * 32; e += COMB_THREADS) {
+            const int row = e >> 5, k4 = (e & 31) * 4;
+            const float4 m = M4[e];
+            Mt[(k4 + 0) * 129 + row] = m.x;
+            Mt[(k4 + 1) * 129 + row] = m.y;
+            Mt[(k4 + 2) * 129 + row] = m.z;
+            Mt[(k4 + 3) * 129 + row] = m.w;
+        }
+        *reinterpret_cast<float4 *>(Ssh + t * SSH_LD + 8 * g) = make_float4(S[0], S[1], S[2], S[3]);
+        *reinterpret_cast<float4 *>(Ssh + t * SSH_LD + 8 * g + 4) = make_float4(S[4], S[5], S[6], S[7]);
+        __syncthreads();
+        const float *Bv = smap(smaps, nseg, h, sg, SMAP_B) + off;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) S[j] = Bv[j];
+#pragma unroll 4
+        for (int k = 0; k < D; ++k) {
+            const float m = Mt[k * 129 + t];
+            const float4 s0 = *reinterpret_cast<const float4 *>(Ssh + k * SSH_LD + 8 * g);
+            const float4 s1 = *reinterpret_cast<const float4 *>(Ssh + k * SSH_LD + 8 * g + 4);
+            S[0] = fmaf(m, s0.x, S[0]); S[1] = fmaf(m, s0.y, S[1]);
+            S[2] = fmaf(m, s0.z, S[2]); S[3] = fmaf(m, s0.w, S[3]);
+            S[4] = fmaf(m, s1.x, S[4]); S[5] = fmaf(m, s1.y, S[5]);
+            S[6] = fmaf(m, s1.z, S[6]); S[7] = fmaf(m, s1.w, S[7]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------
+// K2, wide form: one CTA of 512 threads per (sequence, head), for batches
+// with more chains than the GPU runs at once.  Warpgroup s (warps 4s..4s+3)
+// owns state columns 32s..32s+31; its thread t (0..127) holds row t (a dk
+// channel) of those columns in fp32 registers.  Every MMA spans the whole
+// state (N = 128), so one SM carries a whole head.  Per chunk:
+//   round 1: A_s + B_s = [W ; Q^] S   (M = 128, K = dk, split in halves over
+//            two issuers; rows 0-63 W S, 64-127 Q^ S)
+//   U = U~ - W S (fp16)                (rows 0-63: warps 0-1 of every warpgroup)
+//   round 2: B_s' = Kbar^T U           (M = 128, K = 64; first issuer)
+//            A_s += [0 ; P] U          (second issuer; rows 64-127 of A_s + B_s
+//                                       then hold O)
+//   S = Diag(e^gamma_last) S + B_s'.
+// TMEM holds two 128-column accumulators per set; chunk c uses set s = c % 2
+// for round 1 and the other set's B (whose previous contents, the last
+// chunk's outputs, have left TMEM during round 1) for Kbar^T U.  Operand
+// images arrive with bulk async copies, double buffered; a stage is reloaded
+// once the next chunk's round 1 is issued, when its last reader (the P U MMA)
+// has long finished.
+__global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    // [0..1] loads, [2] round 1 (two issuers), [3] round 2 state, [4] round 2 outputs
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + S2W_MISC);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 5);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wg = warp >> 2, wq = warp & 3;   // column block, TMEM lane quadrant
+    const int row = 32 * wq + lane;            // state row (dk channel) / TMEM lane
+    const int col0 = 32 * wg;                  // first state column of this thread
+    const int H = p.H;
+    const int h = blockIdx.x % H;
+    const int n = blockIdx.x / H;
+    int32_t *ws_hdr = reinterpret_cast<int32_t *>(p.ws);
+    const int32_t *chunk_base = reinterpret_cast<const int32_t *>(p.ws + WS_HEADER);
+    const uint8_t *img_base = p.ws + ws_images_offset(p.N);
+
+    const int cb = chunk_base[n], ce = chunk_base[n + 1];
+    const int a = max(cb, p.w0), b = min(ce, p.w1);
+    const int64_t sbase = ((int64_t)n * H + h) * D * D + (int64_t)row * D + col0;
+    if (cb == ce) {                       // empty sequence: pass the state through
+        if (p.w0 == 0) {
+            for (int j = 0; j < 32; j += 4) {
+                float4 x = p.S0 ? *reinterpret_cast<const float4 *>(p.S0 + sbase + j)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4 *>(p.S_T + sbase + j) = x;
+            }
+        }
+        return;
+    }
+    if (a >= b) return;                   // no chunk of this sequence in the window
+
+    int64_t bos, eos;
+    seq_bounds(p.cu, n, p.T, bos, eos);
+
+    float S[32];
+    {
+        const float *src = (a == cb) ? p.S0 : p.S_T;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            float4 x = src ? *reinterpret_cast<const float4 *>(src + sbase + j)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
+        }
+    }
+    // the zero half of [0 ; P] in both stages
+    for (int e = tid; e < 2 * 8192 / 16; e += K2W_THREADS) {
+        const int st = e / 512, off = (e % 512) * 16;
+        *reinterpret_cast<uint4 *>(sm + st * S2W_STAGE + S2W_PZ + off) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (tid == 0) {
+        for (int j = 0; j < 5; ++j) mbar_init(&mbar[j], j == 2 ? 2 : 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc<512>(tmem_slot);
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    auto issue_loads = [&](int ch, int stage) {
+        const uint8_t *src = img_base + ((uint64_t)(ch - p.w0) * H + h) * CH_STRIDE;
+        uint8_t *dst = sm + stage * S2W_STAGE;
+        uint64_t *mb = &mbar[stage];
+        mbar_arrive_expect_tx(mb, S2W_TX);
+        bulk_g2s(dst + S2W_WQ, src + IMG_W, 8192, mb);              // W, k 0-63
+        bulk_g2s(dst + S2W_WQ + 8192, src + IMG_Q, 8192, mb);       // Q^, k 0-63
+        bulk_g2s(dst + S2W_WQ + 16384, src + IMG_W + 8192, 8192, mb);
+        bulk_g2s(dst + S2W_WQ + 24576, src + IMG_Q + 8192, 8192, mb);
+        bulk_g2s(dst + S2W_KB, src + IMG_KT, 16384, mb);
+        bulk_g2s(dst + S2W_PZ + 8192, src + IMG_P, 8192, mb);
+        bulk_g2s(dst + S2W_U, src + IMG_U, 16384, mb);
+        bulk_g2s(dst + S2W_G, src + IMG_G, 512, mb);
+    };
+    if (tid == 0) {
+        issue_loads(a, 0);
+        if (a + 1 < b) issue_loads(a + 1, 1);
+    }
+    // chunk a + 1 is loaded up front; chunk c + 1 for c > a is loaded during
+    // chunk c (see round 1)
+
+    const uint64_t d_sop = sdesc(smem_addr(sm + S2W_SOP), 128, 2048, LAYOUT_NONE);
+    const uint64_t d_uop = sdesc(smem_addr(sm + S2W_UOP), 128, 1024, LAYOUT_NONE);
+    const uint32_t id_wq = idesc(128, 128, FMT_F16, FMT_F16, 0, 1);
+    const uint32_t id_kb = idesc(128, 128, FMT_F16, FMT_F16, 1, 1);
+
+    // O rows of a finished chunk (TMEM lanes 64-127: warps 2-3 of each group)
+    auto store_o = [&](int set, uint32_t phase, int64_t t0, int L) {
+        if (wq >= 2) {
+            const bool done = mbar_wait(&mbar[4], phase & 1);
+            fence_after_sync();
+            float oa[16], ob[16], pa[16], pb[16];
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + col0), oa);
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + col0 + 16), ob);
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + 128 + col0), pa);
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + 128 + col0 + 16), pb);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) { oa[j] += pa[j]; ob[j] += pb[j]; }
+            const int r = row - 64;
+            if (done && r < L) {
+                __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * D + col0;
+#pragma unroll
+                for (int gq = 0; gq < 4; ++gq) {
+                    const float *src = gq < 2 ? oa + 8 * gq : ob + 8 * (gq - 2);
+                    __nv_bfloat162 b0 = __floats2bfloat162_rn(src[0], src[1]);
+                    __nv_bfloat162 b1 = __floats2bfloat162_rn(src[2], src[3]);
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(src[4], src[5]);
+                    __nv_bfloat162 b3 = __floats2bfloat162_rn(src[6], src[7]);
+                    *reinterpret_cast<uint4 *>(dst + 8 * gq) = make_uint4(
+                        *reinterpret_cast<uint32_t *>(&b0), *reinterpret_cast<uint32_t *>(&b1),
+                        *reinterpret_cast<uint32_t *>(&b2), *reinterpret_cast<uint32_t *>(&b3));
+                }
+            }
+            return done;
+        }
+        return true;
+    };
+
+    bool ok = true;
+    int64_t prev_t0 = 0;
+    int prev_L = 0;
+    for (int ch = a; ch < b; ++ch) {
+        const int i = ch - a, stage = i & 1, set = i & 1;
+        uint8_t *st = sm + stage * S2W_STAGE;
+        const uint32_t acc_a = tmem + 256 * set, acc_b = acc_a + 128;   // round 1
+        const uint32_t acc_s = tmem + 256 * (set ^ 1) + 128;              // Kbar^T U
+        const int64_t t0 = bos + (int64_t)(ch - cb) * C;
+        const int L = (int)((eos - t0) < C ? (eos - t0) : C);
+        ok = __syncthreads_and(mbar_wait(&mbar[stage], (i >> 1) & 1));
+        if (!ok) break;
+
+        // S (fp16) -> B operand [K = dk][N = 128], MN-major, no swizzle:
+        // core matrix (8 K rows x 8 N) at (n/8) * 2048 + (k/8) * 128
+#pragma unroll
+        for (int gq = 0; gq < 4; ++gq) {
+            uint4 v4 = make_uint4(pack_h2(S[8 * gq + 0], S[8 * gq + 1]), pack_h2(S[8 * gq + 2], S[8 * gq + 3]),
+                                  pack_h2(S[8 * gq + 4], S[8 * gq + 5]), pack_h2(S[8 * gq + 6], S[8 * gq + 7]));
+            *reinterpret_cast<uint4 *>(sm + S2W_SOP + (4 * wg + gq) * 2048 + (row >> 3) * 128 + (row & 7) * 16) = v4;
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        if (lane == 0 && warp < 2) {      // round 1: warp w takes K atom w
+            fence_after_sync();
+            const uint64_t dwq = sdesc_k_sw128(smem_addr(st + S2W_WQ));
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4)
+                mma_f16(warp == 0 ? acc_a : acc_b, sdesc_add(dwq, warp * 16384 + s4 * 32),
+                        sdesc_add(d_sop, 256 * (4 * warp + s4)), id_wq, s4 > 0);
+            mma_commit(&mbar[2]);
+            // the previous chunk's P U MMA was the last reader of the other
+            // stage: reload it with the chunk after next
+            if (warp == 0 && i > 0 && ch + 1 < b) {
+                if (mbar_wait(&mbar[4], (i - 1) & 1)) issue_loads(ch + 1, stage ^ 1);
+                else ws_fail(ws_hdr, 2);
+            }
+        }
+        bool o_ok = true;
+        if (i > 0) o_ok = store_o(set ^ 1, (uint32_t)(i - 1), prev_t0, prev_L);
+        ok = __syncthreads_and(mbar_wait(&mbar[2], i & 1) && o_ok);
+        fence_after_sync();
+        if (!ok) break;
+
+        // U = U~ - W S for token rows 0-63 (warps 0-1 of each group)
+        if (wq < 2) {
+            float w0[16], w1[16], x0[16], x1[16];
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + col0), w0);
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + col0 + 16), w1);
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + 128 + col0), x0);
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + 128 + col0 + 16), x1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) { w0[j] += x0[j]; w1[j] += x1[j]; }
+            const int r = row;
+            const uint4 *ut = reinterpret_cast<const uint4 *>(st + S2W_U + wg * 4096 + r * 64);
+            float u[32];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const uint4 x = ut[q4];
+                const __half2 *h2 = reinterpret_cast<const __half2 *>(&x);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(h2[e]);
+                    const int j = 8 * q4 + 2 * e;
+                    const float wa = j < 16 ? w0[j] : w1[j - 16];
+                    const float wb = j + 1 < 16 ? w0[j + 1] : w1[j - 15];
+                    u[j] = f.x - wa;
+                    u[j + 1] = f.y - wb;
+                }
+            }
+#pragma unroll
+            for (int gq = 0; gq < 4; ++gq) {
+                uint4 v4 = make_uint4(pack_h2(u[8 * gq + 0], u[8 * gq + 1]), pack_h2(u[8 * gq + 2], u[8 * gq + 3]),
+                                      pack_h2(u[8 * gq + 4], u[8 * gq + 5]), pack_h2(u[8 * gq + 6], u[8 * gq + 7]));
+                *reinterpret_cast<uint4 *>(sm + S2W_UOP + (4 * wg + gq) * 1024 + (r >> 3) * 128 + (r & 7) * 16) = v4;
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        if (lane == 0 && warp < 2) {      // round 2: warp 0 Kbar^T U, warp 1 [0 ; P] U
+            fence_after_sync();
+            if (warp == 0) {
+                const uint64_t dkb = sdesc(smem_addr(st + S2W_KB), 8192, 1024, LAYOUT_SW128);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(acc_s, sdesc_add(dkb, 2048 * ks), sdesc_add(d_uop, 256 * ks), id_kb, ks > 0);
+                mma_commit(&mbar[3]);
+            } else {
+                const uint64_t dpz = sdesc_k_sw128(smem_addr(st + S2W_PZ));
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(acc_a, sdesc_add(dpz, 32 * ks), sdesc_add(d_uop, 256 * ks), id_wq, 1);
+                mma_commit(&mbar[4]);
+            }
+        }
+        ok = __syncthreads_and(mbar_wait(&mbar[3], i & 1));
+        fence_after_sync();
+        if (!ok) break;
+
+        // S = Diag(e^gamma_last) S + Kbar^T U
+        {
+            float da[16], db[16];
+            tmem_ld16(tmem_at(tmem, wq, 256 * (set ^ 1) + 128 + col0), da);
+            tmem_ld16(tmem_at(tmem, wq, 256 * (set ^ 1) + 128 + col0 + 16), db);
+            tmem_wait_ld();
+            const float gl = reinterpret_cast<const float *>(st + S2W_G)[row];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                S[j] = gl * S[j] + da[j];
+                S[16 + j] = gl * S[16 + j] + db[j];
+            }
+        }
+        prev_t0 = t0;
+        prev_L = L;
+        fence_before_sync();
+        __syncthreads();   // every thread is done with this stage's images
+    }
+    if (ok) ok = __syncthreads_and(store_o((b - 1 - a) & 1, (uint32_t)(b - 1 - a), prev_t0, prev_L));
+
+    if (!ok && tid == 0) ws_fail(ws_hdr, 2);
+#pragma unroll
+    for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4 *>(p.S_T + sbase + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc<512>(tmem);
+}
+
+}  // namespace tcp
+}  // namespace kda

@@ -1,0 +1,612 @@
+// kda_prefill_intra.cu -- the per-chunk kernel of the tensor-core prefill
+// (layouts and the method overview in kda_prefill_tc.cuh).
+#include "kda_prefill_tc.cuh"
+
+namespace kda {
+namespace tcp {
+
+// ------------------------------------------------------------------------------
+// chunk table: chunk_base[n] = number of 64-token chunks before sequence n,
+// capped at `cap` (the host's bound ceil(T/64) + N, which sizes the workspace):
+// only overlapping, inconsistent offsets can reach the cap, and then the
+// excess chunks are dropped instead of written past the workspace.
+// ------------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024)
+chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int cap,
+                   int32_t *ws_hdr, int32_t *chunk_base) {
+    __shared__ int32_t warp_tot[32];
+    __shared__ int32_t carry_s;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) { carry_s = 0; ws_hdr[0] = 0; }
+    __syncthreads();
+    for (int base = 0; base < N; base += 1024) {
+        const int n = base + tid;
+        int cnt = 0;
+        if (n < N) {
+            int64_t bos, eos;
+            seq_bounds(cu, n, T, bos, eos);
+            cnt = (int)((eos - bos + C - 1) / C);
+        }
+        int x = cnt;   // inclusive warp scan
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_tot[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int t = warp_tot[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int y = __shfl_up_sync(0xffffffffu, t, o);
+                if (lane >= o) t += y;
+            }
+            warp_tot[lane] = t;   // inclusive over warps
+        }
+        __syncthreads();
+        const int excl = x - cnt + (warp > 0 ? warp_tot[warp - 1] : 0);
+        if (n < N) chunk_base[n] = min(carry_s + excl, cap);
+        __syncthreads();
+        if (tid == 0) carry_s += warp_tot[31];
+        __syncthreads();
+    }
+    if (tid == 0) chunk_base[N] = min(carry_s, cap);
+}
+
+// ------------------------------------------------------------------------------
+// K1: intra-chunk kernel
+// ------------------------------------------------------------------------------
+// One CTA per SM walks (chunk, head) tasks, chunk-major.  Per task:
+//   1. TMA brings k, q, v (bf16) and g (fp32) rows [t0, t0 + 64) of head h
+//      into staging; issued during the previous task, as soon as its prep
+//      has consumed the staging tiles.
+//   2. Per-channel cumulative log-gate (in place), e^gamma_last, range check;
+//      the previous task's W/U MMA finishes underneath.
+//   3. Element-wise prep, 8 channels of one row per unit: tf32 operands
+//      [K e^g ; Q e^g] and K e^-g for A / P, fp16 K e^g and V for W / U~, the
+//      Q^ and Kbar workspace images; the previous task's W and U~ leave TMEM
+//      for the workspace in two rounds hidden behind it.
+//   4. One M = 128 tf32 MMA group (warps 12-15 issue one channel atom each):
+//      rows 0-63 give A / beta, rows 64-127 give P.  A chunk whose decay
+//      exceeds e^80 on some channel would overflow those factors, so it takes
+//      an exact pairwise CUDA-core path instead.
+//   5. T = (I + A)^-1 on CUDA cores by warps 0-5 (fp32, 16 x 16 blocks,
+//      register-tiled block forward substitution), written as the fp16 image
+//      of T' = T Diag(beta).
+//   6. W = T' (K e^g), U~ = T' V on tcgen05 (fp16), waited for in step 2 of
+//      the next task.
+__device__ __forceinline__ void tma_load_3d(uint8_t *dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint64_t *mbar) {
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4}], [%5];"
+                 :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1),
+                    "r"(c2), "r"(smem_addr(mbar))
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 pack8_h(const float *x) {
+    return make_uint4(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]), pack_h2(x[4], x[5]),
+                      pack_h2(x[6], x[7]));
+}
+
+// [r][c] 128B-swizzled image with 64-channel atoms: byte offset of the 16-byte
+// chunk holding channels c0..c0+7 of row r (c0 a multiple of 8).
+__device__ __forceinline__ uint32_t rc_img_off(int r, int c0) {
+    return (uint32_t)(c0 >> 6) * 8192u + sw128_off(r, (c0 & 63) >> 3);
+}
+
+// acc[2][4] += X[m0..m0+1][k] Y[k][n0..n0+3] over k = 0..15, with X read
+// transposed (Xt[k][m]) and Y row-major, both with row stride LD.
+__device__ __forceinline__ void mm16_2x4(float (&acc)[2][4], const float *Xt, const float *Y) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const float2 x = *reinterpret_cast<const float2 *>(Xt + k * LD);
+        const float4 y = *reinterpret_cast<const float4 *>(Y + k * LD);
+        acc[0][0] = fmaf(x.x, y.x, acc[0][0]); acc[0][1] = fmaf(x.x, y.y, acc[0][1]);
+        acc[0][2] = fmaf(x.x, y.z, acc[0][2]); acc[0][3] = fmaf(x.x, y.w, acc[0][3]);
+        acc[1][0] = fmaf(x.y, y.x, acc[1][0]); acc[1][1] = fmaf(x.y, y.y, acc[1][1]);
+        acc[1][2] = fmaf(x.y, y.z, acc[1][2]); acc[1][3] = fmaf(x.y, y.w, acc[1][3]);
+    }
+}
+
+// fp16 of x at (row r, column i) of the K-major 128B-swizzled T' image
+__device__ __forceinline__ void tp_store1(uint8_t *img, int r, int i, float x) {
+    *reinterpret_cast<__half *>(img + sw128_off(r, i >> 3) + (i & 7) * 2) = __float2half_rn(x);
+}
+
+// T = (I + A)^-1 for the strictly lower 64 x 64 A (row-major, stride LD) in
+// 16 x 16 blocks, fp32 on CUDA cores, and the fp16 image of T' = T Diag(beta).
+// With T_RR the inverses of the diagonal blocks of I + A and F_RJ = T_RR A_RJ
+// (J < R), block forward substitution gives T_RI = -sum_{J=I}^{R-1} F_RJ T_JI
+// for I < R.  Six warps each own one off-diagonal block of T (2 x 4 outputs
+// per lane, partial sums kept in registers) and add one term per pass, so the
+// whole inverse is: diagonal blocks | F | three passes.  Run by warps 0-5
+// only (named barrier 1), leaving the other warps free.  The image's blocks
+// above the diagonal are not written (they hold zeros).
+constexpr int INV_THREADS = 192;
+__device__ __forceinline__ void invert_unit_lower(const float *As, float *Ts, float *Tt, float *Ft,
+                                                  const float *sB, uint8_t *tp_img, int tid) {
+    const int warp = tid >> 5, lane = tid & 31;
+    // diagonal blocks: thread (R, column j) by forward substitution in registers
+    if (tid < 64) {
+        const int R = tid >> 4, j = tid & 15;
+        const float *Ab = As + (16 * R) * LD + 16 * R;
+        float x[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) x[m] = (m == j) ? 1.f : 0.f;
+#pragma unroll
+        for (int i = 0; i < 15; ++i) {
+            const float xi = x[i];
+#pragma unroll
+            for (int r = i + 1; r < 16; ++r) x[r] = fmaf(-Ab[r * LD + i], xi, x[r]);
+        }
+        const float bj = sB[16 * R + j];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            Ts[(16 * R + m) * LD + 16 * R + j] = x[m];
+            tp_store1(tp_img, 16 * R + m, 16 * R + j, x[m] * bj);
+        }
+        float4 *trow = reinterpret_cast<float4 *>(Tt + (16 * R + j) * LD + 16 * R);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+            trow[q4] = make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
+    }
+    bar_sync(1, INV_THREADS);
+
+    // warp w owns block (R, I): (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
+    const int R = warp < 3 ? warp + 1 : (warp < 5 ? warp - 1 : 3);
+    const int I = warp < 3 ? warp : (warp < 5 ? warp - 3 : 0);
+    const int m0 = 2 * (lane >> 2), n0 = 4 * (lane & 3);
+    {   // F_RI = T_RR A_RI, stored transposed
+        float f[2][4] = {};
+        mm16_2x4(f, Tt + (16 * R) * LD + 16 * R + m0, As + (16 * R) * LD + 16 * I + n0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<float2 *>(Ft + (16 * I + n0 + e) * LD + 16 * R + m0) =
+                make_float2(f[0][e], f[1][e]);
+    }
+    bar_sync(1, INV_THREADS);
+    float acc[2][4] = {};
+#pragma unroll
+    for (int pass = 0; pass < 3; ++pass) {
+        const int J = I + pass;
+        if (J < R) {
+            mm16_2x4(acc, Ft + (16 * J) * LD + 16 * R + m0, Ts + (16 * J) * LD + 16 * I + n0);
+            if (J == R - 1) {
+                const float4 b4 = *reinterpret_cast<const float4 *>(sB + 16 * I + n0);
+#pragma unroll
+                for (int a = 0; a < 2; ++a) {
+                    const int r = 16 * R + m0 + a, i = 16 * I + n0;
+                    *reinterpret_cast<float4 *>(Ts + r * LD + i) =
+                        make_float4(-acc[a][0], -acc[a][1], -acc[a][2], -acc[a][3]);
+                    *reinterpret_cast<uint2 *>(tp_img + sw128_off(r, i >> 3) + (i & 7) * 2) =
+                        make_uint2(pack_h2(-acc[a][0] * b4.x, -acc[a][1] * b4.y),
+                                   pack_h2(-acc[a][2] * b4.z, -acc[a][3] * b4.w));
+                }
+            }
+        }
+        if (pass < 2) bar_sync(1, INV_THREADS);
+    }
+}
+
+__global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_constant__ K1Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    float *gL = reinterpret_cast<float *>(sm + S1_MISC);   // [128] gamma_last
+    float *eL = gL + 128;                                  // [128] e^gamma_last
+    float *sB = eL + 128;                                  // [64] beta
+    float *tot = sB + 64;                                  // [4][128] segment totals
+    float *sGs = tot + 512;                                // [64] scalar gates (scalar_gate)
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(sGs + 64);   // [0] TMA, [1] A/P, [2] W/U
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 3);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int32_t *ws_hdr = reinterpret_cast<int32_t *>(p.ws);
+    const int32_t *chunk_base = reinterpret_cast<const int32_t *>(p.ws + WS_HEADER);
+    uint8_t *img_base = p.ws + ws_images_offset(p.N);
+    const int H = p.H;
+
+    if (tid == 0) {
+        mbar_init(&mbar[0], 1);
+        mbar_init(&mbar[1], 4);   // four A/P issuers
+        mbar_init(&mbar[2], 2);   // W and U~ issuers
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc<512>(tmem_slot);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    // T' is lower triangular: the blocks above its diagonal stay zero (the
+    // inverse rewrites only the diagonal and lower blocks)
+    for (int e = tid; e < 64 * 8; e += K1_THREADS) {
+        const int r = e >> 3, ch = e & 7;
+        if (ch >= 2 * ((r >> 4) + 1))
+            *reinterpret_cast<uint4 *>(sm + S1_TP + sw128_off(r, ch)) = make_uint4(0, 0, 0, 0);
+    }
+
+    const int total = chunk_base[p.N];
+    const int c_end = min(p.w1, total);
+    const int ntask = (c_end > p.w0 ? c_end - p.w0 : 0) * H;
+    const int stride = gridDim.x;
+
+    struct Pos { int h, L; int64_t t0; };
+    // A task's position in two steps: fetch issues the offset-table loads,
+    // finish is their first use (placed a phase later, so that the loads'
+    // latency is hidden).  Together they give the sequence bounds clamped into
+    // [0, T] (as seq_bounds does) and the chunk's first token and length.
+    struct PosRaw { int ch, h; int32_t c0, c1, cb; };
+    auto pos_fetch = [&](int task) {
+        PosRaw r{-1, 0, 0, 0, 0};
+        if (task >= ntask) return r;
+        r.ch = p.w0 + task / H;
+        r.h = task % H;
+        const int n = find_seq(chunk_base, p.N, r.ch);
+        r.c0 = p.cu[n];
+        r.c1 = p.cu[n + 1];
+        r.cb = chunk_base[n];
+        return r;
+    };
+    auto pos_finish = [&](const PosRaw &r) {
+        Pos q{0, 0, 0};
+        if (r.ch < 0) return q;
+        int64_t bos = r.c0, eos = r.c1;
+        bos = bos < 0 ? 0 : (bos > p.T ? p.T : bos);
+        eos = eos < bos ? bos : (eos > p.T ? p.T : eos);
+        q.h = r.h;
+        q.t0 = bos + (int64_t)(r.ch - r.cb) * C;
+        q.L = (int)((eos - q.t0) < C ? (eos - q.t0) : C);
+        return q;
+    };
+    auto task_pos = [&](int task) { return pos_finish(pos_fetch(task)); };
+    // beta (and the scalar gate) of row `tid` of a task, read ahead into registers
+    auto row_params = [&](const Pos &q, int task, float &b, float &gs) {
+        b = 0.f; gs = 0.f;
+        if (tid < C && task < ntask && tid < q.L) {
+            b = p.beta[(q.t0 + tid) * H + q.h];
+            if (p.scalar_gate) gs = p.g[(q.t0 + tid) * H + q.h];
+        }
+    };
+    constexpr uint32_t TILE_BF16 = 16384, TILE_G = 32768;
+    auto expect_tma = [&]() {
+        mbar_arrive_expect_tx(&mbar[0], 3 * TILE_BF16 + (p.scalar_gate ? 0 : TILE_G));
+    };
+    auto tma_kqg = [&](const Pos &q) {
+        tma_load_3d(sm + S1_STG_K, &p.tm_k, 0, q.h, (int)q.t0, &mbar[0]);
+        tma_load_3d(sm + S1_STG_Q, &p.tm_q, 0, q.h, (int)q.t0, &mbar[0]);
+        if (!p.scalar_gate) tma_load_3d(sm + S1_STG_G, &p.tm_g, 0, q.h, (int)q.t0, &mbar[0]);
+    };
+    auto tma_v = [&](const Pos &q) {
+        tma_load_3d(sm + S1_STG_V, &p.tm_v, 0, q.h, (int)q.t0, &mbar[0]);
+    };
+    // W and U~ of a finished task: TMEM -> fp16 workspace images.  Row r of
+    // the M = 64 accumulators sits in lane r % 16 of quadrant r / 16; a warp
+    // reads its own quadrant.
+    auto store_wu_cols = [&](uint8_t *dst, int q, int col) {   // 16 columns
+        const int r = 16 * q + lane;
+        float w[16], u[16];
+        tmem_ld16(tmem_at(tmem, q, W_COL + col), w);
+        tmem_ld16(tmem_at(tmem, q, U_COL + col), u);
+        tmem_wait_ld();
+        if (lane < 16) {
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {
+                const int c0 = col + 8 * hc;
+                *reinterpret_cast<uint4 *>(dst + IMG_W + rc_img_off(r, c0)) = pack8_h(w + 8 * hc);
+                *reinterpret_cast<uint4 *>(dst + IMG_U + (c0 >> 5) * 4096 + r * 64 + (c0 & 31) * 2) =
+                    pack8_h(u + 8 * hc);
+            }
+        }
+    };
+    auto store_wu = [&](uint8_t *dst) {        // all 16 warps: 32 columns each
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) store_wu_cols(dst, warp & 3, 32 * (warp >> 2) + 16 * hh);
+    };
+    // The same, split so that the TMEM loads' latency overlaps other work:
+    // round hh (0, 1) of warp w covers columns 32 (w / 4) + 16 hh.
+    auto drain_issue = [&](int hh, float (&w)[16], float (&u)[16]) {
+        const int col = 32 * (warp >> 2) + 16 * hh;
+        tmem_ld16(tmem_at(tmem, warp & 3, W_COL + col), w);
+        tmem_ld16(tmem_at(tmem, warp & 3, U_COL + col), u);
+    };
+    auto drain_finish = [&](uint8_t *dst, int hh, float (&w)[16], float (&u)[16]) {
+        tmem_wait_ld();
+        reg_fence(w);
+        reg_fence(u);
+        const int col = 32 * (warp >> 2) + 16 * hh;
+        const int r = 16 * (warp & 3) + lane;
+        if (lane < 16) {
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {
+                const int c0 = col + 8 * hc;
+                *reinterpret_cast<uint4 *>(dst + IMG_W + rc_img_off(r, c0)) = pack8_h(w + 8 * hc);
+                *reinterpret_cast<uint4 *>(dst + IMG_U + (c0 >> 5) * 4096 + r * 64 + (c0 & 31) * 2) =
+                    pack8_h(u + 8 * hc);
+            }
+        }
+    };
+
+    // positions are resolved one task ahead of the one being loaded, so the
+    // offset-table lookups never sit on the critical path
+    int task = blockIdx.x;
+    Pos cur = task_pos(task), nxt = task_pos(task + stride);
+    float b_cur, gs_cur;
+    row_params(cur, task, b_cur, gs_cur);
+    uint32_t n_issued = 0, n_landed = 0;   // TMA phases (meaningful in thread 0, the issuer)
+    if (tid == 0 && task < ntask) { expect_tma(); tma_kqg(cur); tma_v(cur); n_issued = 1; }
+
+    bool ok = true;
+    uint32_t it = 0, ap_it = 0;
+    uint8_t *out_prev = nullptr;
+    for (; task < ntask; task += stride, ++it) {
+        const int L = cur.L;
+        const int next = task + stride;
+        uint8_t *out = img_base + (uint64_t)task * CH_STRIDE;
+        if (tid < C) {
+            sB[tid] = b_cur;
+            sGs[tid] = gs_cur;
+        }
+        ok = __syncthreads_and(mbar_wait(&mbar[0], it & 1));
+        if (!ok) break;
+        ++n_landed;
+
+        // ---- cumulative log-gate, in place (rows past the sequence: g = 0) ----
+        // thread = (channel c, 16-row segment sg)
+        {
+            const int c = tid & 127, sg = tid >> 7;
+            float *G = reinterpret_cast<float *>(sm + S1_STG_G);
+            float v[16];
+            if (p.scalar_gate) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = sGs[16 * sg + j];
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = G[(16 * sg + j) * 128 + c];
+            }
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                acc += 16 * sg + j < L ? v[j] : 0.f;
+                v[j] = acc;
+            }
+            tot[sg * 128 + c] = acc;
+            __syncthreads();
+            float off = 0.f;
+            for (int s2 = 0; s2 < sg; ++s2) off += tot[s2 * 128 + c];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) G[(16 * sg + j) * 128 + c] = v[j] + off;
+            if (sg == 3) {
+                gL[c] = acc + off;
+                eL[c] = __expf(acc + off);
+            }
+        }
+        // The previous task's W/U MMA ran under the scan; it must be done before
+        // the prep rewrites its B operands and before its results leave TMEM
+        // (this task's W/U MMA reuses the columns), in two rounds hidden behind
+        // the prep.
+        ok = __syncthreads_and(it == 0 || mbar_wait(&mbar[2], (it - 1) & 1));
+        fence_after_sync();
+        if (!ok) break;
+        const bool slow = __syncthreads_or(tid >= 384 && -gL[tid & 127] > RANGE_LIMIT);
+        float dw[16], du[16];
+        if (out_prev) drain_issue(0, dw, du);
+
+        // ---- element-wise prep: unit = (row r, channels c0..c0+7) -------------
+        // tf32 operands [K e^g ; Q e^g] and K e^-g for A / P (not on the slow
+        // path), fp16 K e^g and V for W / U~, the Q^ and Kbar workspace images.
+#pragma unroll 1
+        for (int jj = 0; jj < 2; ++jj) {
+            const int u = tid + K1_THREADS * jj;
+            const int r = u >> 4, c0 = (u & 15) * 8;
+            float kf[8], qf[8], vf[8], gm[8], el[8];
+            {
+                const uint4 kr = *reinterpret_cast<const uint4 *>(sm + S1_STG_K + r * 256 + c0 * 2);
+                const uint4 qr = *reinterpret_cast<const uint4 *>(sm + S1_STG_Q + r * 256 + c0 * 2);
+                const uint4 vr = *reinterpret_cast<const uint4 *>(sm + S1_STG_V + r * 256 + c0 * 2);
+                const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kr);
+                const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qr);
+                const __nv_bfloat162 *v2 = reinterpret_cast<const __nv_bfloat162 *>(&vr);
+                const bool live = r < L;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 a = __bfloat1622float2(k2[e]), b2 = __bfloat1622float2(q2[e]),
+                                 c2 = __bfloat1622float2(v2[e]);
+                    kf[2 * e] = live ? a.x : 0.f; kf[2 * e + 1] = live ? a.y : 0.f;
+                    qf[2 * e] = live ? b2.x : 0.f; qf[2 * e + 1] = live ? b2.y : 0.f;
+                    vf[2 * e] = live ? c2.x : 0.f; vf[2 * e + 1] = live ? c2.y : 0.f;
+                }
+                const float4 g0 = *reinterpret_cast<const float4 *>(sm + S1_STG_G + r * 512 + c0 * 4);
+                const float4 g1 = *reinterpret_cast<const float4 *>(sm + S1_STG_G + r * 512 + c0 * 4 + 16);
+                gm[0] = g0.x; gm[1] = g0.y; gm[2] = g0.z; gm[3] = g0.w;
+                gm[4] = g1.x; gm[5] = g1.y; gm[6] = g1.z; gm[7] = g1.w;
+                const float4 e0 = *reinterpret_cast<const float4 *>(eL + c0);
+                const float4 e1 = *reinterpret_cast<const float4 *>(eL + c0 + 4);
+                el[0] = e0.x; el[1] = e0.y; el[2] = e0.z; el[3] = e0.w;
+                el[4] = e1.x; el[5] = e1.y; el[6] = e1.z; el[7] = e1.w;
+            }
+            float kg[8], qg[8], kh[8], kb[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float ep = __expf(gm[e]);
+                kg[e] = kf[e] * ep;
+                qg[e] = qf[e] * ep;
+                if (!slow) {   // e^-gamma <= e^80 here: Kbar = (K e^-g) e^gamma_last
+                    kh[e] = kf[e] * __expf(-gm[e]);
+                    kb[e] = kh[e] * el[e];
+                } else {
+                    kh[e] = 0.f;
+                    kb[e] = kf[e] * __expf(gL[c0 + e] - gm[e]);
+                }
+            }
+            const uint32_t ioff = rc_img_off(r, c0);
+            *reinterpret_cast<uint4 *>(sm + S1_KG16 + ioff) = pack8_h(kg);
+            *reinterpret_cast<uint4 *>(sm + S1_V16 + ioff) = pack8_h(vf);
+            *reinterpret_cast<uint4 *>(out + IMG_Q + ioff) = pack8_h(qg);
+            *reinterpret_cast<uint4 *>(out + IMG_KT + ioff) = pack8_h(kb);
+            if (!slow) {
+                const uint32_t atom = (uint32_t)(c0 >> 5), ch0 = (uint32_t)(c0 & 31) >> 2;
+#pragma unroll
+                for (int hc = 0; hc < 2; ++hc) {
+                    const uint32_t cc = ch0 + hc;
+                    *reinterpret_cast<float4 *>(sm + S1_OPA + atom * 16384 + sw128_off(r, cc)) =
+                        make_float4(kg[4 * hc], kg[4 * hc + 1], kg[4 * hc + 2], kg[4 * hc + 3]);
+                    *reinterpret_cast<float4 *>(sm + S1_OPA + atom * 16384 + sw128_off(64 + r, cc)) =
+                        make_float4(qg[4 * hc], qg[4 * hc + 1], qg[4 * hc + 2], qg[4 * hc + 3]);
+                    *reinterpret_cast<float4 *>(sm + S1_OPB + atom * 8192 + sw128_off(r, cc)) =
+                        make_float4(kh[4 * hc], kh[4 * hc + 1], kh[4 * hc + 2], kh[4 * hc + 3]);
+                }
+            }
+            if (jj == 0 && out_prev) {
+                drain_finish(out_prev, 0, dw, du);
+                drain_issue(1, dw, du);
+            }
+        }
+        if (out_prev) drain_finish(out_prev, 1, dw, du);
+        if (tid < 128) reinterpret_cast<float *>(out + IMG_G)[tid] = eL[tid];
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+
+        // ---- A and P: tf32 MMAs, M = 128 ([K e^g ; Q e^g]), N = 64 (K e^-g).
+        // Issuing one keeps its thread busy for a few hundred cycles, so the
+        // 16 K steps are spread over four issuers (warps 12-15, accumulator =
+        // channel atom); warp 12 then starts the next task's loads (every
+        // staging tile is consumed).  Meanwhile every thread resolves the
+        // task after next.
+        if (!slow && warp >= K1_ISSUER0 && lane == 0) {
+            const int atom = warp - K1_ISSUER0;
+            fence_after_sync();
+            const uint64_t da = sdesc_k_sw128(smem_addr(sm + S1_OPA));
+            const uint64_t db = sdesc_k_sw128(smem_addr(sm + S1_OPB));
+            const uint32_t id = idesc(128, 64, FMT_TF32, FMT_TF32, 0, 0);
+#pragma unroll
+            for (int s2 = 0; s2 < 4; ++s2) {   // 8 tf32 channels per step
+                const uint32_t wi = s2 * 32;
+                mma_tf32(tmem + AP_COL + 64 * atom, sdesc_add(da, atom * 16384 + wi),
+                         sdesc_add(db, atom * 8192 + wi), id, s2 > 0);
+            }
+            mma_commit(&mbar[1]);
+            if (atom == 0 && next < ntask) { expect_tma(); tma_kqg(nxt); tma_v(nxt); }
+        }
+        row_params(nxt, next, b_cur, gs_cur);              // consumed next task
+        const PosRaw nn_raw = pos_fetch(next + stride);    // finished after the W/U MMA
+
+        float *As = reinterpret_cast<float *>(sm + S1_AS);
+        if (!slow) {
+            if (tid == 0 && next < ntask) ++n_issued;
+            fence_before_sync();
+            ok = __syncthreads_and(mbar_wait(&mbar[1], ap_it & 1));
+            ++ap_it;
+            fence_after_sync();
+            if (!ok) break;
+            {   // warp = (lane quadrant q, 16-column block cb); lane = row
+                const int q = warp & 3, cb = warp >> 2;
+                const int row = 32 * q + lane;
+                float d[16], d1[16], d2[16], d3[16];
+                tmem_ld16(tmem_at(tmem, q, AP_COL + 16 * cb), d);
+                tmem_ld16(tmem_at(tmem, q, AP_COL + 64 + 16 * cb), d1);
+                tmem_ld16(tmem_at(tmem, q, AP_COL + 128 + 16 * cb), d2);
+                tmem_ld16(tmem_at(tmem, q, AP_COL + 192 + 16 * cb), d3);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) d[e] = (d[e] + d1[e]) + (d2[e] + d3[e]);
+                if (row < 64) {
+                    const float b = sB[row];
+                    float4 *arow = reinterpret_cast<float4 *>(As + row * LD + 16 * cb);
+#pragma unroll
+                    for (int e4 = 0; e4 < 4; ++e4) {
+                        float a4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 16 * cb + 4 * e4 + e;
+                            a4[e] = row > i ? b * d[4 * e4 + e] : 0.f;
+                        }
+                        arow[e4] = make_float4(a4[0], a4[1], a4[2], a4[3]);
+                    }
+                } else {
+                    const int r = row - 64;
+                    float pv[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) pv[e] = (16 * cb + e) <= r ? d[e] : 0.f;
+                    *reinterpret_cast<uint4 *>(out + IMG_P + sw128_off(r, 2 * cb)) = pack8_h(pv);
+                    *reinterpret_cast<uint4 *>(out + IMG_P + sw128_off(r, 2 * cb + 1)) = pack8_h(pv + 8);
+                }
+            }
+        } else {
+            // ---- exact pairwise path for chunks whose decay leaves fp32 range
+            const __nv_bfloat16 *Kb = reinterpret_cast<const __nv_bfloat16 *>(sm + S1_STG_K);
+            const __nv_bfloat16 *Qb = reinterpret_cast<const __nv_bfloat16 *>(sm + S1_STG_Q);
+            const float *Gm = reinterpret_cast<const float *>(sm + S1_STG_G);
+            for (int e = tid; e < C * C; e += K1_THREADS) {
+                const int r = e >> 6, i = e & 63;
+                float a = 0.f, pp = 0.f;
+                if (i <= r && r < L) {
+                    for (int c = 0; c < D; ++c) {
+                        const float ki = __bfloat162float(Kb[i * 128 + c]) *
+                                         __expf(Gm[r * 128 + c] - Gm[i * 128 + c]);
+                        a += __bfloat162float(Kb[r * 128 + c]) * ki;
+                        pp += __bfloat162float(Qb[r * 128 + c]) * ki;
+                    }
+                }
+                As[r * LD + i] = i < r ? sB[r] * a : 0.f;
+                *reinterpret_cast<__half *>(out + IMG_P + sw128_off(r, i >> 3) + (i & 7) * 2) =
+                    __float2half_rn(pp);
+            }
+            fence_before_sync();
+            __syncthreads();
+            if (tid == 0 && next < ntask) {   // staging is consumed
+                expect_tma(); tma_kqg(nxt); tma_v(nxt);
+                ++n_issued;
+            }
+        }
+        __syncthreads();
+
+        // ---- T = (I + A)^-1 and the fp16 image of T' = T Diag(beta) (warps 0-5)
+        if (warp < 6)
+            invert_unit_lower(As, reinterpret_cast<float *>(sm + S1_TS),
+                              reinterpret_cast<float *>(sm + S1_TT),
+                              reinterpret_cast<float *>(sm + S1_FT), sB, sm + S1_TP, tid);
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+
+        // ---- W = T' (K e^g), U~ = T' V on tcgen05 (fp16, B operands MN-major);
+        // warp 0 issues W, warp 1 issues U~
+        if (lane == 0 && warp < 2) {
+            fence_after_sync();
+            const uint64_t dt = sdesc_k_sw128(smem_addr(sm + S1_TP));
+            const uint64_t db = sdesc(smem_addr(sm + (warp == 0 ? S1_KG16 : S1_V16)), 8192, 1024,
+                                      LAYOUT_SW128);
+            const uint32_t id = idesc(64, 128, FMT_F16, FMT_F16, 0, 1);
+            const uint32_t col = warp == 0 ? W_COL : U_COL;
+#pragma unroll
+            for (int s2 = 0; s2 < 4; ++s2)
+                mma_f16(tmem + col, sdesc_add(dt, 32 * s2), sdesc_add(db, 2048 * s2), id, s2 > 0);
+            mma_commit(&mbar[2]);   // waited for after the next task's gate scan
+        }
+        out_prev = out;
+        cur = nxt;
+        nxt = pos_finish(nn_raw);
+    }
+    // the last W/U MMA, then its results
+    if (ok && it > 0) {
+        ok = __syncthreads_and(mbar_wait(&mbar[2], (it - 1) & 1));
+        fence_after_sync();
+        if (ok) store_wu(out_prev);
+    }
+    if (!ok && tid == 0) {
+        ws_fail(ws_hdr, 1);
+        // let copies and MMAs still in flight finish before the CTA's shared
+        // memory and TMEM are released (bounded waits)
+        if (n_issued > n_landed) mbar_wait(&mbar[0], (n_issued - 1) & 1, 1u << 20);
+        if (it > 0) mbar_wait(&mbar[2], (it - 1) & 1, 1u << 20);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc<512>(tmem);
+}
+
+}  // namespace tcp
+}  // namespace kda

@@ -1,0 +1,199 @@
+// kda_prefill_tc.cuh -- chunked KDA prefill on the 5th-generation tensor cores
+// (tcgen05 + TMEM), bf16 inputs, fp32 state: the workspace and shared-memory
+// layouts, kernel parameters and kernel declarations shared by
+// kda_prefill_intra.cu (the per-chunk kernel), kda_prefill_chain.cu (the state
+// chain) and kda_prefill_tc.cu (the host side).
+//
+// Method: the chunkwise-parallel form of the lineage essay "GPT-2부터 Kimi
+// K3까지", section "병렬화 트릭" -- chunks of C = 64 tokens, masked attention
+// inside a chunk, the state plus a matmul between chunks, and the deltas of a
+// chunk resolved at once through a UT (Householder-style) transform -- with
+// the per-channel gate of its section "KDA: Kimi의 비법".  For a chunk with
+// per-channel cumulative log-gate gamma and entering state S:
+//
+//   A[r,i] = beta_r sum_c k_rc k_ic e^(gamma_rc - gamma_ic)   i <  r
+//   P[r,i] =        sum_c q_rc k_ic e^(gamma_rc - gamma_ic)   i <= r
+//   T  = (I + A)^-1,  T' = T Diag(beta)
+//   W  = T' (K * e^gamma),  U~ = T' V                      (independent of S)
+//   U  = U~ - W S,   O = (Q * e^gamma) S + P U,
+//   S <- Diag(e^gamma_last) S + (K * e^(gamma_last - gamma))^T U
+//
+// Two kernels split that along the only sequential dependency (the state):
+//
+//  * intra_kernel (K1) runs every (chunk, head) independently: the gate scan
+//    and factors on CUDA cores, A and P on tcgen05 (tf32), the triangular
+//    inverse on CUDA cores (fp32, 16x16 blocks), W and U~ on tcgen05 (fp16).
+//    It writes the chunk's operands to a workspace, already laid out as the
+//    shared-memory images the second kernel's MMAs read.
+//  * chain_kernel (K2) walks the chunks of one (sequence, head, block of 32
+//    state columns) in order with the fp32 state in registers: W S and Q^ S,
+//    then K^T U and P U, each a tcgen05 round trip.  Operand images arrive
+//    with bulk async copies, double buffered.  chain_wide_kernel is the same
+//    walk for all 128 columns in one CTA (for batches with many chains); for
+//    one sequence with few heads, the chunk-affine scan runs the slice chains
+//    over segments and chains the segments' maps (segment_combine_kernel).
+//
+// Gate factors inside a chunk are referenced to the chunk start (K e^gamma,
+// K e^-gamma), which stays inside fp32 while every channel's log-gate sum over
+// the chunk is above -80; a chunk beyond that forms A and P pair by pair with
+// e^(gamma_r - gamma_i) <= 1 instead, so any gate strength gives finite results.
+//
+// Operand precision (chosen with a CPU emulation against the fp64 oracle):
+// A and P use tf32 operands (the gated factors need fp32 range); every other
+// product uses fp16 operands with fp32 accumulation; the state stays fp32.
+#pragma once
+
+#include "kda_internal.cuh"
+#include "kda_tc.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+namespace kda {
+namespace tcp {
+
+using namespace tc;
+
+constexpr int C = 64;          // tokens per chunk
+constexpr int D = 128;         // dk = dv
+constexpr int DVS = 32;        // state columns per chain CTA
+constexpr int NSLICE = D / DVS;
+
+// workspace: header | chunk table | per (chunk, head) operand images
+constexpr uint32_t WS_HEADER = 256;
+constexpr uint32_t IMG_W = 0;          // W   [64 x 128] fp16, K-major SW128 (2 atoms)
+constexpr uint32_t IMG_Q = 16384;      // Q^  [64 x 128] fp16, K-major SW128 (2 atoms)
+constexpr uint32_t IMG_KT = 32768;     // Kb [64 x 128] fp16, [r][c] SW128 (MN-major A)
+constexpr uint32_t IMG_P = 49152;      // P   [64 x 64] fp16, K-major SW128
+constexpr uint32_t IMG_U = 57344;      // U~  [4 slices][64][32] fp16
+constexpr uint32_t IMG_G = 73728;      // e^gamma_last [128] fp32
+constexpr uint32_t CH_STRIDE = 74240;  // bytes per (chunk, head)
+constexpr int WINDOW_CHUNKS = 2048;    // chunks per K1/K2 window
+
+__host__ __device__ inline uint64_t ws_images_offset(int N) {
+    uint64_t off = WS_HEADER + 4ull * (uint64_t)(N + 1);
+    return (off + 1023) & ~1023ull;
+}
+
+__device__ __forceinline__ void ws_fail(int32_t *ws_hdr, int code) { atomicExch(ws_hdr, code); }
+
+// sequence holding global chunk c (chunk_base is non-decreasing)
+__device__ __forceinline__ int find_seq(const int32_t *chunk_base, int N, int c) {
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (chunk_base[mid] <= c) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// ---- per-chunk kernel: shared-memory layout and parameters ------------------
+constexpr int K1_THREADS = 512;
+constexpr int K1_ISSUER0 = 12;  // warps 12-15 issue the A/P MMAs
+constexpr uint32_t S1_STG_K = 0, S1_STG_Q = 16384, S1_STG_V = 32768;  // bf16 [64][128]
+constexpr uint32_t S1_STG_G = 49152;                                  // fp32 [64][128]
+constexpr uint32_t S1_OPA = 81920;    // tf32 [K e^g ; Q e^g]: 4 atoms x 128 rows x 128 B
+constexpr uint32_t S1_OPB = 147456;   // tf32 K e^-g: 4 atoms x 64 rows x 128 B
+constexpr uint32_t S1_KG16 = 180224;  // fp16 K e^g, [r][c] 128B-swizzled (MN-major B)
+constexpr uint32_t S1_V16 = 196608;   // fp16 V, same layout
+constexpr uint32_t S1_TP = 212992;    // fp16 T', K-major SW128 [r][i]
+constexpr uint32_t S1_MISC = 221184;
+constexpr uint32_t S1_BYTES = S1_MISC + 4096 + 1024;
+// after the A/P MMA has completed the operand area is reused by the inverse:
+constexpr int LD = 68;                          // fp32 row stride of the 64 x 64 tiles
+constexpr uint32_t TILE_BYTES = 64 * LD * 4;    // 17,408
+constexpr uint32_t S1_AS = S1_OPA;                   // A    fp32 [64][LD]
+constexpr uint32_t S1_TS = S1_OPA + TILE_BYTES;      // T    fp32 [64][LD]
+constexpr uint32_t S1_TT = S1_OPA + 2 * TILE_BYTES;  // T_RR transposed (diagonal blocks)
+constexpr uint32_t S1_FT = S1_OPA + 3 * TILE_BYTES;  // F = T_RR A_RJ, transposed
+static_assert(S1_FT + TILE_BYTES <= S1_KG16, "inverse scratch overlaps the fp16 operands");
+constexpr int AP_COL = 0, W_COL = 256, U_COL = 384;  // TMEM: 4 A/P partials of 64, W, U~
+constexpr float RANGE_LIMIT = 80.f;                   // e^80 stays inside fp32
+
+struct K1Params {
+    CUtensorMap tm_q, tm_k, tm_v, tm_g;   // 3D maps over [T][H][128] (tm_g unused for scalar gates)
+    const float *g;                       // scalar gates [T][H] (when scalar_gate)
+    const float *beta;
+    const int32_t *cu;
+    uint8_t *ws;
+    int N, H;
+    int64_t T;
+    int w0, w1;
+    int scalar_gate;
+};
+
+// ---- chain kernel (one 32-column slice per CTA) ------------------------------
+constexpr int K2_THREADS = 128;
+constexpr uint32_t S2_WQ = 0;          // [W ; Q^] K-major SW128, 2 atoms x 128 rows
+constexpr uint32_t S2_KB = 32768;      // Kbar [r][c] SW128 (MN-major A)
+constexpr uint32_t S2_PZ = 49152;      // [0 ; P] K-major SW128, 128 rows (rows 0-63 zero)
+constexpr uint32_t S2_U = 65536;       // U~ slice [64][32] fp16
+constexpr uint32_t S2_G = 69632;       // e^gamma_last [128] fp32
+constexpr uint32_t S2_STAGE = 70656;   // bytes per stage (multiple of 1024)
+constexpr uint32_t S2_SOP = 2 * S2_STAGE;                 // S fp16, K=128 x N=32, MN-major
+constexpr uint32_t S2_UOP = S2_SOP + 8192;                // U fp16, K=64 x N=32, MN-major
+constexpr uint32_t S2_MISC = S2_UOP + 4096;
+constexpr uint32_t S2_BYTES = S2_MISC + 256 + 1024;
+constexpr uint32_t S2_TX = 4 * 8192 + 16384 + 8192 + 4096 + 512;   // bytes landing per stage
+// TMEM set s (0, 1) at column 128 s: D_A +0, D_B +32, D_S +64, D_S2 +96
+
+struct K2Params {
+    const float *S0;
+    float *S_T;
+    __nv_bfloat16 *o;
+    const int32_t *cu;
+    uint8_t *ws;
+    int N, H;
+    int64_t T;
+    int w0, w1;
+    // chunk-affine scan of one sequence (N = 1), see segment_launch_plan
+    int nseg;          // 0: off; else the window's chunks in nseg segments
+    int seg_len;       // chunks per segment
+    int phase;         // 0: segment maps (and segment 0 itself), 1: segments 1..nseg-1
+    float *smaps;      // [H][nseg][3][128][128] fp32: M_s, B_s, start state of segment s
+};
+
+// Roles of a chain CTA in a segment launch.
+enum : int { SEG_FULL = 0, SEG_B = 1, SEG_M = 2 };
+constexpr int SMAP_M = 0, SMAP_B = 1, SMAP_START = 2;
+__host__ __device__ inline float *smap(float *smaps, int nseg, int h, int s, int which) {
+    return smaps + ((((size_t)h * nseg + s) * 3 + which) << 14);   // 128 x 128 each
+}
+
+// ---- combine step of the chunk-affine scan -----------------------------------
+constexpr int COMB_THREADS = 512;
+constexpr int SSH_LD = 40;
+constexpr uint32_t COMB_BYTES = (128 * 129 + 128 * SSH_LD) * sizeof(float);
+// ---- chain kernel, wide form (all 128 columns per CTA) ------------------------
+constexpr int K2W_THREADS = 512;
+constexpr uint32_t S2W_WQ = 0;          // [W ; Q^] K-major SW128, 2 atoms x 128 rows
+constexpr uint32_t S2W_KB = 32768;      // Kbar [r][c] SW128 (MN-major A)
+constexpr uint32_t S2W_PZ = 49152;      // [0 ; P] K-major SW128, 128 rows (rows 0-63 zero)
+constexpr uint32_t S2W_U = 65536;       // U~ [4 column blocks][64][32] fp16
+constexpr uint32_t S2W_G = 81920;       // e^gamma_last [128] fp32
+constexpr uint32_t S2W_STAGE = 82944;   // bytes per stage (multiple of 1024)
+constexpr uint32_t S2W_SOP = 2 * S2W_STAGE;                 // S fp16, K = 128 x N = 128, MN-major
+constexpr uint32_t S2W_UOP = S2W_SOP + 32768;               // U fp16, K = 64 x N = 128, MN-major
+constexpr uint32_t S2W_MISC = S2W_UOP + 16384;
+constexpr uint32_t S2W_BYTES = S2W_MISC + 256 + 1024;
+constexpr uint32_t S2W_TX = 4 * 8192 + 16384 + 8192 + 16384 + 512;   // bytes landing per stage
+// TMEM set s (0, 1) at column 256 s: A_s +0, B_s +128
+
+
+// ---- kernels -----------------------------------------------------------------
+__global__ void __launch_bounds__(1024)
+chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int cap,
+                   int32_t *ws_hdr, int32_t *chunk_base);
+__global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_constant__ K1Params p);
+__global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p);
+__global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Params p);
+__global__ void __launch_bounds__(COMB_THREADS) segment_combine_kernel(float *smaps, int nseg);
+
+}  // namespace tcp
+}  // namespace kda
