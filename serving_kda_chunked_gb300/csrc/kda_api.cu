@@ -14,13 +14,14 @@ kda_status cuda_status(cudaError_t e) {
     return KDA_ERR_CUDA;
 }
 
-// Shared by the per-channel (KDA) and per-head (Gated DeltaNet) entry points:
-// they differ only in the layout of g ([T, H, dk] vs [T, H]).
+// Shared by the per-channel (KDA) and per-head (Gated DeltaNet) entry points,
+// which differ only in the layout of g ([T, H, dk] vs [T, H]), and by the
+// no-allocation entry point, which has no workspace argument.
 kda_status prefill_impl(const void *q, const void *k, const void *v, const float *g,
                         const float *beta, const float *S0, const int32_t *cu_seqlens,
                         int32_t N, int64_t T_total, int32_t H, int32_t dk, int32_t dv,
                         int32_t dtype, int32_t chunk, void *o, float *S_T, void *workspace,
-                        uint64_t workspace_bytes, bool scalar_gate, void *stream) {
+                        uint64_t workspace_bytes, bool scalar_gate, bool noalloc, void *stream) {
     if (N < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
     if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
     if (dk <= 0 || dv <= 0 || chunk <= 0) return KDA_ERR_INVALID_ARG;
@@ -37,9 +38,13 @@ kda_status prefill_impl(const void *q, const void *k, const void *v, const float
     const bool tensor_path = dtype == KDA_BF16 && dk == 128;
     if (tensor_path) {
         if (T_total / 64 + N > 0x3fffffffLL) return KDA_ERR_UNSUPPORTED;
-        const uint64_t need = kda::prefill_tc_workspace_bytes(N, T_total, H);
-        if (!workspace || workspace_bytes < need || !aligned16(workspace))
-            return KDA_ERR_INVALID_ARG;
+        if (noalloc) {
+            if (kda::noalloc_window_chunks(N, H) < 1) return KDA_ERR_TOO_LARGE;
+        } else {
+            const uint64_t need = kda::prefill_tc_workspace_bytes(N, T_total, H);
+            if (!workspace || workspace_bytes < need || !aligned16(workspace))
+                return KDA_ERR_INVALID_ARG;
+        }
     }
 
     kda::PrefillArgs a;
@@ -48,9 +53,9 @@ kda_status prefill_impl(const void *q, const void *k, const void *v, const float
     a.N = N; a.H = H; a.dk = dk; a.dv = dv; a.dtype = dtype; a.chunk = chunk;
     a.T = T_total;
     a.scalar_gate = scalar_gate;
-    if (tensor_path)
-        return cuda_status(kda::launch_prefill_tc(a, workspace, (cudaStream_t)stream));
-    return cuda_status(kda::launch_prefill_simt(a, (cudaStream_t)stream));
+    if (!tensor_path) return cuda_status(kda::launch_prefill_simt(a, (cudaStream_t)stream));
+    if (noalloc) return cuda_status(kda::launch_prefill_tc_noalloc(a, (cudaStream_t)stream));
+    return cuda_status(kda::launch_prefill_tc(a, workspace, (cudaStream_t)stream));
 }
 
 kda_status decode_impl(const void *q, const void *k, const void *v, const float *g,
@@ -91,7 +96,7 @@ kda_status kda_prefill_chunked(const void *q, const void *k, const void *v,
                                void *workspace, uint64_t workspace_bytes,
                                void *stream) {
     return prefill_impl(q, k, v, g, beta, S0, cu_seqlens, N, T_total, H, dk, dv, dtype, chunk,
-                        o, S_T, workspace, workspace_bytes, false, stream);
+                        o, S_T, workspace, workspace_bytes, false, false, stream);
 }
 
 kda_status kda_gdn_prefill_chunked(const void *q, const void *k, const void *v,
@@ -103,7 +108,7 @@ kda_status kda_gdn_prefill_chunked(const void *q, const void *k, const void *v,
                                    void *workspace, uint64_t workspace_bytes,
                                    void *stream) {
     return prefill_impl(q, k, v, g, beta, S0, cu_seqlens, N, T_total, H, dk, dv, dtype, chunk,
-                        o, S_T, workspace, workspace_bytes, true, stream);
+                        o, S_T, workspace, workspace_bytes, true, false, stream);
 }
 
 kda_status kda_prefill_chunked_noalloc(const void *q, const void *k, const void *v,
@@ -113,32 +118,8 @@ kda_status kda_prefill_chunked_noalloc(const void *q, const void *k, const void 
                                        int32_t dk, int32_t dv, int32_t dtype,
                                        int32_t chunk, void *o, float *S_T,
                                        void *stream) {
-    if (N < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
-    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
-    if (dk <= 0 || dv <= 0 || chunk <= 0) return KDA_ERR_INVALID_ARG;
-    if (!head_ok(dk, dv) || chunk != 64) return KDA_ERR_UNSUPPORTED;
-    if (N == 0) return T_total == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
-    if (!cu_seqlens || !S_T) return KDA_ERR_INVALID_ARG;
-    if (T_total > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) ||
-        !aligned16(o) || !aligned16(S0) || !aligned16(S_T) || !aligned4(beta) ||
-        !aligned4(cu_seqlens))
-        return KDA_ERR_INVALID_ARG;
-    if ((int64_t)N * H * (dv / 32) > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
-    const bool tensor_path = dtype == KDA_BF16 && dk == 128;
-    if (tensor_path) {
-        if (T_total / 64 + N > 0x3fffffffLL) return KDA_ERR_UNSUPPORTED;
-        if (kda::noalloc_window_chunks(N, H) < 1) return KDA_ERR_TOO_LARGE;
-    }
-
-    kda::PrefillArgs a;
-    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S0 = S0;
-    a.cu_seqlens = cu_seqlens; a.o = o; a.S_T = S_T;
-    a.N = N; a.H = H; a.dk = dk; a.dv = dv; a.dtype = dtype; a.chunk = chunk;
-    a.T = T_total;
-    if (tensor_path)
-        return cuda_status(kda::launch_prefill_tc_noalloc(a, (cudaStream_t)stream));
-    return cuda_status(kda::launch_prefill_simt(a, (cudaStream_t)stream));
+    return prefill_impl(q, k, v, g, beta, S0, cu_seqlens, N, T_total, H, dk, dv, dtype, chunk,
+                        o, S_T, nullptr, 0, false, true, stream);
 }
 
 uint64_t kda_noalloc_scratch_bytes(void) { return (uint64_t)KDA_NOALLOC_SCRATCH_MIB << 20; }
@@ -207,6 +188,6 @@ const char *kda_status_string(int32_t status) {
     }
 }
 
-int32_t kda_abi_version(void) { return (2 << 16) | 1; }
+int32_t kda_abi_version(void) { return (2 << 16) | 2; }
 
 }  // extern "C"
