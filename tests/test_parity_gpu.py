@@ -545,3 +545,14 @@ def test_gdn_decode_pooled_slots():
         assert torch.all(o[1] == 0)
         untouched = [p for p in range(P) if p not in idx]
         assert torch.equal(pool[untouched], before[untouched])
+
+
+def test_prefill_more_heads_than_one_wave():
+    """H=48, one sequence: 192 chain slices, more than the SMs, so the slice
+    chains run in two waves; 48 heads per chunk in the per-chunk kernel."""
+    cfg = ki.PrefillConfig("h48", H=48, d=128, dtype="bf16", T=1000, s0_std=0.1)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=71)
+    o, S_T = _run_prefill(inp)
+    o_ref, S_ref = _oracle_prefill(inp)
+    assert_close("o", o, o_ref, 2e-3)
+    assert_close("S_T", S_T, S_ref, 2e-3)
