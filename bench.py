@@ -231,23 +231,41 @@ def device_id_for_smi(local):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def bench_prefill(args, world, kda, ki, torch):
+def bench_prefill(args, world, kda, ki, torch, workload="single", heads=None, tokens=None,
+                  api="workspace"):
+    """Prefill calls on one of the prefill workloads (the benchmark line uses
+    "single" as drawn; --part prefill picks another workload, other head counts
+    or lengths of the single sequence, or the no-allocation entry point, for
+    profiling)."""
     dev = torch.device("cuda", torch.cuda.current_device())
-    inp = ki.prefill_inputs("single", device=dev)
+    over = {}
+    if heads is not None:
+        over["H"] = heads
+    if tokens is not None:
+        over["T"] = tokens
+    cfg = ki.prefill_config(workload, **over) if over else workload
+    inp = ki.prefill_inputs(cfg, device=dev)
     names = ("q", "k", "v", "g", "beta")
     in_bytes = sum(inp[n].numel() * inp[n].element_size() for n in names)
     n_copies = max(2, math.ceil(2 * L2_BYTES / in_bytes) + 1)
     sets = [inp] + [{n: inp[n].clone() for n in names} for _ in range(n_copies - 1)]
     cu = inp["cu_seqlens"]
-    o = torch.empty((T_PREFILL, H, D), dtype=torch.bfloat16, device=dev)
-    S_T = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
-    ws = torch.empty(kda.kda_prefill_workspace_size(1, T_PREFILL, H, D, D, torch.bfloat16),
-                     dtype=torch.uint8, device=dev)
+    T, Hn, N = inp["q"].shape[0], inp["q"].shape[1], cu.shape[0] - 1
+    o = torch.empty((T, Hn, D), dtype=torch.bfloat16, device=dev)
+    S_T = torch.empty((N, Hn, D, D), dtype=torch.float32, device=dev)
+    ws = None
+    if api == "workspace":
+        ws = torch.empty(kda.kda_prefill_workspace_size(N, T, Hn, D, D, torch.bfloat16),
+                         dtype=torch.uint8, device=dev)
 
     def step(i):
         s = sets[i % n_copies]
-        kda.kda_prefill_chunked(s["q"], s["k"], s["v"], s["g"], s["beta"], cu, None,
-                                o=o, S_T=S_T, workspace=ws)
+        if ws is None:
+            kda.kda_prefill_chunked_noalloc(s["q"], s["k"], s["v"], s["g"], s["beta"], cu,
+                                            inp["S0"], o=o, S_T=S_T)
+        else:
+            kda.kda_prefill_chunked(s["q"], s["k"], s["v"], s["g"], s["beta"], cu, inp["S0"],
+                                    o=o, S_T=S_T, workspace=ws)
 
     for i in range(args.warmup):
         step(i)
@@ -278,7 +296,8 @@ def bench_prefill(args, world, kda, ki, torch):
     barrier(world)
     ms_total = max_over_ranks(world, ms_total)
     return dict(ms_per_step=ms_total / args.steps, launch_ms=launch_ms,
-                clocks=clk.summary(), in_bytes=in_bytes, n_copies=n_copies)
+                clocks=clk.summary(), in_bytes=in_bytes, n_copies=n_copies, tokens=T,
+                tokens_per_s=T / (ms_total / args.steps) * 1e3)
 
 
 def bench_prefill_e2e(args, world, kda, ki, torch):
@@ -413,8 +432,11 @@ def run_ours(args):
     peaks, peak_kind = load_peaks()
 
     if args.part != "all":
-        fn = bench_prefill if args.part == "prefill" else bench_decode
-        res = fn(args, world, kda, ki, torch)
+        if args.part == "prefill":
+            res = bench_prefill(args, world, kda, ki, torch, args.workload, args.heads,
+                                args.tokens, args.api)
+        else:
+            res = bench_decode(args, world, kda, ki, torch)
         if rank == 0:
             print("part %s: %s" % (args.part, {k: v for k, v in res.items() if k != "clocks"}))
         return
@@ -543,6 +565,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=("single", "varlen", "long"), default="single",
+                    help="prefill workload of --part prefill (the benchmark line always uses "
+                         "the single-sequence workload)")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="--part prefill: head count of the drawn workload (default: its own)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="--part prefill --workload single: sequence length (default 8192)")
+    ap.add_argument("--api", choices=("workspace", "noalloc"), default="workspace",
+                    help="--part prefill: the entry point (noalloc: the fixed-scratch call, "
+                         "which runs the state chain without the chunk-affine scan)")
     ap.add_argument("--part", choices=("all", "prefill", "decode"), default="all",
                     help="profiling aid: run only one sub-benchmark (prints no JSON line)")
     ap.add_argument("--decode-steps", type=int, default=STEPS_DEC,
