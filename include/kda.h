@@ -161,6 +161,60 @@ kda_status kda_prefill_chunked_noalloc(const void *q, const void *k, const void 
 uint64_t kda_noalloc_scratch_bytes(void);
 
 /*
+ * kda_prefill_chunked_host -- kda_prefill_chunked with the tensors in HOST
+ * memory: the call copies the inputs in and the outputs out itself, and
+ * overlaps those copies with the kernels.  (No counterpart in the method's
+ * description; it serves callers whose activations live on the host.)
+ *
+ *   q, k, v, g, beta, S0, o, S_T   as kda_prefill_chunked, in host memory;
+ *              page-locked memory (cudaHostAlloc, cudaHostRegister) lets the
+ *              copies run asynchronously, pageable memory works but the
+ *              runtime then stages each copy through the host
+ *   cu_seqlens [N + 1] int32 in host memory, read by this call on the host:
+ *              cu[0] = 0, non-decreasing, cu[N] = T_total, else
+ *              KDA_ERR_INVALID_ARG (so T_total < 2^31)
+ *   workspace  DEVICE scratch of at least kda_prefill_host_workspace_size(...)
+ *              bytes, 16-byte aligned; calls sharing it must not overlap
+ *
+ * The token range is cut into up to 16 pieces (at least 512 and at most
+ * 16,384 tokens each, every cut on a 64-token chunk boundary of the sequence
+ * it falls in).  Each piece is copied into one of two device staging slots,
+ * runs as a packed prefill over the sequences it overlaps (their states
+ * carried in a device state buffer in the workspace, exactly as the state
+ * crosses windows inside one kda_prefill_chunked call), and its outputs are
+ * copied back while the next piece is copied in and computed.  The results
+ * equal those of kda_prefill_chunked on the same values.
+ *
+ * The copies run on two internal streams per device (created, with their
+ * events, on the first call on that device and kept until the process ends);
+ * the call is ordered after earlier work on `stream`, and `stream` reaches
+ * its end only after the last copy into o and S_T.  Host buffers must stay
+ * valid and unchanged (outputs: unread) until then.  Calls from several host
+ * threads are serialised while they enqueue.  kda_prefill_check(workspace,
+ * stream) reports the device-side status of every piece.  Pointers that the
+ * runtime identifies as device memory in place of a host buffer (or host
+ * memory as the workspace) are rejected with KDA_ERR_INVALID_ARG.
+ */
+kda_status kda_prefill_chunked_host(const void *q, const void *k, const void *v,
+                                    const float *g, const float *beta,
+                                    const float *S0, const int32_t *cu_seqlens,
+                                    int32_t N, int64_t T_total, int32_t H,
+                                    int32_t dk, int32_t dv, int32_t dtype,
+                                    int32_t chunk, void *o, float *S_T,
+                                    void *workspace, uint64_t workspace_bytes,
+                                    void *stream);
+
+/*
+ * Bytes of device workspace kda_prefill_chunked_host needs for these sizes
+ * (staging for two pieces, the prefill scratch of one piece, the N states and
+ * the offsets).  Pure host arithmetic; 0 for arguments the call would reject
+ * on their sizes alone (and for N = 0, which needs none).
+ */
+uint64_t kda_prefill_host_workspace_size(int32_t N, int64_t T_total, int32_t H,
+                                         int32_t dk, int32_t dv, int32_t dtype,
+                                         int32_t chunk);
+
+/*
  * kda_decode_step -- one token for each of B independent sequences; the
  * states are updated in place.
  *

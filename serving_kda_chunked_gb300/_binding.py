@@ -63,6 +63,10 @@ def load() -> ctypes.CDLL:
         lib.kda_prefill_chunked_noalloc.argtypes = [
             vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, i32, vp, vp, vp]
         lib.kda_prefill_chunked_noalloc.restype = ctypes.c_int
+        lib.kda_prefill_chunked_host.argtypes = lib.kda_prefill_chunked.argtypes
+        lib.kda_prefill_chunked_host.restype = ctypes.c_int
+        lib.kda_prefill_host_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32, i32]
+        lib.kda_prefill_host_workspace_size.restype = u64
         lib.kda_noalloc_scratch_bytes.argtypes = []
         lib.kda_noalloc_scratch_bytes.restype = u64
         lib.kda_prefill_check.argtypes = [vp, vp]
@@ -162,6 +166,68 @@ def _prefill(fn, gate_shape, q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_T, wo
         _ptr(workspace), ws_bytes, _stream(stream))
     if st != KDA_OK:
         raise KdaError(fn, st)
+    return o, S_T
+
+
+def _check_host(name, t, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.device.type != "cpu":
+        raise ValueError("%s must be a host (CPU) tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+def kda_prefill_host_workspace_size(N, T, H, dk, dv, dtype, chunk=64) -> int:
+    """Device workspace bytes ``kda_prefill_chunked_host`` needs."""
+    code = _DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(load().kda_prefill_host_workspace_size(N, T, H, dk, dv, code, chunk))
+
+
+def kda_prefill_chunked_host(q, k, v, g, beta, cu_seqlens, S0=None, *, chunk: int = 64,
+                             o=None, S_T=None, workspace=None, device=None, stream=None):
+    """``kda_prefill_chunked`` over HOST tensors (``kda_prefill_chunked_host``
+    in kda.h): q, k, v, g, beta, cu_seqlens, S0 and the outputs o, S_T are CPU
+    tensors (page-locked ones let the copies overlap the kernels); the call
+    copies them to and from the GPU itself.  ``workspace`` is a CUDA uint8
+    tensor (allocated on ``device``, default the current one, if omitted).
+    Returns (o, S_T); they are complete once ``stream`` has reached this call's
+    end (synchronise before reading them)."""
+    _check_host("q", q)
+    if q.dtype not in _DTYPE_CODE:
+        raise ValueError("q must be bfloat16 or float32")
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    _check_host("k", k, q.dtype, (T, H, dk))
+    _check_host("v", v, q.dtype, (T, H, dv))
+    _check_host("g", g, torch.float32, (T, H, dk))
+    _check_host("beta", beta, torch.float32, (T, H))
+    _check_host("cu_seqlens", cu_seqlens, torch.int32)
+    N = cu_seqlens.shape[0] - 1
+    if S0 is not None:
+        _check_host("S0", S0, torch.float32, (N, H, dk, dv))
+    pin = q.is_pinned()
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=q.dtype, pin_memory=pin)
+    _check_host("o", o, q.dtype, (T, H, dv))
+    if S_T is None:
+        S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, pin_memory=pin)
+    _check_host("S_T", S_T, torch.float32, (N, H, dk, dv))
+    if workspace is None:
+        need = kda_prefill_host_workspace_size(N, T, H, dk, dv, q.dtype, chunk)
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _check_cuda("workspace", workspace, torch.uint8)
+    st = load().kda_prefill_chunked_host(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
+        N, T, H, dk, dv, _DTYPE_CODE[q.dtype], int(chunk), _ptr(o), _ptr(S_T),
+        _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != KDA_OK:
+        raise KdaError("kda_prefill_chunked_host", st)
     return o, S_T
 
 

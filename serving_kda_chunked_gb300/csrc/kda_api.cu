@@ -122,6 +122,67 @@ kda_status kda_prefill_chunked_noalloc(const void *q, const void *k, const void 
                         o, S_T, nullptr, 0, false, true, stream);
 }
 
+kda_status kda_prefill_chunked_host(const void *q, const void *k, const void *v,
+                                    const float *g, const float *beta,
+                                    const float *S0, const int32_t *cu_seqlens,
+                                    int32_t N, int64_t T_total, int32_t H,
+                                    int32_t dk, int32_t dv, int32_t dtype,
+                                    int32_t chunk, void *o, float *S_T,
+                                    void *workspace, uint64_t workspace_bytes,
+                                    void *stream) {
+    if (N < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
+    if (dk <= 0 || dv <= 0 || chunk <= 0) return KDA_ERR_INVALID_ARG;
+    if (!head_ok(dk, dv) || chunk != 64) return KDA_ERR_UNSUPPORTED;
+    if (N == 0) return T_total == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+    if (T_total > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;   // offsets are int32
+    if (!cu_seqlens || !S_T) return KDA_ERR_INVALID_ARG;
+    if (T_total > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    if ((int64_t)N * H * (dv / 32) > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+    const uint64_t need = kda::prefill_host_workspace_bytes(N, T_total, H, dk, dv, dtype);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KDA_ERR_INVALID_ARG;
+    // host buffers must not be device memory, the workspace must be (checked
+    // where the runtime can tell)
+    const void *host_ptrs[] = {cu_seqlens, q, k, v, g, beta, S0, o, S_T};
+    for (const void *ptr : host_ptrs) {
+        if (!ptr) continue;
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) { (void)cudaGetLastError(); continue; }
+        if (at.type == cudaMemoryTypeDevice) return KDA_ERR_INVALID_ARG;
+    }
+    {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, workspace) == cudaSuccess) {
+            if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+                return KDA_ERR_INVALID_ARG;
+        } else {
+            (void)cudaGetLastError();
+        }
+    }
+    // the offsets are read here: cu[0] = 0, non-decreasing, cu[N] = T_total
+    if (cu_seqlens[0] != 0 || (int64_t)cu_seqlens[N] != T_total) return KDA_ERR_INVALID_ARG;
+    for (int32_t n = 0; n < N; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n]) return KDA_ERR_INVALID_ARG;
+
+    kda::HostPrefillArgs h;
+    kda::PrefillArgs &a = h.args;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S0 = S0;
+    a.cu_seqlens = nullptr; a.o = o; a.S_T = S_T;
+    a.N = N; a.H = H; a.dk = dk; a.dv = dv; a.dtype = dtype; a.chunk = chunk;
+    a.T = T_total;
+    a.scalar_gate = false;
+    h.cu_host = cu_seqlens;
+    return cuda_status(kda::launch_prefill_host(h, workspace, (cudaStream_t)stream));
+}
+
+uint64_t kda_prefill_host_workspace_size(int32_t N, int64_t T_total, int32_t H, int32_t dk,
+                                         int32_t dv, int32_t dtype, int32_t chunk) {
+    if (N <= 0 || T_total < 0 || T_total > 0x7fffffffLL || H <= 0 || !head_ok(dk, dv) ||
+        chunk != 64 || (dtype != KDA_BF16 && dtype != KDA_FP32))
+        return 0;
+    return kda::prefill_host_workspace_bytes(N, T_total, H, dk, dv, dtype);
+}
+
 uint64_t kda_noalloc_scratch_bytes(void) { return (uint64_t)KDA_NOALLOC_SCRATCH_MIB << 20; }
 
 uint64_t kda_prefill_workspace_size(int32_t N, int64_t T_total, int32_t H, int32_t dk,
@@ -188,6 +249,6 @@ const char *kda_status_string(int32_t status) {
     }
 }
 
-int32_t kda_abi_version(void) { return (2 << 16) | 2; }
+int32_t kda_abi_version(void) { return (2 << 16) | 3; }
 
 }  // extern "C"

@@ -197,3 +197,52 @@ def test_binding_rejects_host_tensors(lib):
     with pytest.raises(ValueError, match="CUDA"):
         kda.kda_prefill_chunked_noalloc(q, q, q, q, torch.zeros(4, 2),
                                         torch.zeros(2, dtype=torch.int32))
+
+
+def _host_prefill(lib, cu_vals, **kw):
+    """kda_prefill_chunked_host with a real host offsets array."""
+    cu = (ctypes.c_int32 * len(cu_vals))(*cu_vals)
+    a = dict(q=P, k=P, v=P, g=P, beta=P, S0=None, N=len(cu_vals) - 1, T=cu_vals[-1], H=2,
+             dk=128, dv=128, dtype=0, chunk=64, o=P, S_T=P, ws=P, ws_bytes=1 << 40)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.kda_prefill_chunked_host(
+        vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), vp(a["S0"]),
+        ctypes.cast(cu, vp), a["N"], a["T"], a["H"], a["dk"], a["dv"], a["dtype"], a["chunk"],
+        vp(a["o"]), vp(a["S_T"]), vp(a["ws"]), a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("cu_vals,kw,expect", [
+    ([0, 64], dict(H=0), kda.KDA_ERR_INVALID_ARG),
+    ([0, 64], dict(dk=96, dv=96), kda.KDA_ERR_UNSUPPORTED),
+    ([0, 64], dict(chunk=128), kda.KDA_ERR_UNSUPPORTED),
+    ([0, 64], dict(dtype=5), kda.KDA_ERR_INVALID_ARG),
+    ([0, 64], dict(q=None), kda.KDA_ERR_INVALID_ARG),
+    ([0, 64], dict(S_T=None), kda.KDA_ERR_INVALID_ARG),
+    ([0, 64], dict(ws=None), kda.KDA_ERR_INVALID_ARG),
+    ([0, 64], dict(ws_bytes=4096), kda.KDA_ERR_INVALID_ARG),
+    ([0, 64], dict(ws=P + 8), kda.KDA_ERR_INVALID_ARG),
+    ([0, 64], dict(T=1 << 31), kda.KDA_ERR_INVALID_ARG),
+    ([1, 64], {}, kda.KDA_ERR_INVALID_ARG),             # cu[0] != 0
+    ([0, 64], dict(T=65), kda.KDA_ERR_INVALID_ARG),     # cu[N] != T
+    ([0, 40, 30, 64], {}, kda.KDA_ERR_INVALID_ARG),     # decreasing offsets
+    ([0], dict(N=0, T=0), kda.KDA_OK),                  # empty batch: no-op
+    ([0], dict(N=0, T=5), kda.KDA_ERR_INVALID_ARG),
+])
+def test_host_prefill_validation(lib, cu_vals, kw, expect):
+    assert _host_prefill(lib, cu_vals, **kw) == expect
+
+
+def test_host_workspace_size(lib):
+    f = kda.kda_prefill_host_workspace_size
+    import torch
+    small = f(1, 8192, 32, 128, 128, torch.bfloat16)
+    # two staging slots of 512 tokens (q, k, v bf16, g, beta fp32; o bf16)
+    # plus the prefill scratch of one piece and the state
+    assert small >= 2 * 512 * 32 * (3 * 256 + 512 + 4 + 256) + 32 * 128 * 128 * 4
+    assert f(1, 1 << 20, 32, 128, 128, torch.bfloat16) > small    # 16,384-token pieces
+    assert f(4, 8192, 32, 128, 128, torch.bfloat16) > small       # more states
+    assert f(1, 256, 2, 64, 64, torch.float32) > 0                # CUDA-core path
+    assert f(0, 0, 32, 128, 128, torch.bfloat16) == 0
+    assert f(1, 64, 32, 96, 96, torch.bfloat16) == 0
+    assert f(1, 1 << 31, 32, 128, 128, torch.bfloat16) == 0
