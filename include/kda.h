@@ -176,7 +176,7 @@ uint64_t kda_noalloc_scratch_bytes(void);
  *   workspace  DEVICE scratch of at least kda_prefill_host_workspace_size(...)
  *              bytes, 16-byte aligned; calls sharing it must not overlap
  *
- * The token range is cut into up to 16 pieces (at least 512 and at most
+ * The token range is cut into about 8 pieces (at least 512 and at most
  * 16,384 tokens each, every cut on a 64-token chunk boundary of the sequence
  * it falls in).  Each piece is copied into one of two device staging slots,
  * runs as a packed prefill over the sequences it overlaps (their states

@@ -1,6 +1,6 @@
 // kda_host.cu -- prefill from host memory (kda_prefill_chunked_host in kda.h).
 //
-// The token range is cut into pieces of a few hundred to 16 K tokens.  Each
+// The token range is cut into pieces of 512 to 16 K tokens.  Each
 // piece's inputs are copied into one of two device staging slots on a copy
 // stream, the piece runs as an ordinary packed prefill on the caller's stream
 // (the states of its sequences carried in a device state buffer, read and
@@ -18,12 +18,34 @@
 
 #include "../../include/kda.h"
 #include "kda_internal.cuh"
+#include "kda_prefill_tc.cuh"
 
 namespace kda {
 
 namespace {
 
-constexpr int64_t PIECES = 16;        // pieces per call (before the limits below)
+// Workspace of the tensor-core prefill for any call of at most N sequences
+// and T tokens (a piece): the operand images grow with N and T; the segment
+// maps of the chunk-affine scan (one sequence only) are taken at their
+// largest segment count (the limit the scan plan of the tensor-core prefill
+// uses), which is not monotone in T.
+size_t prefill_tc_piece_workspace_bytes(int32_t N, int64_t T, int32_t H) {
+    using namespace tcp;
+    const int64_t bound = (T + C - 1) / C + N;
+    const int64_t wch = bound < WINDOW_CHUNKS ? bound : WINDOW_CHUNKS;
+    const size_t images = (size_t)ws_images_offset(N) + (size_t)wch * (size_t)H * CH_STRIDE;
+    const int64_t gmax = H > 0 ? (128 / H + 4) / 8 : 0;
+    const size_t maps = gmax >= 4 ? (size_t)H * gmax * 3 * (D * D * sizeof(float)) : 0;
+    return ((images + 255) & ~(size_t)255) + maps;
+}
+
+// Each host->device copy carries a fixed cost of ~3 us on top of the link
+// time (211 GB/s measured from pinned memory), and the last piece's kernels
+// and output copy are not overlapped: 8 pieces of a call of 8 K tokens
+// measured 1.93 ms per call, 16 pieces 1.99 ms, 4 pieces 1.94 ms (the copies
+// alone, as one piece, take 1.70 ms).  Alternating the pieces over two copy
+// streams measured slower (2.06 ms for 16 pieces).
+constexpr int64_t PIECES = 8;         // pieces per call (before the limits below)
 constexpr int64_t PIECE_MIN = 512;    // tokens: keeps every SM busy in the per-chunk kernel
 constexpr int64_t PIECE_MAX = 16384;  // tokens: bounds the staging buffers
 constexpr int64_t CHUNK = 64;

@@ -42,9 +42,6 @@ size_t prefill_tc_workspace_bytes(int32_t N, int64_t T, int32_t H);
 // (0: not even one chunk fits).
 int64_t noalloc_window_chunks(int32_t N, int32_t H);
 cudaError_t launch_prefill_tc_noalloc(const PrefillArgs &a, cudaStream_t stream);
-// Workspace for any tensor-core call of at most N sequences and T tokens.
-size_t prefill_tc_piece_workspace_bytes(int32_t N, int64_t T, int32_t H);
-
 // Prefill from host memory: q, k, v, g, beta, S0, o and S_T of `args` are
 // host pointers, cu_seqlens of `args` is unused; `cu_host` holds the
 // validated offsets in host memory.

@@ -84,17 +84,6 @@ size_t smaps_bytes(int32_t N, int32_t H, int64_t wch) {
 
 }  // namespace
 
-size_t prefill_tc_piece_workspace_bytes(int32_t N, int64_t T, int32_t H) {
-    // the images grow with N and T; the segment maps (one sequence only) are
-    // taken at their largest segment count, which is not monotone in T
-    const int64_t bound = (T + C - 1) / C + N;
-    const int64_t wch = bound < WINDOW_CHUNKS ? bound : WINDOW_CHUNKS;
-    const size_t images = (size_t)ws_images_offset(N) + (size_t)wch * (size_t)H * CH_STRIDE;
-    const int64_t gmax = H > 0 ? (128 / H + 4) / 8 : 0;
-    const size_t maps = gmax >= 4 ? (size_t)H * gmax * 3 * (D * D * sizeof(float)) : 0;
-    return ((images + 255) & ~(size_t)255) + maps;
-}
-
 size_t prefill_tc_workspace_bytes(int32_t N, int64_t T, int32_t H) {
     const int64_t bound = (T + C - 1) / C + N;
     const int64_t wch = bound < WINDOW_CHUNKS ? bound : WINDOW_CHUNKS;

@@ -64,7 +64,7 @@ def _ragged(dtype, d, H, seed):
 
 
 def test_host_equals_device_single_sequence_workload():
-    """T = 8192, H = 32, d = 128, bf16: 16 pieces of 512 tokens."""
+    """T = 8192, H = 32, d = 128, bf16: 8 pieces of 1,024 tokens."""
     inp = ki.prefill_inputs("single", device=DEV)
     o_d, S_d = _device_call(inp)
     o_h, S_h = _host_call(inp)
