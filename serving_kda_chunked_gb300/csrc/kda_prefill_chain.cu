@@ -21,6 +21,69 @@ namespace tcp {
 // few MMAs on the state's critical path are spread over several issuing warps.
 // TMEM accumulators alternate between two sets so that the outputs of chunk
 // i are read while the MMAs of chunk i + 1 run.
+// ------------------------------------------------------------------------------
+// window plan (batches of many sequences): the sequences with chunks in the
+// window [w0, w1) -- and, in the first window, the empty ones, whose initial
+// state passes through -- ordered by their chain length in the window, longest
+// first (a counting sort over the length, at most WINDOW_CHUNKS).  A chain
+// CTA runs for a time proportional to its length, so starting the longest
+// first shortens the tail of the launch (longest-processing-time-first list
+// scheduling); the chain form follows from the number of chain slices listed.
+// ------------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024)
+window_plan_kernel(const int32_t *__restrict__ chunk_base, int N, int w0, int w1, int H,
+                   int slice_cap, int32_t *plan) {
+    constexpr int NB = WINDOW_CHUNKS + 1;   // bin WINDOW_CHUNKS - length, length 0 .. WINDOW_CHUNKS
+    __shared__ int32_t start[NB];
+    __shared__ int32_t warp_tot[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < NB; i += 1024) start[i] = 0;
+    __syncthreads();
+    for (int n = tid; n < N; n += 1024) {
+        const int cb = chunk_base[n], ce = chunk_base[n + 1];
+        const int len = min(max(0, min(ce, w1) - max(cb, w0)), WINDOW_CHUNKS);
+        if (len > 0 || (w0 == 0 && cb == ce)) atomicAdd(&start[WINDOW_CHUNKS - len], 1);
+    }
+    __syncthreads();
+    // exclusive scan of the bins: thread t owns bins 2t and 2t + 1, thread 1023
+    // also the last bin
+    const int b0 = 2 * tid;
+    const int c0 = start[b0], c1 = start[b0 + 1], c2 = tid == 1023 ? start[NB - 1] : 0;
+    int x = c0 + c1 + c2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int t = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        warp_tot[lane] = t;
+    }
+    __syncthreads();
+    const int excl = x - (c0 + c1 + c2) + (warp > 0 ? warp_tot[warp - 1] : 0);
+    start[b0] = excl;
+    start[b0 + 1] = excl + c0;
+    if (tid == 1023) {
+        start[NB - 1] = excl + c0 + c1;
+        const int total = excl + c0 + c1 + c2;
+        plan[1] = total;
+        plan[0] = (int64_t)total * H * NSLICE > slice_cap ? PLAN_WIDE : PLAN_SLICE;
+    }
+    __syncthreads();
+    for (int n = tid; n < N; n += 1024) {
+        const int cb = chunk_base[n], ce = chunk_base[n + 1];
+        const int len = min(max(0, min(ce, w1) - max(cb, w0)), WINDOW_CHUNKS);
+        if (len > 0 || (w0 == 0 && cb == ce)) plan[2 + atomicAdd(&start[WINDOW_CHUNKS - len], 1)] = n;
+    }
+}
+
 __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -34,6 +97,10 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     int slice = unit % NSLICE;
     int h = (unit / NSLICE) % H;
     int n = unit / (NSLICE * H);
+    if (p.plan) {   // many sequences: the window plan's order, if it picked this form
+        if (p.plan[0] != PLAN_SLICE || unit >= p.plan[1] * H * NSLICE) return;
+        n = p.plan[2 + unit / (NSLICE * H)];
+    }
     int32_t *ws_hdr = reinterpret_cast<int32_t *>(p.ws);
     const int32_t *chunk_base = reinterpret_cast<const int32_t *>(p.ws + WS_HEADER);
     const uint8_t *img_base = p.ws + ws_images_offset(p.N);
@@ -397,7 +464,11 @@ __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Para
     const int col0 = 32 * wg;                  // first state column of this thread
     const int H = p.H;
     const int h = blockIdx.x % H;
-    const int n = blockIdx.x / H;
+    int n = blockIdx.x / H;
+    if (p.plan) {   // many sequences: the window plan's order, if it picked this form
+        if (p.plan[0] != PLAN_WIDE || (int)blockIdx.x >= p.plan[1] * H) return;
+        n = p.plan[2 + blockIdx.x / H];
+    }
     int32_t *ws_hdr = reinterpret_cast<int32_t *>(p.ws);
     const int32_t *chunk_base = reinterpret_cast<const int32_t *>(p.ws + WS_HEADER);
     const uint8_t *img_base = p.ws + ws_images_offset(p.N);

@@ -35,15 +35,35 @@ bool token_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, uint32_
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sm_count() {
-    static int cached = 0;
-    if (!cached) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&cached, cudaDevAttrMultiProcessorCount, dev);
-        if (cached <= 0) cached = 1;
+// Per-device setup, once per device: the kernels' shared-memory limits (a
+// function attribute of the device's context) and the SM count.
+cudaError_t device_setup(int *nsm) {
+    static std::mutex mu;
+    static int sms[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!sms[dev]) {
+        e = cudaFuncSetAttribute(intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)S1_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)S2_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(chain_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)S2W_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(segment_combine_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)COMB_BYTES);
+        int n = 0;
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        sms[dev] = n > 0 ? n : 1;
     }
-    return cached;
+    *nsm = sms[dev];
+    return cudaSuccess;
 }
 
 }  // namespace tcp
@@ -99,21 +119,9 @@ namespace {
 // segment maps of the chunk-affine scan behind them.
 cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, bool scan,
                            cudaStream_t st) {
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)S1_BYTES);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S2_BYTES);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(chain_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)S2W_BYTES);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(segment_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)COMB_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    int nsm = 1;
+    cudaError_t e = device_setup(&nsm);
+    if (e != cudaSuccess) return e;
     float *smaps = nullptr;
     if (scan) {
         const size_t images = (size_t)ws_images_offset(a.N) + (size_t)window * (size_t)a.H * CH_STRIDE;
@@ -121,11 +129,10 @@ cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, bo
     }
     int32_t *hdr = reinterpret_cast<int32_t *>(ws);
     const int64_t bound = (a.T + C - 1) / C + a.N;
-    chunk_table_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.N, a.T, (int)bound, hdr,
-                                          reinterpret_cast<int32_t *>(ws + WS_HEADER));
-    cudaError_t e = cudaGetLastError();
+    int32_t *chunk_base = reinterpret_cast<int32_t *>(ws + WS_HEADER);
+    chunk_table_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.N, a.T, (int)bound, hdr, chunk_base);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int nsm = sm_count();
     K1Params p1;
     if (a.T > 0) {
         if (!token_map(&p1.tm_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.H, a.T) ||
@@ -151,7 +158,7 @@ cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, bo
         K2Params p2;
         p2.S0 = a.S0; p2.S_T = a.S_T; p2.o = (__nv_bfloat16 *)a.o; p2.cu = a.cu_seqlens;
         p2.ws = ws; p2.N = a.N; p2.H = a.H; p2.T = a.T; p2.w0 = (int)w0; p2.w1 = (int)w1;
-        p2.nseg = 0; p2.seg_len = 0; p2.phase = 0; p2.smaps = smaps;
+        p2.nseg = 0; p2.seg_len = 0; p2.phase = 0; p2.smaps = smaps; p2.plan = nullptr;
         const int64_t wch = (bound - w0) < window ? (bound - w0) : window;
         const SegPlan pl = smaps ? segment_plan(a.N, a.H, wch) : SegPlan{0, 0};
         if (pl.nseg) {            // chunk-affine scan over this window
@@ -168,12 +175,22 @@ cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, bo
         // A chain is latency-bound: one (sequence, head, 32-column slice) per
         // SM finishes soonest when all slices run at once; with more than two
         // waves of slices, one CTA per (sequence, head) carrying all four
-        // slices gets through about twice the chains per SM.
+        // slices gets through about twice the chains per SM.  With that many
+        // sequences, which of them have chunks in this window is known on the
+        // device only: a one-block kernel lists them (longest chain first) and
+        // picks the form, both forms are launched, and the CTAs of the form
+        // not picked return at once.
         const int64_t slices = (int64_t)a.N * a.H * NSLICE;
-        if (slices > 2 * (int64_t)nsm)
+        if (slices > 2 * (int64_t)nsm) {
+            int32_t *plan = reinterpret_cast<int32_t *>(ws + ws_plan_offset(a.N));
+            window_plan_kernel<<<1, 1024, 0, st>>>(chunk_base, a.N, (int)w0, (int)w1, a.H,
+                                                   2 * nsm, plan);
+            p2.plan = plan;
             chain_wide_kernel<<<(unsigned)((int64_t)a.N * a.H), K2W_THREADS, S2W_BYTES, st>>>(p2);
-        else
+            chain_kernel<<<(unsigned)(2 * nsm), K2_THREADS, S2_BYTES, st>>>(p2);
+        } else {
             chain_kernel<<<(unsigned)slices, K2_THREADS, S2_BYTES, st>>>(p2);
+        }
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -60,7 +60,7 @@ constexpr int D = 128;         // dk = dv
 constexpr int DVS = 32;        // state columns per chain CTA
 constexpr int NSLICE = D / DVS;
 
-// workspace: header | chunk table | per (chunk, head) operand images
+// workspace: header | chunk table | chain plan | per (chunk, head) operand images
 constexpr uint32_t WS_HEADER = 256;
 constexpr uint32_t IMG_W = 0;          // W   [64 x 128] fp16, K-major SW128 (2 atoms)
 constexpr uint32_t IMG_Q = 16384;      // Q^  [64 x 128] fp16, K-major SW128 (2 atoms)
@@ -71,8 +71,15 @@ constexpr uint32_t IMG_G = 73728;      // e^gamma_last [128] fp32
 constexpr uint32_t CH_STRIDE = 74240;  // bytes per (chunk, head)
 constexpr int WINDOW_CHUNKS = 2048;    // chunks per K1/K2 window
 
+// Chain plan of a window (batches of many sequences): [0] the chain form
+// (PLAN_SLICE or PLAN_WIDE), [1] the number of sequences listed, [2 ..] those
+// sequences, longest chain in the window first.
+constexpr int PLAN_SLICE = 0, PLAN_WIDE = 1;
+__host__ __device__ inline uint64_t ws_plan_offset(int N) {
+    return WS_HEADER + 4ull * (uint64_t)(N + 1);
+}
 __host__ __device__ inline uint64_t ws_images_offset(int N) {
-    uint64_t off = WS_HEADER + 4ull * (uint64_t)(N + 1);
+    uint64_t off = ws_plan_offset(N) + 4ull * (uint64_t)(N + 2);
     return (off + 1023) & ~1023ull;
 }
 
@@ -157,6 +164,10 @@ struct K2Params {
     int seg_len;       // chunks per segment
     int phase;         // 0: segment maps (and segment 0 itself), 1: segments 1..nseg-1
     float *smaps;      // [H][nseg][3][128][128] fp32: M_s, B_s, start state of segment s
+    // window plan (many sequences): CTAs take sequences in the plan's order
+    // and return at once unless the plan picked their chain form; nullptr:
+    // sequence = block index order
+    const int32_t *plan;
 };
 
 // Roles of a chain CTA in a segment launch.
@@ -190,6 +201,9 @@ constexpr uint32_t S2W_TX = 4 * 8192 + 16384 + 8192 + 16384 + 512;   // bytes la
 __global__ void __launch_bounds__(1024)
 chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int cap,
                    int32_t *ws_hdr, int32_t *chunk_base);
+__global__ void __launch_bounds__(1024)
+window_plan_kernel(const int32_t *__restrict__ chunk_base, int N, int w0, int w1, int H,
+                   int slice_cap, int32_t *plan);
 __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_constant__ K1Params p);
 __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p);
 __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Params p);
