@@ -135,8 +135,8 @@ kda_status kda_prefill_check(const void *workspace, void *stream);
  * (64 MiB) inside the library, held by every GPU that loads the library
  * until the process exits.  Long inputs are processed in as many windows of
  * chunks as that array needs; the call is rejected with KDA_ERR_TOO_LARGE
- * only when not even one chunk of all H heads (74,240 bytes each) plus the
- * N + 1 sequence offsets fits.
+ * only when not even one chunk of all H heads (74,240 bytes each) plus a
+ * header of 8 N + 268 bytes (the chunk table and the chain plan) fits.
  *
  * - The first call on a device looks up the array's device address with
  *   cudaGetSymbolAddress while that device is current; make that first call
