@@ -252,13 +252,13 @@ def bench_prefill(args, world, kda, ki, torch, workload="single", heads=None, to
     n_copies = max(2, math.ceil(2 * L2_BYTES / in_bytes) + 1)
     sets = [inp] + [{n: inp[n].clone() for n in names} for _ in range(n_copies - 1)]
     cu = inp["cu_seqlens"]
-    T, Hn, N = inp["q"].shape[0], inp["q"].shape[1], cu.shape[0] - 1
-    o = torch.empty((T, Hn, D), dtype=torch.bfloat16, device=dev)
-    S_T = torch.empty((N, Hn, D, D), dtype=torch.float32, device=dev)
+    T, Hn, d, N = inp["q"].shape[0], inp["q"].shape[1], inp["q"].shape[2], cu.shape[0] - 1
+    o = torch.empty((T, Hn, d), dtype=inp["q"].dtype, device=dev)
+    S_T = torch.empty((N, Hn, d, d), dtype=torch.float32, device=dev)
     ws = None
     if api == "workspace":
-        ws = torch.empty(kda.kda_prefill_workspace_size(N, T, Hn, D, D, torch.bfloat16),
-                         dtype=torch.uint8, device=dev)
+        need = kda.kda_prefill_workspace_size(N, T, Hn, d, d, inp["q"].dtype)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
 
     def step(i):
         s = sets[i % n_copies]
@@ -561,7 +561,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("single", "varlen", "long"), default="single",
+    ap.add_argument("--workload", choices=("single", "varlen", "long", "tiny"), default="single",
                     help="prefill workload of --part prefill (the benchmark line always uses "
                          "the single-sequence workload)")
     ap.add_argument("--heads", type=int, default=None,

@@ -17,10 +17,14 @@
 //   O      = (Q * exp(gamma)) S + P U
 //   S_next = Diag(exp(gamma_last)) S + (K * exp(gamma_last - gamma))^T U
 //
-// Every exponent above is <= 0 (pairs with i <= r only), so nothing can
-// overflow.  Columns of S are independent, so one CTA owns one (sequence,
-// head, block of DVS state columns) and walks the sequence's chunks in order
-// with its state slice in shared memory.
+// While no channel decays below e^-80 over the chunk, the pair factor is
+// split as exp(gamma_rc) * exp(-gamma_ic), both inside fp32, and A and P are
+// plain products of the scaled rows (2 exponentials per element instead of
+// one per pair and channel).  Otherwise each pair's exponent is formed first;
+// it is <= 0 (pairs with i <= r only), so nothing can overflow.  Columns of S
+// are independent, so one CTA owns one (sequence, head, block of DVS state
+// columns) and walks the sequence's chunks in order with its state slice in
+// shared memory.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -28,13 +32,14 @@ namespace {
 
 constexpr int C = 64;      // tokens per chunk
 constexpr int NT = 256;    // threads per CTA
+constexpr float RANGE_LIMIT = 80.f;   // e^80 stays inside fp32
 
 template <int DK, int DVS>
 struct SimtSmem {
     static constexpr int KP = DK + 1;  // padded row stride of [C][DK] tiles
     static constexpr int CP = C + 1;   // padded row stride of [C][C] tiles
     static constexpr size_t floats =
-        3 * (size_t)C * KP + 2 * (size_t)C * CP + (size_t)DK * DVS +
+        4 * (size_t)C * KP + 2 * (size_t)C * CP + (size_t)DK * DVS +
         (size_t)C * DVS + C + 2 * DK;
     static constexpr size_t bytes = floats * sizeof(float);
 };
@@ -53,7 +58,8 @@ prefill_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     float *sK = smem;              // [C][KP]  k, then k * exp(gamma)
     float *sQ = sK + C * KP;       // [C][KP]  q, then q * exp(gamma)
     float *sG = sQ + C * KP;       // [C][KP]  g, then gamma, then kbar
-    float *sA = sG + C * KP;       // [C][CP]  A
+    float *sKn = sG + C * KP;      // [C][KP]  k * exp(-gamma) (single-reference chunks)
+    float *sA = sKn + C * KP;      // [C][CP]  A
     float *sP = sA + C * CP;       // [C][CP]  P
     float *sS = sP + C * CP;       // [DK][DVS] state slice
     float *sV = sS + DK * DVS;     // [C][DVS] v, then rhs, then U
@@ -112,34 +118,65 @@ prefill_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         }
         __syncthreads();
 
-        // ---- gated K K^T (strictly lower, times beta_r) and Q K^T (lower)
-        for (int pidx = tid; pidx < C * C; pidx += NT) {
-            const int r = pidx / C, i = pidx % C;
-            float a = 0.f, p = 0.f;
-            if (i <= r) {
-                const float *gr = sG + r * KP, *gi = sG + i * KP;
-                const float *kr = sK + r * KP, *ki = sK + i * KP, *qr = sQ + r * KP;
-#pragma unroll 4
-                for (int c = 0; c < DK; ++c) {
-                    const float kie = ki[c] * expf(gr[c] - gi[c]);
-                    a += kr[c] * kie;
-                    p += qr[c] * kie;
-                }
+        const bool single_ref = __syncthreads_and(tid >= DK || sGL[tid] >= -RANGE_LIMIT);
+        if (single_ref) {
+            // ---- K*exp(gamma), Q*exp(gamma), K*exp(-gamma) and
+            // kbar = K*exp(-gamma)*exp(gamma_last)
+            for (int idx = tid; idx < C * DK; idx += NT) {
+                const int r = idx / DK, c = idx % DK;
+                const float gam = sG[r * KP + c];
+                const float kk = sK[r * KP + c];
+                const float kn = kk * expf(-gam);
+                const float e = expf(gam);
+                sKn[r * KP + c] = kn;
+                sG[r * KP + c] = kn * sEL[c];
+                sK[r * KP + c] = kk * e;
+                sQ[r * KP + c] *= e;
             }
-            sA[r * CP + i] = i < r ? sB[r] * a : 0.f;
-            sP[r * CP + i] = p;
-        }
-        __syncthreads();
-
-        // ---- K*exp(gamma), Q*exp(gamma), kbar = K*exp(gamma_last - gamma)
-        for (int idx = tid; idx < C * DK; idx += NT) {
-            const int r = idx / DK, c = idx % DK;
-            const float gam = sG[r * KP + c];
-            const float e = expf(gam);
-            const float kk = sK[r * KP + c];
-            sG[r * KP + c] = kk * expf(sGL[c] - gam);
-            sK[r * KP + c] = kk * e;
-            sQ[r * KP + c] *= e;
+            __syncthreads();
+            // ---- gated K K^T (strictly lower, times beta_r) and Q K^T (lower)
+            for (int pidx = tid; pidx < C * C; pidx += NT) {
+                const int r = pidx / C, i = pidx % C;
+                float a = 0.f, p = 0.f;
+                if (i <= r) {
+                    const float *kr = sK + r * KP, *qr = sQ + r * KP, *ki = sKn + i * KP;
+#pragma unroll 8
+                    for (int c = 0; c < DK; ++c) {
+                        a += kr[c] * ki[c];
+                        p += qr[c] * ki[c];
+                    }
+                }
+                sA[r * CP + i] = i < r ? sB[r] * a : 0.f;
+                sP[r * CP + i] = p;
+            }
+        } else {
+            // ---- the same with each pair's exponent formed first
+            for (int pidx = tid; pidx < C * C; pidx += NT) {
+                const int r = pidx / C, i = pidx % C;
+                float a = 0.f, p = 0.f;
+                if (i <= r) {
+                    const float *gr = sG + r * KP, *gi = sG + i * KP;
+                    const float *kr = sK + r * KP, *ki = sK + i * KP, *qr = sQ + r * KP;
+#pragma unroll 4
+                    for (int c = 0; c < DK; ++c) {
+                        const float kie = ki[c] * expf(gr[c] - gi[c]);
+                        a += kr[c] * kie;
+                        p += qr[c] * kie;
+                    }
+                }
+                sA[r * CP + i] = i < r ? sB[r] * a : 0.f;
+                sP[r * CP + i] = p;
+            }
+            __syncthreads();
+            for (int idx = tid; idx < C * DK; idx += NT) {
+                const int r = idx / DK, c = idx % DK;
+                const float gam = sG[r * KP + c];
+                const float e = expf(gam);
+                const float kk = sK[r * KP + c];
+                sG[r * KP + c] = kk * expf(sGL[c] - gam);
+                sK[r * KP + c] = kk * e;
+                sQ[r * KP + c] *= e;
+            }
         }
         __syncthreads();
 
@@ -154,19 +191,31 @@ prefill_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         }
         __syncthreads();
 
-        // ---- forward substitution (I + A) U = rhs, one column per warp pass
+        // ---- forward substitution (I + A) U = rhs; warp w solves columns
+        // w, w + 8, ... together (independent chains, one load of A per row)
         {
+            constexpr int NW = NT / 32, CPW = DVS / NW;
+            static_assert(DVS % NW == 0, "columns per warp");
             const int warp = tid / 32, lane = tid % 32;
-            for (int j = warp; j < DVS; j += NT / 32) {
-                float x0 = sV[lane * DVS + j];
-                float x1 = sV[(lane + 32) * DVS + j];
-                for (int r = 0; r < C; ++r) {
-                    const float ur = __shfl_sync(0xffffffffu, r < 32 ? x0 : x1, r & 31);
-                    if (lane > r) x0 -= sA[lane * CP + r] * ur;
-                    if (lane + 32 > r) x1 -= sA[(lane + 32) * CP + r] * ur;
+            float x0[CPW], x1[CPW];
+#pragma unroll
+            for (int m = 0; m < CPW; ++m) {
+                x0[m] = sV[lane * DVS + warp + NW * m];
+                x1[m] = sV[(lane + 32) * DVS + warp + NW * m];
+            }
+            for (int r = 0; r < C; ++r) {
+                const float a0 = sA[lane * CP + r], a1 = sA[(lane + 32) * CP + r];
+#pragma unroll
+                for (int m = 0; m < CPW; ++m) {
+                    const float ur = __shfl_sync(0xffffffffu, r < 32 ? x0[m] : x1[m], r & 31);
+                    if (lane > r) x0[m] -= a0 * ur;
+                    if (lane + 32 > r) x1[m] -= a1 * ur;
                 }
-                sV[lane * DVS + j] = x0;
-                sV[(lane + 32) * DVS + j] = x1;
+            }
+#pragma unroll
+            for (int m = 0; m < CPW; ++m) {
+                sV[lane * DVS + warp + NW * m] = x0[m];
+                sV[(lane + 32) * DVS + warp + NW * m] = x1[m];
             }
         }
         __syncthreads();
