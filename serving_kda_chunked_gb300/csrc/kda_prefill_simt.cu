@@ -134,20 +134,39 @@ prefill_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                 sQ[r * KP + c] *= e;
             }
             __syncthreads();
-            // ---- gated K K^T (strictly lower, times beta_r) and Q K^T (lower)
-            for (int pidx = tid; pidx < C * C; pidx += NT) {
-                const int r = pidx / C, i = pidx % C;
-                float a = 0.f, p = 0.f;
-                if (i <= r) {
-                    const float *kr = sK + r * KP, *qr = sQ + r * KP, *ki = sKn + i * KP;
-#pragma unroll 8
-                    for (int c = 0; c < DK; ++c) {
-                        a += kr[c] * ki[c];
-                        p += qr[c] * ki[c];
+            // ---- gated K K^T (strictly lower, times beta_r) and Q K^T (lower):
+            // thread t owns rows 4 (t / 16) + u and columns t % 16 + 16 w
+            // (u, w < 4), so that a warp's column loads hit 16 distinct banks
+            static_assert(NT == 256 && C == 64, "one 4 x 4 tile of the 64 x 64 products per thread");
+            {
+                const int r0 = 4 * (tid >> 4), i0 = tid & 15;
+                float a[4][4] = {}, pq[4][4] = {};
+                const float *kr = sK + r0 * KP, *qr = sQ + r0 * KP, *ki = sKn + i0 * KP;
+#pragma unroll 4
+                for (int c = 0; c < DK; ++c) {
+                    float x[4], y[4], z[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        x[u] = kr[u * KP + c];
+                        y[u] = qr[u * KP + c];
+                        z[u] = ki[16 * u * KP + c];
                     }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            a[u][w] = fmaf(x[u], z[w], a[u][w]);
+                            pq[u][w] = fmaf(y[u], z[w], pq[u][w]);
+                        }
                 }
-                sA[r * CP + i] = i < r ? sB[r] * a : 0.f;
-                sP[r * CP + i] = p;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int r = r0 + u, i = i0 + 16 * w;
+                        sA[r * CP + i] = i < r ? sB[r] * a[u][w] : 0.f;
+                        sP[r * CP + i] = i <= r ? pq[u][w] : 0.f;
+                    }
             }
         } else {
             // ---- the same with each pair's exponent formed first
@@ -180,14 +199,31 @@ prefill_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         }
         __syncthreads();
 
+        // [C][DVS] results below: thread t owns rows r2, r2 + 1 and columns
+        // j4 .. j4 + 3 (state rows are read as float4)
+        static_assert(C * DVS == 8 * NT, "two rows x four columns per thread");
+        const int j4 = 4 * (tid % (DVS / 4)), r2 = 2 * (tid / (DVS / 4));
+
         // ---- right-hand side: beta (V - (K*exp(gamma)) S)
-        for (int idx = tid; idx < C * DVS; idx += NT) {
-            const int r = idx / DVS, j = idx % DVS;
-            float acc = 0.f;
-            const float *kr = sK + r * KP;
-#pragma unroll 8
-            for (int c = 0; c < DK; ++c) acc += kr[c] * sS[c * DVS + j];
-            sV[idx] = sB[r] * (sV[idx] - acc);
+        {
+            float acc[2][4] = {};
+            const float *k0 = sK + r2 * KP;
+#pragma unroll 4
+            for (int c = 0; c < DK; ++c) {
+                const float4 s4 = *reinterpret_cast<const float4 *>(sS + c * DVS + j4);
+                const float x0 = k0[c], x1 = k0[KP + c];
+                acc[0][0] = fmaf(x0, s4.x, acc[0][0]); acc[0][1] = fmaf(x0, s4.y, acc[0][1]);
+                acc[0][2] = fmaf(x0, s4.z, acc[0][2]); acc[0][3] = fmaf(x0, s4.w, acc[0][3]);
+                acc[1][0] = fmaf(x1, s4.x, acc[1][0]); acc[1][1] = fmaf(x1, s4.y, acc[1][1]);
+                acc[1][2] = fmaf(x1, s4.z, acc[1][2]); acc[1][3] = fmaf(x1, s4.w, acc[1][3]);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                float *vr = sV + (r2 + u) * DVS + j4;
+                const float b = sB[r2 + u];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) vr[w] = b * (vr[w] - acc[u][w]);
+            }
         }
         __syncthreads();
 
@@ -220,27 +256,61 @@ prefill_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         }
         __syncthreads();
 
-        // ---- outputs O = (Q*exp(gamma)) S + P U
-        for (int idx = tid; idx < C * DVS; idx += NT) {
-            const int r = idx / DVS, j = idx % DVS;
-            if (r >= L) continue;
-            float acc = 0.f;
-            const float *qr = sQ + r * KP;
-#pragma unroll 8
-            for (int c = 0; c < DK; ++c) acc += qr[c] * sS[c * DVS + j];
-            const float *pr = sP + r * CP;
-            for (int i = 0; i <= r; ++i) acc += pr[i] * sV[i * DVS + j];
-            o[((c0 + r) * H + h) * DV + col0 + j] = from_f32<Tin>(acc);
+        // ---- outputs O = (Q*exp(gamma)) S + P U (P is zero above the diagonal)
+        {
+            float acc[2][4] = {};
+            const float *q0 = sQ + r2 * KP;
+#pragma unroll 4
+            for (int c = 0; c < DK; ++c) {
+                const float4 s4 = *reinterpret_cast<const float4 *>(sS + c * DVS + j4);
+                const float x0 = q0[c], x1 = q0[KP + c];
+                acc[0][0] = fmaf(x0, s4.x, acc[0][0]); acc[0][1] = fmaf(x0, s4.y, acc[0][1]);
+                acc[0][2] = fmaf(x0, s4.z, acc[0][2]); acc[0][3] = fmaf(x0, s4.w, acc[0][3]);
+                acc[1][0] = fmaf(x1, s4.x, acc[1][0]); acc[1][1] = fmaf(x1, s4.y, acc[1][1]);
+                acc[1][2] = fmaf(x1, s4.z, acc[1][2]); acc[1][3] = fmaf(x1, s4.w, acc[1][3]);
+            }
+            const float *p0 = sP + r2 * CP;
+            for (int i = 0; i <= r2 + 1; ++i) {
+                const float4 u4 = *reinterpret_cast<const float4 *>(sV + i * DVS + j4);
+                const float x0 = p0[i], x1 = p0[CP + i];
+                acc[0][0] = fmaf(x0, u4.x, acc[0][0]); acc[0][1] = fmaf(x0, u4.y, acc[0][1]);
+                acc[0][2] = fmaf(x0, u4.z, acc[0][2]); acc[0][3] = fmaf(x0, u4.w, acc[0][3]);
+                acc[1][0] = fmaf(x1, u4.x, acc[1][0]); acc[1][1] = fmaf(x1, u4.y, acc[1][1]);
+                acc[1][2] = fmaf(x1, u4.z, acc[1][2]); acc[1][3] = fmaf(x1, u4.w, acc[1][3]);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (r2 + u < L)
+                    store4(o + ((c0 + r2 + u) * H + h) * DV + col0 + j4,
+                           make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]));
         }
         __syncthreads();
 
-        // ---- state carry S = Diag(exp(gamma_last)) S + kbar^T U
-        for (int idx = tid; idx < DK * DVS; idx += NT) {
-            const int c = idx / DVS, j = idx % DVS;
-            float acc = sEL[c] * sS[idx];
-#pragma unroll 8
-            for (int r = 0; r < C; ++r) acc += sG[r * KP + c] * sV[r * DVS + j];
-            sS[idx] = acc;
+        // ---- state carry S = Diag(exp(gamma_last)) S + kbar^T U: thread t
+        // owns state rows c2, c2 + 1 (+ 64 per pass) and columns j4 .. j4 + 3
+#pragma unroll
+        for (int pass = 0; pass < DK / 64; ++pass) {
+            const int c2 = 64 * pass + r2;
+            float acc[2][4];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const float4 s4 = *reinterpret_cast<const float4 *>(sS + (c2 + u) * DVS + j4);
+                const float e = sEL[c2 + u];
+                acc[u][0] = e * s4.x; acc[u][1] = e * s4.y; acc[u][2] = e * s4.z; acc[u][3] = e * s4.w;
+            }
+#pragma unroll 4
+            for (int r = 0; r < C; ++r) {
+                const float4 u4 = *reinterpret_cast<const float4 *>(sV + r * DVS + j4);
+                const float x0 = sG[r * KP + c2], x1 = sG[r * KP + c2 + 1];
+                acc[0][0] = fmaf(x0, u4.x, acc[0][0]); acc[0][1] = fmaf(x0, u4.y, acc[0][1]);
+                acc[0][2] = fmaf(x0, u4.z, acc[0][2]); acc[0][3] = fmaf(x0, u4.w, acc[0][3]);
+                acc[1][0] = fmaf(x1, u4.x, acc[1][0]); acc[1][1] = fmaf(x1, u4.y, acc[1][1]);
+                acc[1][2] = fmaf(x1, u4.z, acc[1][2]); acc[1][3] = fmaf(x1, u4.w, acc[1][3]);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)   // rows only this thread reads
+                *reinterpret_cast<float4 *>(sS + (c2 + u) * DVS + j4) =
+                    make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
         }
         __syncthreads();
     }
