@@ -422,6 +422,30 @@ def test_prefill_many_short_sequences():
     assert torch.equal(S_T[5], inp["S0"][5])
 
 
+def test_prefill_thousands_of_sequences():
+    """3,150 packed sequences (0-65 tokens, every chunk edge), H = 2: more
+    sequences than the 1,024 threads of the chunk-table and window-plan
+    kernels, and more chunks (3,150) than one window, so both kernels loop
+    and the second window plans only the sequences left.  The host-buffer
+    call (pieces of ~8,800 tokens over hundreds of sequences each) is checked
+    against the oracle too."""
+    lengths = [0, 1, 5, 17, 64, 65, 3] * 450
+    cfg = ki.PrefillConfig("thousands", H=2, d=128, dtype="bf16", n_seqs=len(lengths),
+                           s0_std=0.2)
+    inp = ki.prefill_inputs(cfg, device=DEV, seed=33, lengths=lengths)
+    o, S_T = _run_prefill(inp)
+    o_ref, S_ref = _oracle_prefill(inp)
+    assert_close("o", o, o_ref, 2e-3)
+    assert_close("S_T", S_T, S_ref, 2e-3)
+    empty = [n for n, L in enumerate(lengths) if L == 0]
+    assert torch.equal(S_T[empty], inp["S0"][empty])
+    host = [inp[n].cpu() for n in ("q", "k", "v", "g", "beta")]
+    o_h, S_h = kda.kda_prefill_chunked_host(*host, inp["cu_seqlens"].cpu(), inp["S0"].cpu())
+    torch.cuda.synchronize()
+    assert_close("o (host buffers)", o_h, o_ref, 2e-3)
+    assert_close("S_T (host buffers)", S_h, S_ref, 2e-3)
+
+
 @pytest.mark.parametrize("case", ["beta0", "gate0"])
 def test_prefill_degenerate_gates(case):
     """beta = 0: nothing is written, the state only decays (o_t = S_t^T q_t with
