@@ -176,9 +176,10 @@ uint64_t kda_noalloc_scratch_bytes(void);
  *   workspace  DEVICE scratch of at least kda_prefill_host_workspace_size(...)
  *              bytes, 16-byte aligned; calls sharing it must not overlap
  *
- * The token range is cut into about 8 pieces (at least 512 and at most
- * 16,384 tokens each, every cut on a 64-token chunk boundary of the sequence
- * it falls in).  Each piece is copied into one of two device staging slots,
+ * The token range is cut into pieces of about T_total / 6 tokens (at least
+ * 512, at most 16,384) that halve toward the end of the call (down to 256
+ * tokens), every cut on a 64-token chunk boundary of the sequence it falls
+ * in.  Each piece is copied into one of two device staging slots,
  * runs as a packed prefill over the sequences it overlaps (their states
  * carried in a device state buffer in the workspace, exactly as the state
  * crosses windows inside one kda_prefill_chunked call), and its outputs are

@@ -41,14 +41,16 @@ size_t prefill_tc_piece_workspace_bytes(int32_t N, int64_t T, int32_t H) {
 
 // Each host->device copy carries a fixed cost of ~3 us on top of the link
 // time (211 GB/s measured from pinned memory), and the last piece's kernels
-// and output copy are not overlapped: 8 pieces of a call of 8 K tokens
-// measured 1.93 ms per call, 16 pieces 1.99 ms, 4 pieces 1.94 ms (the copies
-// alone, as one piece, take 1.70 ms).  Alternating the pieces over two copy
-// streams measured slower (2.06 ms for 16 pieces).
-constexpr int64_t PIECES = 8;         // pieces per call (before the limits below)
+// and output copy are not overlapped.  A call of 8 K tokens measured, per
+// call: equal pieces, 16: 1.99 ms, 8: 1.93 ms, 4: 1.94 ms; with the pieces
+// halving toward the end (down to 256 tokens), 12: 1.95 ms, 8: 1.91 ms,
+// 6: 1.89 ms.  The copies alone, as one piece, take 1.70 ms.  Alternating
+// the pieces over two copy streams measured slower (2.06 ms for 16 pieces).
+constexpr int64_t PIECES = 6;         // full-size pieces per call (before the limits below)
 constexpr int64_t PIECE_MIN = 512;    // tokens: keeps every SM busy in the per-chunk kernel
 constexpr int64_t PIECE_MAX = 16384;  // tokens: bounds the staging buffers
 constexpr int64_t CHUNK = 64;
+constexpr int64_t TAIL_MIN = 256;     // tokens: the smallest piece at the end of a call
 
 inline uint64_t align256(uint64_t x) { return (x + 255) & ~(uint64_t)255; }
 
@@ -104,14 +106,22 @@ struct Piece {
     int32_t n0, n;  // sequences n0 .. n0 + n - 1 overlap it
 };
 
-// Cut [0, T) into pieces of at most `cap` tokens, each boundary on a chunk
-// boundary of the sequence it falls in.  `cu` is validated (cu[0] = 0,
+// Cut [0, T) into pieces of at most `cap` tokens (at least TAIL_MIN, or what
+// is left), each boundary on a chunk boundary of the sequence it falls in.  `cu` is validated (cu[0] = 0,
 // non-decreasing, cu[N] = T).
 std::vector<Piece> plan_pieces(const int32_t *cu, int32_t N, int64_t T, int64_t cap) {
     std::vector<Piece> out;
     int32_t m = 0;   // sequence containing token a (or the first with cu[m+1] > a)
     for (int64_t a = 0; a < T;) {
-        int64_t b = a + cap;
+        // toward the end the pieces halve (down to TAIL_MIN tokens): the last
+        // piece's kernels and output copy are the part of the call that
+        // nothing overlaps
+        const int64_t rem = T - a;
+        int64_t len = (rem / 2 + CHUNK - 1) / CHUNK * CHUNK;
+        if (len < TAIL_MIN) len = TAIL_MIN;
+        if (rem - len < TAIL_MIN) len = rem;   // no piece smaller than TAIL_MIN after this one
+        if (len > cap) len = cap;
+        int64_t b = a + len;
         if (b >= T) {
             b = T;
         } else {
@@ -121,7 +131,7 @@ std::vector<Piece> plan_pieces(const int32_t *cu, int32_t N, int64_t T, int64_t 
             b = bos + (b - bos) / CHUNK * CHUNK;      // > a: see below
         }
         // b > a: if b stayed in a's sequence it moved down by less than 64 from
-        // a + cap >= a + 64 (a is on that sequence's chunk grid); otherwise it
+        // a + len >= a + 64 (a is on that sequence's chunk grid); otherwise it
         // is at least the start of a later sequence, which is > a.
         while ((int64_t)cu[m + 1] <= a) ++m;
         int32_t last = m;

@@ -64,7 +64,8 @@ def _ragged(dtype, d, H, seed):
 
 
 def test_host_equals_device_single_sequence_workload():
-    """T = 8192, H = 32, d = 128, bf16: 8 pieces of 1,024 tokens."""
+    """T = 8192, H = 32, d = 128, bf16: pieces of 1,408 tokens halving to 320
+    at the end (cuts on chunk boundaries)."""
     inp = ki.prefill_inputs("single", device=DEV)
     o_d, S_d = _device_call(inp)
     o_h, S_h = _host_call(inp)
