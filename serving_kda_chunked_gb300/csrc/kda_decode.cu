@@ -40,6 +40,13 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
               bool scalar_gate) {
     using Sh = DecodeShape<D, ROWS>;
     constexpr int LANES = Sh::LANES, GROUPS = Sh::GROUPS, NT = Sh::NT;
+    // Launched as a programmatic dependent: the CTAs may become resident while
+    // the previous kernel on the stream (typically the previous decode step,
+    // which writes these states) is still finishing; every global access
+    // comes after the wait for its completion.  Once every CTA of this step
+    // has started, the next step may be launched the same way.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
     const int lane = tid % LANES;
     const int grp = tid / LANES;
@@ -127,13 +134,26 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     }
 }
 
+// Consecutive decode steps are separate launches of ~160 us each (1 GiB of
+// state at B = 256, H = 32); launching each as a programmatic dependent of the
+// previous kernel hides the launch and CTA ramp-up (~2 us per step measured
+// between back-to-back launches) behind the previous step's last wave.
 template <int D, int ROWS, typename Tin, bool POOLED>
 cudaError_t launch(const DecodeArgs &a, cudaStream_t st) {
     const int64_t units = (int64_t)a.B * a.H;
-    decode_kernel<D, ROWS, Tin, POOLED><<<(unsigned)units, DecodeShape<D, ROWS>::NT, 0, st>>>(
-        (const Tin *)a.q, (const Tin *)a.k, (const Tin *)a.v, a.g, a.beta, a.S,
-        (Tin *)a.o, a.slots, a.H, a.P, a.scalar_gate);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)units);
+    cfg.blockDim = dim3(DecodeShape<D, ROWS>::NT);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_kernel<D, ROWS, Tin, POOLED>, (const Tin *)a.q,
+                              (const Tin *)a.k, (const Tin *)a.v, a.g, a.beta, a.S, (Tin *)a.o,
+                              a.slots, a.H, a.P, a.scalar_gate);
 }
 
 template <bool POOLED>
