@@ -40,7 +40,7 @@ struct SimtSmem {
     static constexpr int CP = C + 1;   // padded row stride of [C][C] tiles
     static constexpr size_t floats =
         4 * (size_t)C * KP + 2 * (size_t)C * CP + (size_t)DK * DVS +
-        (size_t)C * DVS + C + 2 * DK;
+        (size_t)C * DVS + C + 2 * DK + NT;
     static constexpr size_t bytes = floats * sizeof(float);
 };
 
@@ -66,6 +66,7 @@ prefill_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     float *sB = sV + C * DVS;      // [C] beta
     float *sGL = sB + C;           // [DK] gamma at the chunk's last row
     float *sEL = sGL + DK;         // [DK] exp(gamma_last)
+    float *sTot = sEL + DK;        // [NT / DK][DK] per-segment gate sums
 
     const int tid = threadIdx.x;
     const int unit = blockIdx.x;
@@ -85,18 +86,28 @@ prefill_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     for (int64_t c0 = bos; c0 < eos; c0 += C) {
         const int L = (int)((eos - c0) < C ? (eos - c0) : C);
         // ---- stage the chunk; rows past the sequence end are no-op tokens
-        for (int idx = tid; idx < C * DK; idx += NT) {
-            const int r = idx / DK, c = idx % DK;
-            float kv = 0.f, qv = 0.f, gv = 0.f;
-            if (r < L) {
-                const int64_t off = ((c0 + r) * H + h) * DK + c;
-                kv = to_f32(k[off]);
-                qv = to_f32(q[off]);
-                gv = scalar_gate ? g[(c0 + r) * H + h] : g[off];
+        // (four rows' loads in flight per thread before any is stored)
+        static_assert((C * DK) % (4 * NT) == 0, "staging in rounds of four");
+        for (int idx0 = tid; idx0 < C * DK; idx0 += 4 * NT) {
+            float kv[4], qv[4], gv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int idx = idx0 + u * NT, r = idx / DK, c = idx % DK;
+                kv[u] = qv[u] = gv[u] = 0.f;
+                if (r < L) {
+                    const int64_t off = ((c0 + r) * H + h) * DK + c;
+                    kv[u] = to_f32(k[off]);
+                    qv[u] = to_f32(q[off]);
+                    gv[u] = scalar_gate ? g[(c0 + r) * H + h] : g[off];
+                }
             }
-            sK[r * KP + c] = kv;
-            sQ[r * KP + c] = qv;
-            sG[r * KP + c] = gv;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int idx = idx0 + u * NT, r = idx / DK, c = idx % DK;
+                sK[r * KP + c] = kv[u];
+                sQ[r * KP + c] = qv[u];
+                sG[r * KP + c] = gv[u];
+            }
         }
         for (int idx = tid; idx < C * DVS; idx += NT) {
             const int r = idx / DVS, j = idx % DVS;
@@ -106,15 +117,30 @@ prefill_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             sB[r] = r < L ? beta[(c0 + r) * H + h] : 0.f;
         __syncthreads();
 
-        // ---- per-channel cumulative log-gate
-        if (tid < DK) {
+        // ---- per-channel cumulative log-gate: thread (channel c, row segment
+        // sg) scans its segment, then adds the totals of the segments before it
+        {
+            constexpr int NSEG = NT / DK, SEG = C / NSEG;
+            static_assert(NT % DK == 0 && C % NSEG == 0, "row segments");
+            const int c = tid % DK, sg = tid / DK;
             float acc = 0.f;
-            for (int r = 0; r < C; ++r) {
-                acc += sG[r * KP + tid];
-                sG[r * KP + tid] = acc;
+#pragma unroll 4
+            for (int r = sg * SEG; r < (sg + 1) * SEG; ++r) {
+                acc += sG[r * KP + c];
+                sG[r * KP + c] = acc;
             }
-            sGL[tid] = acc;
-            sEL[tid] = expf(acc);
+            sTot[sg * DK + c] = acc;
+            __syncthreads();
+            float off = 0.f;
+            for (int s2 = 0; s2 < sg; ++s2) off += sTot[s2 * DK + c];
+            if (sg > 0) {
+#pragma unroll 4
+                for (int r = sg * SEG; r < (sg + 1) * SEG; ++r) sG[r * KP + c] += off;
+            }
+            if (sg == NSEG - 1) {
+                sGL[c] = acc + off;
+                sEL[c] = expf(acc + off);
+            }
         }
         __syncthreads();
 
