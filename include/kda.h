@@ -194,7 +194,8 @@ uint64_t kda_noalloc_scratch_bytes(void);
  * threads are serialised while they enqueue.  kda_prefill_check(workspace,
  * stream) reports the device-side status of every piece.  Pointers that the
  * runtime identifies as device memory in place of a host buffer (or host
- * memory as the workspace) are rejected with KDA_ERR_INVALID_ARG.
+ * memory, or another device's memory, as the workspace) are rejected with
+ * KDA_ERR_INVALID_ARG.  The call runs on the current device.
  */
 kda_status kda_prefill_chunked_host(const void *q, const void *k, const void *v,
                                     const float *g, const float *beta,

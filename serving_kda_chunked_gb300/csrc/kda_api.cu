@@ -152,8 +152,12 @@ kda_status kda_prefill_chunked_host(const void *q, const void *k, const void *v,
     }
     {
         cudaPointerAttributes at;
-        if (cudaPointerGetAttributes(&at, workspace) == cudaSuccess) {
+        int dev = -1;
+        if (cudaPointerGetAttributes(&at, workspace) == cudaSuccess &&
+            cudaGetDevice(&dev) == cudaSuccess) {
             if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+                return KDA_ERR_INVALID_ARG;
+            if (at.type == cudaMemoryTypeDevice && at.device != dev)   // the call runs on the current device
                 return KDA_ERR_INVALID_ARG;
         } else {
             (void)cudaGetLastError();
