@@ -45,8 +45,14 @@ B_DEC, STEPS_DEC = 256, 1024
 PREFILL_BYTES_PER_TOKEN = 3 * H * D * 2 + H * D * 4 + H * 4 + H * D * 2
 STATE_BYTES = H * D * D * 4                      # one sequence's fp32 state
 # dense tensor-core work per token (all heads) at C = 64: per head-token
-# 10*C*d + 6*d^2 flops (gated QK^T and KK^T tiles, W, U~, W S, Q S, P U, K^T U)
-PREFILL_FLOPS_PER_TOKEN = H * (10 * 64 * D + 6 * D * D)
+# 10*C*d + 6*d^2 flops (gated QK^T and KK^T tiles, W, U~, W S, Q S, P U, K^T U).
+# By operand kind: the gated K K^T and Q K^T tiles (4*C*d) run as tf32 MMAs,
+# everything else (6*C*d + 6*d^2) as fp16 MMAs.
+PREFILL_TF32_FLOPS_PER_TOKEN = H * 4 * 64 * D
+PREFILL_F16_FLOPS_PER_TOKEN = H * (6 * 64 * D + 6 * D * D)
+PREFILL_FLOPS_PER_TOKEN = PREFILL_TF32_FLOPS_PER_TOKEN + PREFILL_F16_FLOPS_PER_TOKEN
+# dense tf32 over dense bf16/fp16 tensor rate (nominal 1.1 / 2.25 PFLOP/s)
+TF32_RATIO = 1.1 / 2.25
 # decode: one sequence-step reads and writes every state of its 32 heads plus
 # q, k, v (bf16), g (fp32), beta, o (bf16)
 DECODE_BYTES_PER_TOKEN = 2 * STATE_BYTES + H * D * (2 * 3 + 4 + 2) + H * 4
@@ -249,7 +255,9 @@ def bench_prefill(args, world, kda, ki, torch, workload="single", heads=None, to
     inp = ki.prefill_inputs(cfg, device=dev)
     names = ("q", "k", "v", "g", "beta")
     in_bytes = sum(inp[n].numel() * inp[n].element_size() for n in names)
-    n_copies = max(2, math.ceil(2 * L2_BYTES / in_bytes) + 1)
+    # rotate over copies of the inputs so that no call finds its inputs in L2
+    # (one copy when they are far larger than L2)
+    n_copies = 1 if in_bytes > 8 * L2_BYTES else max(2, math.ceil(2 * L2_BYTES / in_bytes) + 1)
     sets = [inp] + [{n: inp[n].clone() for n in names} for _ in range(n_copies - 1)]
     cu = inp["cu_seqlens"]
     T, Hn, d, N = inp["q"].shape[0], inp["q"].shape[1], inp["q"].shape[2], cu.shape[0] - 1
@@ -299,7 +307,52 @@ def bench_prefill(args, world, kda, ki, torch, workload="single", heads=None, to
     ms_total = max_over_ranks(world, ms_total)
     return dict(ms_per_step=ms_total / args.steps, launch_ms=launch_ms,
                 clocks=clk.summary(), in_bytes=in_bytes, n_copies=n_copies, tokens=T,
+                n_seqs=N, has_s0=inp["S0"] is not None,
                 tokens_per_s=T / (ms_total / args.steps) * 1e3)
+
+
+def prefill_launches(N, T, Hn, nsm=152):
+    """Kernels one tensor-core prefill call launches (the host-side plan of
+    the library): the chunk table, then per window of 2048 chunks the
+    per-chunk kernel and the chain -- with more than two waves of 32-column
+    chains, the window-plan kernel and both chain forms."""
+    bound = -(-T // 64) + N
+    windows = -(-bound // 2048)
+    per_window = 1 + (3 if N * Hn * 4 > 2 * nsm else 1)
+    return 1 + windows * per_window
+
+
+def prefill_roofline(pf, peaks, peak_kind, traffic=None):
+    """Roofline of one prefill call (chunk table + per-chunk + chain kernels)
+    from its mean CUDA-event duration.  Primary: the tensor cores, against
+    the dense peak of the operand kinds the call uses (tf32 for the gated
+    K K^T / Q K^T tiles at the nominal tf32/bf16 ratio, fp16 at the measured
+    bf16 rate); beside it the HBM fraction of the algorithmic bytes (inputs,
+    outputs, and the 2 MiB fp32 state per sequence read and written)."""
+    launch_s = pf["launch_ms"] * 1e-3
+    T = pf["tokens"]
+    state_io = pf["n_seqs"] * STATE_BYTES * (2 if pf["has_s0"] else 1)
+    bytes_launch = T * PREFILL_BYTES_PER_TOKEN + state_io
+    flops_tf32 = T * PREFILL_TF32_FLOPS_PER_TOKEN
+    flops_f16 = T * PREFILL_F16_FLOPS_PER_TOKEN
+    flops = flops_tf32 + flops_f16
+    bf16 = peaks["bf16_tflops"]
+    # time at peak of each kind, summed: the mixed peak is flops / that time
+    t_peak = flops_tf32 / (bf16 * TF32_RATIO * 1e12) + flops_f16 / (bf16 * 1e12)
+    mixed_peak = flops / t_peak / 1e12
+    tflops = flops / launch_s / 1e12
+    gbs = bytes_launch / launch_s / 1e9
+    src = ("%s (MEASURED_PEAKS.json)" % peak_kind) if peak_kind == "measured" else "fallback"
+    return {"bound": "tensor", "achieved": round(tflops, 2), "peak": round(mixed_peak, 1),
+            "unit": "TFLOP/s", "frac": round(tflops / mixed_peak, 4), "traffic": traffic,
+            "kernel": "prefill op: chunk_table_kernel + intra_kernel + chain_kernel",
+            "peak_source": "%s: bf16_tflops %.1f burst for fp16 MMAs, x %.3f (nominal "
+                           "tf32/bf16) for tf32 MMAs" % (src, bf16, TF32_RATIO),
+            "flops_per_launch": flops, "flops_tf32": flops_tf32, "flops_f16": flops_f16,
+            "launch_ms": round(pf["launch_ms"], 4),
+            "hbm": {"achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(gbs / peaks["hbm_gbs"], 4), "bytes_per_launch": bytes_launch,
+                    "peak_source": "%s hbm_gbs" % src}}
 
 
 def bench_prefill_e2e(args, world, kda, ki, torch):
@@ -441,23 +494,33 @@ def run_ours(args):
     dc = bench_decode(args, world, kda, ki, torch)
 
     tok_s = world * T_PREFILL / (pf["ms_per_step"] * 1e-3)
-    launch_s = pf["launch_ms"] * 1e-3
-    bytes_launch = T_PREFILL * PREFILL_BYTES_PER_TOKEN + STATE_BYTES  # + S_T; S0 = NULL
-    achieved = bytes_launch / launch_s / 1e9
-    flops_launch = T_PREFILL * PREFILL_FLOPS_PER_TOKEN
-    tflops = flops_launch / launch_s / 1e12
     traffic = kernel_traffic("prefill_tc_single_T8192", PREFILL_SOURCES)
-    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": traffic,
-                "kernel": "prefill op: chunk_table_kernel + intra_kernel + chain_kernel",
-                "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
-                if peak_kind == "measured" else "fallback",
-                "bytes_per_launch": bytes_launch, "launch_ms": round(pf["launch_ms"], 4),
-                "tensor": {"flops_per_launch": flops_launch,
-                           "achieved_tflops": round(tflops, 2),
-                           "peak_tflops": peaks["bf16_tflops"],
-                           "frac": round(tflops / peaks["bf16_tflops"], 4)}}
+    roofline = prefill_roofline(pf, peaks, peak_kind, traffic)
+
+    # the other two prefill workloads, each timed alone with its own clocks
+    extra = {}
+    if not args.no_extra_workloads:
+        wl_desc = {
+            "varlen": "KDA chunked prefill, 16 packed sequences with lengths uniform in "
+                      "[512, 16384] (145,226 tokens), H=32, dk=dv=128, bf16 q/k/v, fp32 "
+                      "g/beta, S0 ~ N(0, 0.02^2)",
+            "long": "KDA chunked prefill, B=1 sequence, T=1,048,576, H=32, dk=dv=128, bf16 "
+                    "q/k/v, fp32 g = -0.1 softplus(N)/beta, S0=0",
+        }
+        for wl, steps in (("varlen", 10), ("long", 3)):
+            wargs = argparse.Namespace(**vars(args))
+            wargs.steps, wargs.warmup = steps, 3
+            r = bench_prefill(wargs, world, kda, ki, torch, wl)
+            extra[wl] = {"value": round(world * r["tokens"] / (r["ms_per_step"] * 1e-3), 1),
+                         "unit": "tokens/s", "ms_per_step": round(r["ms_per_step"], 4),
+                         "steps": steps, "warmup": 3,
+                         "gpu_launches": steps * prefill_launches(r["n_seqs"], r["tokens"], H),
+                         "config": {"workload": wl_desc[wl], "tokens": r["tokens"],
+                                    "l2": "inputs %.1f GB, far larger than L2"
+                                          % (r["in_bytes"] / 1e9)},
+                         "roofline": prefill_roofline(r, peaks, peak_kind),
+                         "clocks": r["clocks"]}
+            torch.cuda.empty_cache()
 
     dec_tok_s = world * B_DEC * dc["steps"] / (dc["ms_total"] * 1e-3)
     dec_bytes_launch = B_DEC * DECODE_BYTES_PER_TOKEN
@@ -505,6 +568,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "decode": decode,
     }
+    line.update(extra)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -561,6 +625,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="skip the varlen and long-context prefill keys of the line")
     ap.add_argument("--workload", choices=("single", "varlen", "long", "tiny"), default="single",
                     help="prefill workload of --part prefill (the benchmark line always uses "
                          "the single-sequence workload)")

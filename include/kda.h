@@ -33,6 +33,16 @@
  *     CUDA error is cleared with cudaGetLastError so that it does not leak
  *     into the caller's later checks.  No C++ exception or abort crosses the
  *     ABI.
+ *   - Work runs on the CURRENT device (cudaGetDevice); `stream` must belong to
+ *     it.  Every non-NULL tensor pointer of a device entry point is checked
+ *     with cudaPointerGetAttributes: memory of another device, host memory
+ *     (page-locked or not) and pointers the runtime does not know are
+ *     rejected with KDA_ERR_INVALID_ARG; managed memory is accepted.  With no
+ *     usable device the call returns KDA_ERR_CUDA.
+ *   - The library caches per-device state for the life of the process
+ *     (kernel attributes, the address of the no-allocation scratch, the
+ *     host-buffer entry point's streams).  Do not use it across a
+ *     cudaDeviceReset of a device it has run on.
  *   - Gates g are the log of the per-channel forgetting rate alpha in (0, 1]:
  *     finite values <= 0.  beta is the write strength in [0, 1].
  */
@@ -116,8 +126,9 @@ uint64_t kda_prefill_workspace_size(int32_t N, int64_t T_total, int32_t H,
 /*
  * Synchronise `stream` and report the device-side status of the last
  * kda_prefill_chunked call that used `workspace`: KDA_ERR_TIMEOUT if one of
- * its kernels gave up on a bounded wait (its outputs are then incomplete),
- * KDA_ERR_CUDA if the stream reports an error, else KDA_OK.
+ * its kernels gave up on a bounded wait (its outputs are then incomplete: a
+ * state-chain kernel that finds the per-chunk kernel of its window failed
+ * writes nothing), KDA_ERR_CUDA if the stream reports an error, else KDA_OK.
  */
 kda_status kda_prefill_check(const void *workspace, void *stream);
 
@@ -146,8 +157,8 @@ kda_status kda_prefill_check(const void *workspace, void *stream);
  *   overlap on the GPU (other streams, other host threads) race on it.
  * - It calls no allocator: no cudaMalloc, cudaFree or allocating library
  *   routine.  fp32 and d = 64 inputs need no scratch at all.
- * - Its device-side timeout status is not reported; use kda_prefill_chunked
- *   with kda_prefill_check where that status matters.
+ * - Its device-side status (a bounded wait that gave up) is kept in the first
+ *   word of the array; kda_prefill_noalloc_check reads it.
  */
 kda_status kda_prefill_chunked_noalloc(const void *q, const void *k, const void *v,
                                        const float *g, const float *beta,
@@ -159,6 +170,19 @@ kda_status kda_prefill_chunked_noalloc(const void *q, const void *k, const void 
 
 /* Size in bytes of the fixed scratch array behind the no-allocation entry. */
 uint64_t kda_noalloc_scratch_bytes(void);
+
+/*
+ * kda_prefill_noalloc_check -- kda_prefill_check for the no-allocation entry
+ * point: synchronise `stream`, then read the status word that the last
+ * kda_prefill_chunked_noalloc call on the current device left in the fixed
+ * scratch array.  KDA_ERR_TIMEOUT if one of its kernels gave up on a bounded
+ * wait (its outputs were then left incomplete or untouched), KDA_ERR_CUDA if
+ * the stream reports an error, else KDA_OK (also before any such call).  The
+ * word is shared like the rest of the array: a no-allocation call enqueued on
+ * another stream of the same device between that call and this check
+ * overwrites it.  (No counterpart in the method's description.)
+ */
+kda_status kda_prefill_noalloc_check(void *stream);
 
 /*
  * kda_prefill_chunked_host -- kda_prefill_chunked with the tensors in HOST
@@ -191,7 +215,11 @@ uint64_t kda_noalloc_scratch_bytes(void);
  * the call is ordered after earlier work on `stream`, and `stream` reaches
  * its end only after the last copy into o and S_T.  Host buffers must stay
  * valid and unchanged (outputs: unread) until then.  Calls from several host
- * threads are serialised while they enqueue.  kda_prefill_check(workspace,
+ * threads on one device are serialised while they enqueue; calls on different
+ * devices are not.  With pageable (not page-locked) buffers each copy runs
+ * synchronously with respect to the host, so the pieces no longer overlap
+ * their copies with the kernels and the call takes about as long as its
+ * copies plus its kernels in series.  kda_prefill_check(workspace,
  * stream) reports the device-side status of every piece.  Pointers that the
  * runtime identifies as device memory in place of a host buffer (or host
  * memory, or another device's memory, as the workspace) are rejected with

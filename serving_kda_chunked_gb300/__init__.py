@@ -10,13 +10,14 @@ from ._binding import (KDA_BF16, KDA_ERR_CUDA, KDA_ERR_INVALID_ARG,
                        kda_decode_step_pooled, kda_gdn_decode_step, kda_gdn_decode_step_pooled,
                        kda_gdn_prefill_chunked,
                        kda_noalloc_scratch_bytes, kda_prefill_check, kda_prefill_chunked,
+                       kda_prefill_noalloc_check,
                        kda_prefill_chunked_host, kda_prefill_chunked_noalloc,
                        kda_prefill_host_workspace_size,
                        kda_prefill_workspace_size, load, status_string)
 
 __all__ = ["kda_prefill_chunked", "kda_prefill_chunked_noalloc", "kda_noalloc_scratch_bytes",
            "kda_prefill_chunked_host", "kda_prefill_host_workspace_size",
-           "kda_prefill_workspace_size", "kda_prefill_check",
+           "kda_prefill_workspace_size", "kda_prefill_check", "kda_prefill_noalloc_check",
            "kda_decode_step", "kda_decode_step_pooled", "kda_gdn_prefill_chunked",
            "kda_gdn_decode_step", "kda_gdn_decode_step_pooled", "status_string",
            "abi_version", "load", "KdaError", "LIB_PATH", "KDA_OK",

@@ -71,6 +71,8 @@ def load() -> ctypes.CDLL:
         lib.kda_noalloc_scratch_bytes.restype = u64
         lib.kda_prefill_check.argtypes = [vp, vp]
         lib.kda_prefill_check.restype = ctypes.c_int
+        lib.kda_prefill_noalloc_check.argtypes = [vp]
+        lib.kda_prefill_noalloc_check.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [
             vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]
         lib.kda_decode_step.restype = ctypes.c_int
@@ -101,10 +103,23 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream):
+def _stream(stream, device=None):
+    """Raw handle of ``stream`` (default: the current stream of ``device``, or
+    of the current device); a given stream must live on ``device``."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
+    elif device is not None and stream.device != torch.device(device):
+        raise ValueError("stream is on %s, the tensors on %s" % (stream.device, device))
     return ctypes.c_void_p(int(stream.cuda_stream))
+
+
+def _same_device(device, **tensors):
+    """Every given tensor (None skipped) must be on ``device``: the library
+    runs on one device per call and rejects memory of any other."""
+    for name, t in tensors.items():
+        if t is not None and t.device != device:
+            raise ValueError("%s is on %s, but q is on %s: all tensors of a call must be on "
+                             "one device" % (name, t.device, device))
 
 
 def _check_cuda(name, t, dtype=None, shape=None):
@@ -129,7 +144,16 @@ def kda_prefill_workspace_size(N, T, H, dk, dv, dtype, chunk=64) -> int:
 def kda_prefill_check(workspace, stream=None) -> int:
     """Synchronise the stream and return the device status of the last
     prefill that used ``workspace`` (KDA_OK or KDA_ERR_TIMEOUT)."""
-    return int(load().kda_prefill_check(_ptr(workspace), _stream(stream)))
+    dev = None if workspace is None else workspace.device
+    with torch.cuda.device(dev):
+        return int(load().kda_prefill_check(_ptr(workspace), _stream(stream, dev)))
+
+
+def kda_prefill_noalloc_check(stream=None, device=None) -> int:
+    """Synchronise the stream and return the device status of the last
+    no-allocation prefill on ``device`` (default: the current device)."""
+    with torch.cuda.device(device):
+        return int(load().kda_prefill_noalloc_check(_stream(stream, device)))
 
 
 def _prefill(fn, gate_shape, q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_T, workspace,
@@ -160,10 +184,13 @@ def _prefill(fn, gate_shape, q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_T, wo
     if workspace is not None:
         _check_cuda("workspace", workspace, torch.uint8)
         ws_bytes = workspace.numel()
-    st = getattr(load(), fn)(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
-        N, T, H, dk, dv, _DTYPE_CODE[q.dtype], int(chunk), _ptr(o), _ptr(S_T),
-        _ptr(workspace), ws_bytes, _stream(stream))
+    _same_device(q.device, k=k, v=v, g=g, beta=beta, cu_seqlens=cu_seqlens, S0=S0, o=o,
+                 S_T=S_T, workspace=workspace)
+    with torch.cuda.device(q.device):
+        st = getattr(load(), fn)(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
+            N, T, H, dk, dv, _DTYPE_CODE[q.dtype], int(chunk), _ptr(o), _ptr(S_T),
+            _ptr(workspace), ws_bytes, _stream(stream, q.device))
     if st != KDA_OK:
         raise KdaError(fn, st)
     return o, S_T
@@ -222,10 +249,11 @@ def kda_prefill_chunked_host(q, k, v, g, beta, cu_seqlens, S0=None, *, chunk: in
         dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     _check_cuda("workspace", workspace, torch.uint8)
-    st = load().kda_prefill_chunked_host(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
-        N, T, H, dk, dv, _DTYPE_CODE[q.dtype], int(chunk), _ptr(o), _ptr(S_T),
-        _ptr(workspace), workspace.numel(), _stream(stream))
+    with torch.cuda.device(workspace.device):
+        st = load().kda_prefill_chunked_host(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
+            N, T, H, dk, dv, _DTYPE_CODE[q.dtype], int(chunk), _ptr(o), _ptr(S_T),
+            _ptr(workspace), workspace.numel(), _stream(stream, workspace.device))
     if st != KDA_OK:
         raise KdaError("kda_prefill_chunked_host", st)
     return o, S_T
@@ -261,9 +289,13 @@ def kda_prefill_chunked_noalloc(q, k, v, g, beta, cu_seqlens, S0=None, *, chunk:
     if S_T is None:
         S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
     _check_cuda("S_T", S_T, torch.float32, (N, H, dk, dv))
-    st = load().kda_prefill_chunked_noalloc(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
-        N, T, H, dk, dv, _DTYPE_CODE[q.dtype], int(chunk), _ptr(o), _ptr(S_T), _stream(stream))
+    _same_device(q.device, k=k, v=v, g=g, beta=beta, cu_seqlens=cu_seqlens, S0=S0, o=o,
+                 S_T=S_T)
+    with torch.cuda.device(q.device):
+        st = load().kda_prefill_chunked_noalloc(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
+            N, T, H, dk, dv, _DTYPE_CODE[q.dtype], int(chunk), _ptr(o), _ptr(S_T),
+            _stream(stream, q.device))
     if st != KDA_OK:
         raise KdaError("kda_prefill_chunked_noalloc", st)
     return o, S_T
@@ -306,9 +338,11 @@ def _decode(fn, gate_shape, q, k, v, g, beta, S, o, stream):
     if o is None:
         o = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
     _check_cuda("o", o, q.dtype, (B, H, dv))
-    st = getattr(load(), fn)(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S), B, H, dk, dv,
-        _DTYPE_CODE[q.dtype], _ptr(o), _stream(stream))
+    _same_device(q.device, k=k, v=v, g=g, beta=beta, S=S, o=o)
+    with torch.cuda.device(q.device):
+        st = getattr(load(), fn)(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S), B, H, dk, dv,
+            _DTYPE_CODE[q.dtype], _ptr(o), _stream(stream, q.device))
     if st != KDA_OK:
         raise KdaError(fn, st)
     return o
@@ -348,9 +382,12 @@ def _decode_pooled(fn, gate_shape, q, k, v, g, beta, S_pool, slots, o, stream):
     if o is None:
         o = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
     _check_cuda("o", o, q.dtype, (B, H, dv))
-    st = getattr(load(), fn)(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S_pool), _ptr(slots),
-        S_pool.shape[0], B, H, dk, dv, _DTYPE_CODE[q.dtype], _ptr(o), _stream(stream))
+    _same_device(q.device, k=k, v=v, g=g, beta=beta, S_pool=S_pool, slots=slots, o=o)
+    with torch.cuda.device(q.device):
+        st = getattr(load(), fn)(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S_pool), _ptr(slots),
+            S_pool.shape[0], B, H, dk, dv, _DTYPE_CODE[q.dtype], _ptr(o),
+            _stream(stream, q.device))
     if st != KDA_OK:
         raise KdaError(fn, st)
     return o

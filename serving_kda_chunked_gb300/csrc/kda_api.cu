@@ -2,6 +2,8 @@
 #include "../../include/kda.h"
 #include "kda_internal.cuh"
 
+#include <initializer_list>
+
 namespace {
 
 inline bool aligned16(const void *p) { return p == nullptr || ((uintptr_t)p & 15u) == 0; }
@@ -12,6 +14,30 @@ kda_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return KDA_OK;
     (void)cudaGetLastError();  // clear a sticky launch error for the caller
     return KDA_ERR_CUDA;
+}
+
+// The kernels run on the current device, so every buffer they touch must be
+// memory that device owns (or managed memory).  Host memory -- page-locked
+// memory is reachable from the device, but at PCIe/C2C speed -- and another
+// device's memory are rejected before anything is launched.  Without a usable
+// device the call fails with KDA_ERR_CUDA.
+kda_status check_device_ptrs(std::initializer_list<const void *> ptrs) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    for (const void *p : ptrs) {
+        if (!p) continue;
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return KDA_ERR_INVALID_ARG;
+        }
+        if (at.type == cudaMemoryTypeManaged) continue;
+        if (at.type != cudaMemoryTypeDevice || at.device != dev) return KDA_ERR_INVALID_ARG;
+    }
+    return KDA_OK;
 }
 
 // Shared by the per-channel (KDA) and per-head (Gated DeltaNet) entry points,
@@ -47,6 +73,10 @@ kda_status prefill_impl(const void *q, const void *k, const void *v, const float
         }
     }
 
+    const kda_status dst = check_device_ptrs({q, k, v, g, beta, S0, cu_seqlens, o, S_T,
+                                              tensor_path && !noalloc ? workspace : nullptr});
+    if (dst != KDA_OK) return dst;
+
     kda::PrefillArgs a;
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S0 = S0;
     a.cu_seqlens = cu_seqlens; a.o = o; a.S_T = S_T;
@@ -74,6 +104,8 @@ kda_status decode_impl(const void *q, const void *k, const void *v, const float 
         !aligned16(S) || !aligned16(o) || !aligned4(beta) || !aligned4(slots))
         return KDA_ERR_INVALID_ARG;
     if ((int64_t)B * H > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+    const kda_status dst = check_device_ptrs({q, k, v, g, beta, S, o, pooled ? slots : nullptr});
+    if (dst != KDA_OK) return dst;
 
     kda::DecodeArgs a;
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S = S; a.o = o;
@@ -206,6 +238,15 @@ kda_status kda_prefill_check(const void *workspace, void *stream) {
     return word != 0 ? KDA_ERR_TIMEOUT : KDA_OK;
 }
 
+kda_status kda_prefill_noalloc_check(void *stream) {
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    int32_t word = 0;
+    e = kda::noalloc_status(&word);
+    if (e != cudaSuccess) return cuda_status(e);
+    return word != 0 ? KDA_ERR_TIMEOUT : KDA_OK;
+}
+
 kda_status kda_decode_step(const void *q, const void *k, const void *v,
                            const float *g, const float *beta, float *S,
                            int32_t B, int32_t H, int32_t dk, int32_t dv,
@@ -253,6 +294,6 @@ const char *kda_status_string(int32_t status) {
     }
 }
 
-int32_t kda_abi_version(void) { return (2 << 16) | 3; }
+int32_t kda_abi_version(void) { return (2 << 16) | 4; }
 
 }  // extern "C"

@@ -161,17 +161,19 @@ __global__ void piece_offsets_kernel(const int32_t *__restrict__ cu, int n0, int
 }
 
 // Two copy streams and the events that order them, per device, created on
-// first use.  The mutex is held while a call enqueues its work, so that
-// concurrent calls never interleave their use of the events.
+// first use.  Each device's mutex is held while a call enqueues its work on
+// that device, so that concurrent calls never interleave their use of the
+// events; calls on different devices do not wait for each other.
 struct Lanes {
+    std::mutex mu;
     cudaStream_t h2d = nullptr, d2h = nullptr;
     cudaEvent_t start = nullptr, done = nullptr, ready = nullptr;
     cudaEvent_t in[2] = {nullptr, nullptr}, comp[2] = {nullptr, nullptr},
                 out[2] = {nullptr, nullptr};
 };
-std::mutex g_lanes_mu;
 Lanes g_lanes[64];
 
+// (called with g_lanes[dev].mu held)
 cudaError_t get_lanes(int dev, Lanes **out) {
     Lanes &L = g_lanes[dev];
     if (!L.h2d) {
@@ -212,7 +214,7 @@ cudaError_t launch_prefill_host(const HostPrefillArgs &h, void *workspace, cudaS
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_lanes_mu);
+    std::lock_guard<std::mutex> lock(g_lanes[dev].mu);
     Lanes *ln = nullptr;
     if ((e = get_lanes(dev, &ln)) != cudaSuccess) return e;
 

@@ -42,6 +42,17 @@ size_t prefill_tc_workspace_bytes(int32_t N, int64_t T, int32_t H);
 // (0: not even one chunk fits).
 int64_t noalloc_window_chunks(int32_t N, int32_t H);
 cudaError_t launch_prefill_tc_noalloc(const PrefillArgs &a, cudaStream_t stream);
+// Device status word of the fixed scratch on the current device (the caller
+// has synchronised): nonzero when a bounded wait of the last no-allocation
+// prefill on this device gave up.
+cudaError_t noalloc_status(int32_t *word);
+
+// Forced-timeout hook of the fault-injection test build (compiled with
+// KDA_FAULT_INJECTION; absent from the library itself): while it is set, the
+// per-chunk kernel of every tensor-core prefill waits on an mbarrier that
+// nothing arrives at, before it issues any copy or tensor-core operation,
+// gives up after a few iterations and reports KDA_ERR_TIMEOUT.
+int fault_force_timeout();
 // Prefill from host memory: q, k, v, g, beta, S0, o and S_T of `args` are
 // host pointers, cu_seqlens of `args` is unused; `cu_host` holds the
 // validated offsets in host memory.

@@ -104,6 +104,9 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     int32_t *ws_hdr = reinterpret_cast<int32_t *>(p.ws);
     const int32_t *chunk_base = reinterpret_cast<const int32_t *>(p.ws + WS_HEADER);
     const uint8_t *img_base = p.ws + ws_images_offset(p.N);
+    // a per-chunk kernel of this call gave up on a wait: its images are
+    // incomplete, so leave o and S_T untouched (the status reports it)
+    if (*reinterpret_cast<volatile int32_t *>(ws_hdr) != 0) return;
 
     // A segment launch (one sequence): phase 0 runs, per head, segment 0
     // itself (slices 0-3) and, for each later segment, its state
@@ -472,6 +475,7 @@ __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Para
     int32_t *ws_hdr = reinterpret_cast<int32_t *>(p.ws);
     const int32_t *chunk_base = reinterpret_cast<const int32_t *>(p.ws + WS_HEADER);
     const uint8_t *img_base = p.ws + ws_images_offset(p.N);
+    if (*reinterpret_cast<volatile int32_t *>(ws_hdr) != 0) return;   // see chain_kernel
 
     const int cb = chunk_base[n], ce = chunk_base[n + 1];
     const int a = max(cb, p.w0), b = min(ce, p.w1);

@@ -214,6 +214,19 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         mbar_init(&mbar[2], 2);   // W and U~ issuers
         mbar_fence_init();
     }
+#ifdef KDA_FAULT_INJECTION
+    // Fault-injection test build: wait on the load barrier before any load has
+    // been issued (nothing will arrive), before TMEM is allocated and before
+    // any MMA, so the bounded wait gives up with nothing in flight; the CTA
+    // records the timeout and returns.
+    if (p.force_timeout) {
+        __syncthreads();
+        if (!__syncthreads_and(mbar_wait(&mbar[0], 0, 64))) {
+            if (tid == 0) ws_fail(ws_hdr, 1);
+            return;
+        }
+    }
+#endif
     if (warp == 0) tmem_alloc<512>(tmem_slot);
     fence_before_sync();
     __syncthreads();

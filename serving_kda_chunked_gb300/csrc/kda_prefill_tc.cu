@@ -3,6 +3,7 @@
 // (layouts and the method overview in kda_prefill_tc.cuh).
 #include "kda_prefill_tc.cuh"
 
+#include <atomic>
 #include <mutex>
 
 namespace kda {
@@ -144,6 +145,7 @@ cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, bo
             return cudaErrorInvalidValue;
     }
     p1.g = a.g; p1.scalar_gate = a.scalar_gate ? 1 : 0;
+    p1.force_timeout = fault_force_timeout();
     p1.beta = a.beta; p1.cu = a.cu_seqlens; p1.ws = ws; p1.N = a.N; p1.H = a.H; p1.T = a.T;
     for (int64_t w0 = 0; w0 < bound; w0 += window) {
         const int64_t w1 = w0 + window;
@@ -219,30 +221,57 @@ int64_t noalloc_window_chunks(int32_t N, int32_t H) {
     return (int64_t)(w < (uint64_t)WINDOW_CHUNKS ? w : (uint64_t)WINDOW_CHUNKS);
 }
 
-cudaError_t launch_prefill_tc_noalloc(const PrefillArgs &a, cudaStream_t st) {
-    // device address of the scratch array, looked up once per device with
-    // that device current (host code cannot use the symbol itself)
+namespace {
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current (host code cannot use the symbol
+// itself: it names a host-side stand-in).
+cudaError_t noalloc_scratch(void **ws) {
     static std::mutex mu;
     static void *addr[64] = {nullptr};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    void *ws = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (!addr[dev]) {
-            e = cudaGetSymbolAddress(&addr[dev], g_noalloc_scratch);
-            if (e != cudaSuccess) {
-                addr[dev] = nullptr;
-                return e;
-            }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        e = cudaGetSymbolAddress(&addr[dev], g_noalloc_scratch);
+        if (e != cudaSuccess) {
+            addr[dev] = nullptr;
+            return e;
         }
-        ws = addr[dev];
     }
+    *ws = addr[dev];
+    return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_prefill_tc_noalloc(const PrefillArgs &a, cudaStream_t st) {
+    void *ws = nullptr;
+    cudaError_t e = noalloc_scratch(&ws);
+    if (e != cudaSuccess) return e;
     const int64_t window = noalloc_window_chunks(a.N, a.H);
     if (window < 1) return cudaErrorInvalidValue;
     return run_prefill_tc(a, static_cast<uint8_t *>(ws), window, false, st);
 }
+
+cudaError_t noalloc_status(int32_t *word) {
+    void *ws = nullptr;
+    cudaError_t e = noalloc_scratch(&ws);
+    if (e != cudaSuccess) return e;
+    return cudaMemcpy(word, ws, sizeof *word, cudaMemcpyDeviceToHost);
+}
+
+#ifdef KDA_FAULT_INJECTION
+static std::atomic<int> g_force_timeout{0};
+int fault_force_timeout() { return g_force_timeout.load(); }
+}  // namespace kda
+
+// Test build only: switch the forced timeout on (nonzero) or off.
+extern "C" void kda_test_force_timeout(int32_t on) { kda::g_force_timeout.store(on ? 1 : 0); }
+
+namespace kda {
+#else
+int fault_force_timeout() { return 0; }
+#endif
 
 }  // namespace kda

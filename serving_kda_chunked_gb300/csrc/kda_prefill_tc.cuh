@@ -133,6 +133,7 @@ struct K1Params {
     int64_t T;
     int w0, w1;
     int scalar_gate;
+    int force_timeout;   // fault-injection test build only (see fault_force_timeout)
 };
 
 // ---- chain kernel (one 32-column slice per CTA) ------------------------------

@@ -12,6 +12,8 @@ only bound the computation; ``plain`` (without rho) is reported beside it.
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -35,8 +37,16 @@ def err(x: torch.Tensor, ref: np.ndarray) -> tuple[float, float]:
     return float(np.max(np.maximum(diff - rho, 0.0)) / scale), float(np.max(diff) / scale)
 
 
+# (test id, tensor name, err, plain, tol) of every comparison of the session;
+# conftest prints the workload rows at the end of the run and can write them all
+# to a JSON file (KDA_PARITY_LOG)
+RECORDS: list[tuple[str, str, float, float, float]] = []
+
+
 def assert_close(name, x, ref, tol):
     e, plain = err(x, ref)
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    RECORDS.append((test, name, e, plain, tol))
     assert e <= tol, "%s: err %.3e > %.1e (plain %.3e)" % (name, e, tol, plain)
     return e, plain
 

@@ -246,3 +246,38 @@ def test_host_workspace_size(lib):
     assert f(0, 0, 32, 128, 128, torch.bfloat16) == 0
     assert f(1, 64, 32, 96, 96, torch.bfloat16) == 0
     assert f(1, 1 << 31, 32, 128, 128, torch.bfloat16) == 0
+
+
+def test_device_pointer_check_runs_after_host_validation(lib):
+    """A call that passes every host check reaches the device-pointer check
+    (cudaPointerGetAttributes on each pointer) before any launch: without a
+    device it reports KDA_ERR_CUDA; with one, the fake addresses used here are
+    not device memory and are rejected as invalid.  Nothing is launched."""
+    import torch
+    ws = 0x100000
+    st = _prefill(lib, ws=ws, ws_bytes=1 << 40)
+    dst = _decode(lib)
+    if torch.cuda.is_available():
+        assert st == kda.KDA_ERR_INVALID_ARG and dst == kda.KDA_ERR_INVALID_ARG
+    else:
+        assert st == kda.KDA_ERR_CUDA and dst == kda.KDA_ERR_CUDA
+
+
+def test_noalloc_check_without_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("covered by the GPU tests")
+    assert lib.kda_prefill_noalloc_check(None) == kda.KDA_ERR_CUDA
+
+
+def test_binding_requires_one_device(lib):
+    """All tensors of a call must be on q's device (meta tensors stand in for a
+    second device: the check looks at devices only)."""
+    import torch
+    from serving_kda_chunked_gb300 import _binding
+    dev = torch.device("cuda", 0)
+    _binding._same_device(torch.device("meta"), k=torch.empty(1, device="meta"), S0=None)
+    with pytest.raises(ValueError, match="one device"):
+        _binding._same_device(dev, k=torch.empty(1, device="meta"))
+    with pytest.raises(ValueError, match="one device"):
+        _binding._same_device(dev, workspace=torch.empty(1))

@@ -59,6 +59,9 @@ def _both(lib, inp):
                                          N, T, H, d, d, kda.KDA_BF16, 64, _p(o), _p(S),
                                          _stream())
     assert st == kda.KDA_OK, kda.status_string(st)
+    # its device status: no bounded wait gave up
+    st = lib.kda_prefill_noalloc_check(_stream())
+    assert st == kda.KDA_OK, kda.status_string(st)
     torch.cuda.synchronize()
     return o, S, o_ref, S_ref
 
