@@ -9,18 +9,16 @@ namespace tcp {
 // ------------------------------------------------------------------------------
 // K2: chain kernel
 // ------------------------------------------------------------------------------
-// One CTA of 128 threads per (sequence, head, block of 32 state columns);
-// thread t owns row t (a dk channel) of the fp32 state.  Per chunk:
-//   round 1: D_A + D_B = [W ; Q^] S   (M = 128: rows 0-63 W S, 64-127 Q^ S;
-//            K steps 0-3 into D_A by warp 0, 4-7 into D_B by warp 1)
+// One CTA of 160 threads per (sequence, head, block of 32 state columns):
+// warps 0-3 hold the fp32 state (thread t = row t, a dk channel), warp 4
+// issues the MMAs and the operand loads.  Per chunk:
+//   round 1: D_A = [W ; Q^] S   (M = 128: rows 0-63 W S, 64-127 Q^ S)
 //   U = U~ - W S (fp16);
-//   round 2: D_S + D_S2 = Kbar^T U (warps 0 and 1, two K steps each),
-//            D_A += [0 ; P] U (warp 2; rows 64-127 then hold O - Q^S_B)
-//   S = Diag(e^gamma_last) S + D_S + D_S2.
-// A thread issuing tcgen05.mma is busy for ~90 cycles per instruction, so the
-// few MMAs on the state's critical path are spread over several issuing warps.
+//   round 2: D_S = Kbar^T U, then D_A += [0 ; P] U (rows 64-127 then hold O)
+//   S = Diag(e^gamma_last) S + D_S.
 // TMEM accumulators alternate between two sets so that the outputs of chunk
-// i are read while the MMAs of chunk i + 1 run.
+// i are read while the MMAs of chunk i + 1 run; operand images arrive with
+// bulk async copies two chunks ahead (three stages).
 // ------------------------------------------------------------------------------
 // window plan (batches of many sequences): the sequences with chunks in the
 // window [w0, w1) -- and, in the first window, the empty ones, whose initial
@@ -88,10 +86,19 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + S2_MISC);   // [0..1] loads, [2] r1, [3] r2
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 4);
+    // [0..2] loads of the three stages, [3] round 1, [4] round 2 state part,
+    // [5] round 2 output part, [6] drain
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + S2_MISC);
+    constexpr int MB_R1 = S2_NSTAGE, MB_R2S = MB_R1 + 1, MB_R2O = MB_R1 + 2, MB_DRAIN = MB_R1 + 3;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + MB_DRAIN + 1);
+    int32_t *iss = reinterpret_cast<int32_t *>(tmem_slot + 1);   // [3] last chunk loaded per stage
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31;
+    // warp index the compiler knows to be warp-uniform (so that the issuer
+    // warp's branch keeps the MMA operands in uniform registers)
+    const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
+    const bool issuer = warp == K2_ISSUER;   // MMAs and operand loads; holds no state
+    const int row = tid;                     // warps 0-3: state row (dk channel) = TMEM lane
     const int H = p.H;
     const int unit = blockIdx.x;
     int slice = unit % NSLICE;
@@ -142,13 +149,13 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
         b = min(b, sa + p.seg_len);
         a = sa;
     }
-    const int64_t sbase = ((int64_t)n * H + h) * D * D + (int64_t)tid * D + slice * DVS;
+    const int64_t sbase_g = ((int64_t)n * H + h) * D * D + (int64_t)row * D + slice * DVS;
     if (cb == ce && !p.nseg) {            // empty sequence: pass the state through
-        if (p.w0 == 0) {
+        if (p.w0 == 0 && !issuer) {
             for (int j = 0; j < DVS; j += 4) {
-                float4 x = p.S0 ? *reinterpret_cast<const float4 *>(p.S0 + sbase + j)
+                float4 x = p.S0 ? *reinterpret_cast<const float4 *>(p.S0 + sbase_g + j)
                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4 *>(p.S_T + sbase + j) = x;
+                *reinterpret_cast<float4 *>(p.S_T + sbase_g + j) = x;
             }
         }
         return;
@@ -163,16 +170,16 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     float S[DVS];
     if (role == SEG_M) {          // identity columns slice*32 .. slice*32+31
 #pragma unroll
-        for (int j = 0; j < DVS; ++j) S[j] = (tid == slice * DVS + j) ? 1.f : 0.f;
-    } else if (role == SEG_B) {
+        for (int j = 0; j < DVS; ++j) S[j] = (row == slice * DVS + j) ? 1.f : 0.f;
+    } else if (role == SEG_B || issuer) {
 #pragma unroll
         for (int j = 0; j < DVS; ++j) S[j] = 0.f;
     } else {
         const float *src = (a == cb) ? p.S0 : p.S_T;
-        int64_t off = sbase;
+        int64_t off = sbase_g;
         if (p.nseg && seg > 0) {  // the start state the combine step produced
             src = smap(p.smaps, p.nseg, h, seg, SMAP_START);
-            off = (int64_t)tid * D + slice * DVS;
+            off = (int64_t)row * D + slice * DVS;
         }
 #pragma unroll
         for (int j = 0; j < DVS; j += 4) {
@@ -183,29 +190,29 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     }
     const bool write_o = role == SEG_FULL;
     const float u_scale = role == SEG_M ? 0.f : 1.f;   // the homogeneous map drops U~
-    // the zero half of [0 ; P] in both stages
-    for (int e = tid; e < 2 * 8192 / 16; e += K2_THREADS) {
+    // the zero half of [0 ; P] in every stage
+    for (int e = tid; e < S2_NSTAGE * 8192 / 16; e += K2_THREADS) {
         const int st = e / 512, off = (e % 512) * 16;
         *reinterpret_cast<uint4 *>(sm + st * S2_STAGE + S2_PZ + off) = make_uint4(0u, 0u, 0u, 0u);
     }
     if (tid == 0) {
-        mbar_init(&mbar[0], 1);
-        mbar_init(&mbar[1], 1);
-        mbar_init(&mbar[2], 2);   // round 1: two issuers
-        mbar_init(&mbar[3], 3);   // round 2: three issuers
+        for (int j = 0; j <= MB_DRAIN; ++j) mbar_init(&mbar[j], 1);
         mbar_fence_init();
+        for (int j = 0; j < S2_NSTAGE; ++j) iss[j] = -1;
     }
     if (warp == 0) tmem_alloc<256>(tmem_slot);
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = warp_uniform(*tmem_slot);
+    const uint32_t smb = warp_uniform(smem_addr(sm));
 
     auto issue_loads = [&](int ch, int stage) {
         const uint8_t *src = img_base + ((uint64_t)(ch - p.w0) * H + h) * CH_STRIDE;
         uint8_t *dst = sm + stage * S2_STAGE;
         uint64_t *mb = &mbar[stage];
+        iss[stage] = ch - a;
         mbar_arrive_expect_tx(mb, S2_TX);
         bulk_g2s(dst + S2_WQ, src + IMG_W, 8192, mb);              // W, k 0-63
         bulk_g2s(dst + S2_WQ + 8192, src + IMG_Q, 8192, mb);       // Q^, k 0-63
@@ -216,163 +223,210 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
         bulk_g2s(dst + S2_U, src + IMG_U + slice * 4096, 4096, mb);
         bulk_g2s(dst + S2_G, src + IMG_G, 512, mb);
     };
-    if (tid == 0 && a < b) {
-        issue_loads(a, 0);
-        if (a + 1 < b) issue_loads(a + 1, 1);
+    if (issuer) {                 // chunks a and a + 1 up front
+        if (elect_one()) {
+            if (a < b) issue_loads(a, 0);
+            if (a + 1 < b) issue_loads(a + 1, 1);
+        }
+        __syncwarp();
     }
 
-    const uint64_t d_sop = sdesc(smem_addr(sm + S2_SOP), 128, 2048, LAYOUT_NONE);
-    const uint64_t d_uop = sdesc(smem_addr(sm + S2_UOP), 128, 1024, LAYOUT_NONE);
     const uint32_t id_wq = idesc(128, DVS, FMT_F16, FMT_F16, 0, 1);
     const uint32_t id_kb = idesc(128, DVS, FMT_F16, FMT_F16, 1, 1);
 
-    // stores the O rows of a finished chunk (threads 64-127: row tid - 64)
-    auto store_o = [&](int set, int64_t t0, int L) {
-        if (warp >= 2) {
-            float oa[16], ob[16], pa[16], pb[16];
-            tmem_ld16(tmem_at(tmem, warp, 128 * set), oa);
-            tmem_ld16(tmem_at(tmem, warp, 128 * set + 16), ob);
-            tmem_ld16(tmem_at(tmem, warp, 128 * set + 32), pa);
-            tmem_ld16(tmem_at(tmem, warp, 128 * set + 48), pb);
-            tmem_wait_ld();
+    // the O rows of a finished chunk (warps 2-3: row - 64), once its P U MMA
+    // (the last to accumulate into them) has completed
+    auto store_o = [&](int set, int64_t t0, int L, uint32_t pu_parity) -> bool {
+        if (!mbar_wait(&mbar[MB_R2O], pu_parity)) return false;
+        fence_after_sync();
+        float oa[16], ob[16];
+        tmem_ld16(tmem_at(tmem, warp, 128 * set), oa);
+        tmem_ld16(tmem_at(tmem, warp, 128 * set + 16), ob);
+        tmem_wait_ld();
+        const int r = row - 64;
+        if (r < L) {
+            __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * D + slice * DVS;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) { oa[j] += pa[j]; ob[j] += pb[j]; }
-            const int r = tid - 64;
-            if (r < L) {
-                __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * D + slice * DVS;
-#pragma unroll
-                for (int gq = 0; gq < DVS / 8; ++gq) {
-                    const float *src = gq < 2 ? oa + 8 * gq : ob + 8 * (gq - 2);
-                    __nv_bfloat162 b0 = __floats2bfloat162_rn(src[0], src[1]);
-                    __nv_bfloat162 b1 = __floats2bfloat162_rn(src[2], src[3]);
-                    __nv_bfloat162 b2 = __floats2bfloat162_rn(src[4], src[5]);
-                    __nv_bfloat162 b3 = __floats2bfloat162_rn(src[6], src[7]);
-                    *reinterpret_cast<uint4 *>(dst + 8 * gq) = make_uint4(
-                        *reinterpret_cast<uint32_t *>(&b0), *reinterpret_cast<uint32_t *>(&b1),
-                        *reinterpret_cast<uint32_t *>(&b2), *reinterpret_cast<uint32_t *>(&b3));
-                }
+            for (int gq = 0; gq < DVS / 8; ++gq) {
+                const float *src = gq < 2 ? oa + 8 * gq : ob + 8 * (gq - 2);
+                __nv_bfloat162 b0 = __floats2bfloat162_rn(src[0], src[1]);
+                __nv_bfloat162 b1 = __floats2bfloat162_rn(src[2], src[3]);
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(src[4], src[5]);
+                __nv_bfloat162 b3 = __floats2bfloat162_rn(src[6], src[7]);
+                *reinterpret_cast<uint4 *>(dst + 8 * gq) = make_uint4(
+                    *reinterpret_cast<uint32_t *>(&b0), *reinterpret_cast<uint32_t *>(&b1),
+                    *reinterpret_cast<uint32_t *>(&b2), *reinterpret_cast<uint32_t *>(&b3));
             }
         }
+        return true;
     };
 
-    bool ok = true;
+    // Per chunk i (stage i % 3, TMEM set i % 2; D_A = set columns 0-31, D_S =
+    // set columns 64-95).  Warps 0-3 hold the fp32 state (thread = row); warp
+    // 4 issues every MMA and load from its elected lane, so no state-holding
+    // warp ever blocks on an issue:
+    //   B1 (all):       S (fp16 operand) written, chunk i's operands landed
+    //   warp 4:         round 1, D_A = [W ; Q^] S (8 K steps) -> MB_R1
+    //   warps 0-1:      U = U~ - W S (rows 0-63), fp16 operand
+    //   warps 2-3:      the O rows of chunk i - 1 (off the critical path)
+    //   B2 (all):       U written
+    //   warp 4:         round 2, D_S = Kbar^T U (4 K steps) -> MB_R2S, then
+    //                   D_A += [0 ; P] U (4 K steps) -> MB_R2O; then the
+    //                   operands of chunk i + 2 into the stage of chunk i - 1
+    //   warps 0-3:      S = Diag(e^gamma_last) S + D_S   (after MB_R2S)
+    // Round 1 of chunk i completes after every MMA of chunk i - 1 (one
+    // issuing thread, whose commits track all its earlier MMAs), so when B2
+    // passes, chunk i - 1's stage and the U operand's previous contents are
+    // free.  Loads therefore run two chunks ahead.
+    bool ok = true, bad = false;
     int64_t prev_t0 = 0;
     int prev_L = 0;
     for (int ch = a; ch < b; ++ch) {
-        const int i = ch - a, stage = i & 1, set = i & 1;
+        const int i = ch - a, stage = i % S2_NSTAGE, set = i & 1;
         uint8_t *st = sm + stage * S2_STAGE;
-        const uint32_t tset = tmem + 128 * set;
         const int64_t t0 = bos + (int64_t)(ch - cb) * C;
         const int L = (int)((eos - t0) < C ? (eos - t0) : C);
-        ok = __syncthreads_and(mbar_wait(&mbar[stage], (i >> 1) & 1));
-        if (!ok) break;
-
-        // S (fp16) -> B operand [K = dk][N = 32], MN-major, no swizzle:
-        // core matrix (8 K rows x 8 N) at (n/8) * 2048 + (k/8) * 128
+        if (!issuer) {
+            // S (fp16) -> B operand [K = dk][N = 32], MN-major, no swizzle:
+            // core matrix (8 K rows x 8 N) at (n/8) * 2048 + (k/8) * 128
 #pragma unroll
-        for (int gq = 0; gq < DVS / 8; ++gq) {
-            uint4 v4 = make_uint4(pack_h2(S[8 * gq + 0], S[8 * gq + 1]), pack_h2(S[8 * gq + 2], S[8 * gq + 3]),
-                                  pack_h2(S[8 * gq + 4], S[8 * gq + 5]), pack_h2(S[8 * gq + 6], S[8 * gq + 7]));
-            *reinterpret_cast<uint4 *>(sm + S2_SOP + gq * 2048 + (tid >> 3) * 128 + (tid & 7) * 16) = v4;
+            for (int gq = 0; gq < DVS / 8; ++gq) {
+                uint4 v4 = make_uint4(pack_h2(S[8 * gq + 0], S[8 * gq + 1]), pack_h2(S[8 * gq + 2], S[8 * gq + 3]),
+                                      pack_h2(S[8 * gq + 4], S[8 * gq + 5]), pack_h2(S[8 * gq + 6], S[8 * gq + 7]));
+                *reinterpret_cast<uint4 *>(sm + S2_SOP + gq * 2048 + (row >> 3) * 128 + (row & 7) * 16) = v4;
+            }
+            fence_async_smem();
         }
-        fence_async_smem();
         fence_before_sync();
-        __syncthreads();
-        if (lane == 0 && warp < 2) {      // round 1: warp w takes K atom w
-            fence_after_sync();
-            const uint64_t dwq = sdesc_k_sw128(smem_addr(st + S2_WQ));
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_f16(tset + 32 * warp, sdesc_add(dwq, warp * 16384 + s * 32),
-                        sdesc_add(d_sop, 256 * (4 * warp + s)), id_wq, s > 0);
-            mma_commit(&mbar[2]);
-        }
-        if (i > 0 && write_o) store_o(set ^ 1, prev_t0, prev_L);   // previous chunk's outputs
-        ok = __syncthreads_and(mbar_wait(&mbar[2], i & 1));
+        ok = __syncthreads_and(!bad && mbar_wait(&mbar[stage], (uint32_t)((i / S2_NSTAGE) & 1)));
         fence_after_sync();
         if (!ok) break;
 
-        // U = U~ - W S for token rows 0-63 (threads 0-63)
-        if (warp < 2) {
-            float w0[16], w1[16], x0[16], x1[16];
+        if (issuer) {                     // round 1
+            const uint32_t stb = warp_uniform(smb + (uint32_t)stage * S2_STAGE);
+            const uint32_t d_a = warp_uniform(tmem + 128u * (uint32_t)set);
+            const uint64_t dwq = sdesc_k_sw128(stb + S2_WQ);
+            const uint64_t dso = sdesc(smb + S2_SOP, 128, 2048, LAYOUT_NONE);
+            if (elect_one()) {
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_f16(d_a, sdesc_add(dwq, (s >> 2) * 16384 + (s & 3) * 32),
+                            sdesc_add(dso, 256 * s), id_wq, s > 0);
+                mma_commit(&mbar[MB_R1]);
+            }
+            __syncwarp();
+        } else if (warp < 2) {            // U = U~ - W S for token rows 0-63
+            if (!mbar_wait(&mbar[MB_R1], i & 1)) bad = true;
+            fence_after_sync();
+            float w0[16], w1[16];
             tmem_ld16(tmem_at(tmem, warp, 128 * set), w0);
             tmem_ld16(tmem_at(tmem, warp, 128 * set + 16), w1);
-            tmem_ld16(tmem_at(tmem, warp, 128 * set + 32), x0);
-            tmem_ld16(tmem_at(tmem, warp, 128 * set + 48), x1);
             tmem_wait_ld();
-            const int r = tid;
-            const __half *ut = reinterpret_cast<const __half *>(st + S2_U) + r * DVS;
             float u[DVS];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                u[j] = u_scale * __half2float(ut[j]) - (w0[j] + x0[j]);
-                u[16 + j] = u_scale * __half2float(ut[16 + j]) - (w1[j] + x1[j]);
+            for (int q = 0; q < 4; ++q) {
+                const uint4 x = *reinterpret_cast<const uint4 *>(st + S2_U + u_img_off(row, q));
+                const __half2 *h2 = reinterpret_cast<const __half2 *>(&x);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(h2[e]);
+                    const int j = 8 * q + 2 * e;
+                    u[j] = u_scale * f.x - (j < 16 ? w0[j] : w1[j - 16]);
+                    u[j + 1] = u_scale * f.y - (j + 1 < 16 ? w0[j + 1] : w1[j - 15]);
+                }
             }
 #pragma unroll
             for (int gq = 0; gq < DVS / 8; ++gq) {
                 uint4 v4 = make_uint4(pack_h2(u[8 * gq + 0], u[8 * gq + 1]), pack_h2(u[8 * gq + 2], u[8 * gq + 3]),
                                       pack_h2(u[8 * gq + 4], u[8 * gq + 5]), pack_h2(u[8 * gq + 6], u[8 * gq + 7]));
-                *reinterpret_cast<uint4 *>(sm + S2_UOP + gq * 1024 + (r >> 3) * 128 + (r & 7) * 16) = v4;
+                *reinterpret_cast<uint4 *>(sm + S2_UOP + gq * 1024 + (row >> 3) * 128 + (row & 7) * 16) = v4;
             }
+            fence_async_smem();
+        } else if (i > 0) {               // warps 2-3: the previous chunk's outputs
+            const uint32_t par = (uint32_t)((i - 1) & 1);
+            const bool okp = write_o ? store_o(set ^ 1, prev_t0, prev_L, par)
+                                     : mbar_wait(&mbar[MB_R2O], par);
+            if (!okp) bad = true;
         }
-        fence_async_smem();
+        // B2 (all): U is in shared memory.  Warps 2-3 take part too: they have
+        // then seen chunk i - 1's P U complete before the issuer commits chunk
+        // i's, so no barrier phase runs two ahead of a thread that waits on it.
         fence_before_sync();
         __syncthreads();
-        if (lane == 0 && warp < 3) {      // round 2: warps 0-1 Kbar^T U halves, warp 2 P U
-            fence_after_sync();
-            if (warp < 2) {
-                const uint64_t dkb = sdesc(smem_addr(st + S2_KB), 8192, 1024, LAYOUT_SW128);
-#pragma unroll
-                for (int s = 0; s < 2; ++s) {
-                    const int ks = 2 * warp + s;
-                    mma_f16(tset + 64 + 32 * warp, sdesc_add(dkb, 2048 * ks),
-                            sdesc_add(d_uop, 256 * ks), id_kb, s > 0);
-                }
-            } else {
-                const uint64_t dpz = sdesc_k_sw128(smem_addr(st + S2_PZ));
+        fence_after_sync();
+        if (issuer) {                     // round 2, then the loads of chunk i + 2
+            const uint32_t stb = warp_uniform(smb + (uint32_t)stage * S2_STAGE);
+            const uint32_t d_a = warp_uniform(tmem + 128u * (uint32_t)set);
+            const uint64_t dkb = sdesc(stb + S2_KB, 8192, 1024, LAYOUT_SW128);
+            const uint64_t dpz = sdesc_k_sw128(stb + S2_PZ);
+            const uint64_t duo = sdesc(smb + S2_UOP, 128, 1024, LAYOUT_NONE);
+            if (elect_one()) {
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_f16(tset, sdesc_add(dpz, 32 * s), sdesc_add(d_uop, 256 * s), id_wq, 1);
+                    mma_f16(d_a + 64, sdesc_add(dkb, 2048 * s), sdesc_add(duo, 256 * s), id_kb, s > 0);
+                mma_commit(&mbar[MB_R2S]);
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_f16(d_a, sdesc_add(dpz, 32 * s), sdesc_add(duo, 256 * s), id_wq, 1);
+                mma_commit(&mbar[MB_R2O]);
+                if (ch + 2 < b) issue_loads(ch + 2, (i + 2) % S2_NSTAGE);
             }
-            mma_commit(&mbar[3]);
-        }
-        ok = __syncthreads_and(mbar_wait(&mbar[3], i & 1));
-        fence_after_sync();
-        if (!ok) break;
-
-        // S = Diag(e^gamma_last) S + Kbar^T U
-        {
-            float d2a[16], d2b[16], d3a[16], d3b[16];
+            __syncwarp();
+        } else {                          // S = Diag(e^gamma_last) S + Kbar^T U
+            if (!mbar_wait(&mbar[MB_R2S], i & 1)) bad = true;
+            fence_after_sync();
+            float d2a[16], d2b[16];
             tmem_ld16(tmem_at(tmem, warp, 128 * set + 64), d2a);
             tmem_ld16(tmem_at(tmem, warp, 128 * set + 80), d2b);
-            tmem_ld16(tmem_at(tmem, warp, 128 * set + 96), d3a);
-            tmem_ld16(tmem_at(tmem, warp, 128 * set + 112), d3b);
             tmem_wait_ld();
-            const float gl = reinterpret_cast<const float *>(st + S2_G)[tid];
+            const float gl = reinterpret_cast<const float *>(st + S2_G)[row];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                S[j] = gl * S[j] + (d2a[j] + d3a[j]);
-                S[16 + j] = gl * S[16 + j] + (d2b[j] + d3b[j]);
+                S[j] = gl * S[j] + d2a[j];
+                S[16 + j] = gl * S[16 + j] + d2b[j];
             }
         }
         prev_t0 = t0;
         prev_L = L;
-        fence_before_sync();
-        __syncthreads();   // every thread is done with this stage
-        if (tid == 0 && ch + 2 < b) issue_loads(ch + 2, stage);
     }
-    if (ok && write_o && a < b) store_o((b - 1 - a) & 1, prev_t0, prev_L);
+    ok = ok && __syncthreads_and(!bad);
+    // the last chunk's outputs (and, in any case, its P U MMA -- the last MMA
+    // issued -- before TMEM is freed)
+    if (ok && a < b && (warp == 2 || warp == 3)) {
+        const uint32_t par = (uint32_t)((b - 1 - a) & 1);
+        const bool okp = write_o ? store_o((b - 1 - a) & 1, prev_t0, prev_L, par)
+                                 : mbar_wait(&mbar[MB_R2O], par);
+        if (!okp) bad = true;
+    }
+    ok = __syncthreads_and(ok && !bad);
 
-    if (!ok && tid == 0) ws_fail(ws_hdr, 2);
+    if (!ok) {
+        // a bounded wait gave up: record it, and let the copies and MMAs this
+        // CTA issued finish (bounded waits) before its shared memory and TMEM
+        // are released
+        if (tid == 0) {
+            ws_fail(ws_hdr, 2);
+            for (int s2 = 0; s2 < S2_NSTAGE; ++s2)
+                if (iss[s2] >= 0)
+                    mbar_wait(&mbar[s2], (uint32_t)((iss[s2] / S2_NSTAGE) & 1), 1u << 20);
+        }
+        if (issuer) {
+            if (elect_one()) {
+                mma_commit(&mbar[MB_DRAIN]);
+                mbar_wait(&mbar[MB_DRAIN], 0, 1u << 20);
+            }
+            __syncwarp();
+        }
+    }
     // final state: S_T, or (segment launch) the segment's map, contribution
     // or end state for the combine step; the last segment writes S_T
     float *dst = nullptr;
     if (!p.nseg || (p.phase == 1 && seg == p.nseg - 1))
-        dst = p.S_T + sbase;
+        dst = p.S_T + sbase_g;
     else if (p.phase == 0)   // segment 0 ends in its B slot
-        dst = smap(p.smaps, p.nseg, h, seg, role == SEG_M ? SMAP_M : SMAP_B) + (int64_t)tid * D +
+        dst = smap(p.smaps, p.nseg, h, seg, role == SEG_M ? SMAP_M : SMAP_B) + (int64_t)row * D +
               slice * DVS;
-    if (dst) {
+    if (dst && !issuer) {
 #pragma unroll
         for (int j = 0; j < DVS; j += 4)
             *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
@@ -440,28 +494,28 @@ __global__ void __launch_bounds__(COMB_THREADS) segment_combine_kernel(float *sm
 // owns state columns 32s..32s+31; its thread t (0..127) holds row t (a dk
 // channel) of those columns in fp32 registers.  Every MMA spans the whole
 // state (N = 128), so one SM carries a whole head.  Per chunk:
-//   round 1: A_s + B_s = [W ; Q^] S   (M = 128, K = dk, split in halves over
-//            two issuers; rows 0-63 W S, 64-127 Q^ S)
+//   round 1: A_s = [W ; Q^] S           (M = 128, K = dk; rows 0-63 W S,
+//            64-127 Q^ S)
 //   U = U~ - W S (fp16)                (rows 0-63: warps 0-1 of every warpgroup)
-//   round 2: B_s' = Kbar^T U           (M = 128, K = 64; first issuer)
-//            A_s += [0 ; P] U          (second issuer; rows 64-127 of A_s + B_s
-//                                       then hold O)
+//   round 2: B_s' = Kbar^T U           (M = 128, K = 64; committed on its own)
+//            A_s += [0 ; P] U          (rows 64-127 of A_s then hold O)
 //   S = Diag(e^gamma_last) S + B_s'.
-// TMEM holds two 128-column accumulators per set; chunk c uses set s = c % 2
-// for round 1 and the other set's B (whose previous contents, the last
-// chunk's outputs, have left TMEM during round 1) for Kbar^T U.  Operand
-// images arrive with bulk async copies, double buffered; a stage is reloaded
-// once the next chunk's round 1 is issued, when its last reader (the P U MMA)
-// has long finished.
+// All MMAs are issued by warp 0's elected lane.  TMEM holds two 128-column
+// accumulators per set; chunk c uses set s = c % 2 for round 1 and the other
+// set's B for Kbar^T U.  Operand images arrive with bulk async copies, double
+// buffered; a stage is reloaded once the next chunk's round 1 is issued, when
+// its last reader (the P U MMA) has long finished.
 __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    // [0..1] loads, [2] round 1 (two issuers), [3] round 2 state, [4] round 2 outputs
+    // [0..1] loads, [2] round 1, [3] round 2 state, [4] round 2 outputs, [5] drain
     uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + S2W_MISC);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 5);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 6);
+    int32_t *iss = reinterpret_cast<int32_t *>(tmem_slot + 1);   // [2] last chunk loaded per stage
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);   // warp-uniform for the compiler
     const int wg = warp >> 2, wq = warp & 3;   // column block, TMEM lane quadrant
     const int row = 32 * wq + lane;            // state row (dk channel) / TMEM lane
     const int col0 = 32 * wg;                  // first state column of this thread
@@ -511,20 +565,23 @@ __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Para
         *reinterpret_cast<uint4 *>(sm + st * S2W_STAGE + S2W_PZ + off) = make_uint4(0u, 0u, 0u, 0u);
     }
     if (tid == 0) {
-        for (int j = 0; j < 5; ++j) mbar_init(&mbar[j], j == 2 ? 2 : 1);
+        for (int j = 0; j < 6; ++j) mbar_init(&mbar[j], 1);
         mbar_fence_init();
+        iss[0] = iss[1] = -1;
     }
     if (warp == 0) tmem_alloc<512>(tmem_slot);
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = warp_uniform(*tmem_slot);
+    const uint32_t smb = warp_uniform(smem_addr(sm));
 
     auto issue_loads = [&](int ch, int stage) {
         const uint8_t *src = img_base + ((uint64_t)(ch - p.w0) * H + h) * CH_STRIDE;
         uint8_t *dst = sm + stage * S2W_STAGE;
         uint64_t *mb = &mbar[stage];
+        iss[stage] = ch - a;
         mbar_arrive_expect_tx(mb, S2W_TX);
         bulk_g2s(dst + S2W_WQ, src + IMG_W, 8192, mb);              // W, k 0-63
         bulk_g2s(dst + S2W_WQ + 8192, src + IMG_Q, 8192, mb);       // Q^, k 0-63
@@ -542,8 +599,6 @@ __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Para
     // chunk a + 1 is loaded up front; chunk c + 1 for c > a is loaded during
     // chunk c (see round 1)
 
-    const uint64_t d_sop = sdesc(smem_addr(sm + S2W_SOP), 128, 2048, LAYOUT_NONE);
-    const uint64_t d_uop = sdesc(smem_addr(sm + S2W_UOP), 128, 1024, LAYOUT_NONE);
     const uint32_t id_wq = idesc(128, 128, FMT_F16, FMT_F16, 0, 1);
     const uint32_t id_kb = idesc(128, 128, FMT_F16, FMT_F16, 1, 1);
 
@@ -552,14 +607,10 @@ __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Para
         if (wq >= 2) {
             const bool done = mbar_wait(&mbar[4], phase & 1);
             fence_after_sync();
-            float oa[16], ob[16], pa[16], pb[16];
+            float oa[16], ob[16];
             tmem_ld16(tmem_at(tmem, wq, 256 * set + col0), oa);
             tmem_ld16(tmem_at(tmem, wq, 256 * set + col0 + 16), ob);
-            tmem_ld16(tmem_at(tmem, wq, 256 * set + 128 + col0), pa);
-            tmem_ld16(tmem_at(tmem, wq, 256 * set + 128 + col0 + 16), pb);
             tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) { oa[j] += pa[j]; ob[j] += pb[j]; }
             const int r = row - 64;
             if (done && r < L) {
                 __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * D + col0;
@@ -586,7 +637,7 @@ __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Para
     for (int ch = a; ch < b; ++ch) {
         const int i = ch - a, stage = i & 1, set = i & 1;
         uint8_t *st = sm + stage * S2W_STAGE;
-        const uint32_t acc_a = tmem + 256 * set, acc_b = acc_a + 128;   // round 1
+        const uint32_t acc_a = tmem + 256 * set;                          // round 1
         const uint32_t acc_s = tmem + 256 * (set ^ 1) + 128;              // Kbar^T U
         const int64_t t0 = bos + (int64_t)(ch - cb) * C;
         const int L = (int)((eos - t0) < C ? (eos - t0) : C);
@@ -604,20 +655,26 @@ __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Para
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
-        if (lane == 0 && warp < 2) {      // round 1: warp w takes K atom w
+        if (warp == 0) {                  // round 1
             fence_after_sync();
-            const uint64_t dwq = sdesc_k_sw128(smem_addr(st + S2W_WQ));
+            const uint32_t stb = warp_uniform(smb + (uint32_t)stage * S2W_STAGE);
+            const uint32_t d_a = warp_uniform(acc_a);
+            const uint64_t dwq = sdesc_k_sw128(stb + S2W_WQ);
+            const uint64_t dso = sdesc(smb + S2W_SOP, 128, 2048, LAYOUT_NONE);
+            if (elect_one()) {
 #pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4)
-                mma_f16(warp == 0 ? acc_a : acc_b, sdesc_add(dwq, warp * 16384 + s4 * 32),
-                        sdesc_add(d_sop, 256 * (4 * warp + s4)), id_wq, s4 > 0);
-            mma_commit(&mbar[2]);
-            // the previous chunk's P U MMA was the last reader of the other
-            // stage: reload it with the chunk after next
-            if (warp == 0 && i > 0 && ch + 1 < b) {
-                if (mbar_wait(&mbar[4], (i - 1) & 1)) issue_loads(ch + 1, stage ^ 1);
-                else ws_fail(ws_hdr, 2);
+                for (int s8 = 0; s8 < 8; ++s8)
+                    mma_f16(d_a, sdesc_add(dwq, (s8 >> 2) * 16384 + (s8 & 3) * 32),
+                            sdesc_add(dso, 256 * s8), id_wq, s8 > 0);
+                mma_commit(&mbar[2]);
+                // the previous chunk's P U MMA was the last reader of the other
+                // stage: reload it with the chunk after next
+                if (i > 0 && ch + 1 < b) {
+                    if (mbar_wait(&mbar[4], (i - 1) & 1)) issue_loads(ch + 1, stage ^ 1);
+                    else ws_fail(ws_hdr, 2);
+                }
             }
+            __syncwarp();
         }
         bool o_ok = true;
         if (i > 0) o_ok = store_o(set ^ 1, (uint32_t)(i - 1), prev_t0, prev_L);
@@ -627,20 +684,15 @@ __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Para
 
         // U = U~ - W S for token rows 0-63 (warps 0-1 of each group)
         if (wq < 2) {
-            float w0[16], w1[16], x0[16], x1[16];
+            float w0[16], w1[16];
             tmem_ld16(tmem_at(tmem, wq, 256 * set + col0), w0);
             tmem_ld16(tmem_at(tmem, wq, 256 * set + col0 + 16), w1);
-            tmem_ld16(tmem_at(tmem, wq, 256 * set + 128 + col0), x0);
-            tmem_ld16(tmem_at(tmem, wq, 256 * set + 128 + col0 + 16), x1);
             tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) { w0[j] += x0[j]; w1[j] += x1[j]; }
             const int r = row;
-            const uint4 *ut = reinterpret_cast<const uint4 *>(st + S2W_U + wg * 4096 + r * 64);
             float u[32];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
-                const uint4 x = ut[q4];
+                const uint4 x = *reinterpret_cast<const uint4 *>(st + S2W_U + wg * 4096 + u_img_off(r, q4));
                 const __half2 *h2 = reinterpret_cast<const __half2 *>(&x);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -662,21 +714,24 @@ __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Para
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
-        if (lane == 0 && warp < 2) {      // round 2: warp 0 Kbar^T U, warp 1 [0 ; P] U
+        if (warp == 0) {                  // round 2: Kbar^T U, then [0 ; P] U
             fence_after_sync();
-            if (warp == 0) {
-                const uint64_t dkb = sdesc(smem_addr(st + S2W_KB), 8192, 1024, LAYOUT_SW128);
+            const uint32_t stb = warp_uniform(smb + (uint32_t)stage * S2W_STAGE);
+            const uint32_t d_a = warp_uniform(acc_a), d_s = warp_uniform(acc_s);
+            const uint64_t dkb = sdesc(stb + S2W_KB, 8192, 1024, LAYOUT_SW128);
+            const uint64_t dpz = sdesc_k_sw128(stb + S2W_PZ);
+            const uint64_t duo = sdesc(smb + S2W_UOP, 128, 1024, LAYOUT_NONE);
+            if (elect_one()) {
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(acc_s, sdesc_add(dkb, 2048 * ks), sdesc_add(d_uop, 256 * ks), id_kb, ks > 0);
+                    mma_f16(d_s, sdesc_add(dkb, 2048 * ks), sdesc_add(duo, 256 * ks), id_kb, ks > 0);
                 mma_commit(&mbar[3]);
-            } else {
-                const uint64_t dpz = sdesc_k_sw128(smem_addr(st + S2W_PZ));
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(acc_a, sdesc_add(dpz, 32 * ks), sdesc_add(d_uop, 256 * ks), id_wq, 1);
+                    mma_f16(d_a, sdesc_add(dpz, 32 * ks), sdesc_add(duo, 256 * ks), id_wq, 1);
                 mma_commit(&mbar[4]);
             }
+            __syncwarp();
         }
         ok = __syncthreads_and(mbar_wait(&mbar[3], i & 1));
         fence_after_sync();
@@ -702,7 +757,22 @@ __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Para
     }
     if (ok) ok = __syncthreads_and(store_o((b - 1 - a) & 1, (uint32_t)(b - 1 - a), prev_t0, prev_L));
 
-    if (!ok && tid == 0) ws_fail(ws_hdr, 2);
+    if (!ok) {
+        // a bounded wait gave up: record it, and let the copies and MMAs this
+        // CTA issued finish (bounded waits) before its shared memory and TMEM
+        // are released
+        __syncthreads();
+        if (tid == 0) {
+            ws_fail(ws_hdr, 2);
+            for (int s2 = 0; s2 < 2; ++s2)
+                if (iss[s2] >= 0) mbar_wait(&mbar[s2], (uint32_t)((iss[s2] >> 1) & 1), 1u << 20);
+        }
+        if (warp == 0) {
+            if (elect_one()) mma_commit(&mbar[5]);
+            __syncwarp();
+            if (lane == 0) mbar_wait(&mbar[5], 0, 1u << 20);
+        }
+    }
 #pragma unroll
     for (int j = 0; j < 32; j += 4)
         *reinterpret_cast<float4 *>(p.S_T + sbase + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);

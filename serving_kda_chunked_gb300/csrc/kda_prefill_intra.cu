@@ -67,8 +67,8 @@ chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int cap,
 //      [K e^g ; Q e^g] and K e^-g for A / P, fp16 K e^g and V for W / U~, the
 //      Q^ and Kbar workspace images; the previous task's W and U~ leave TMEM
 //      for the workspace in two rounds hidden behind it.
-//   4. One M = 128 tf32 MMA group (warps 12-15 issue one channel atom each):
-//      rows 0-63 give A / beta, rows 64-127 give P.  A chunk whose decay
+//   4. One M = 128 tf32 MMA group (16 K steps, one issuer): rows 0-63 give
+//      A / beta, rows 64-127 give P.  A chunk whose decay
 //      exceeds e^80 on some channel would overflow those factors, so it takes
 //      an exact pairwise CUDA-core path instead.
 //   5. T = (I + A)^-1 on CUDA cores by warps 0-5 (fp32, 16 x 16 blocks,
@@ -202,7 +202,10 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
     uint64_t *mbar = reinterpret_cast<uint64_t *>(sGs + 64);   // [0] TMA, [1] A/P, [2] W/U
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 3);
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31;
+    // warp index the compiler knows to be warp-uniform, so that an issuing
+    // warp's branch keeps the MMA operands in uniform registers
+    const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
     int32_t *ws_hdr = reinterpret_cast<int32_t *>(p.ws);
     const int32_t *chunk_base = reinterpret_cast<const int32_t *>(p.ws + WS_HEADER);
     uint8_t *img_base = p.ws + ws_images_offset(p.N);
@@ -210,8 +213,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
 
     if (tid == 0) {
         mbar_init(&mbar[0], 1);
-        mbar_init(&mbar[1], 4);   // four A/P issuers
-        mbar_init(&mbar[2], 2);   // W and U~ issuers
+        mbar_init(&mbar[1], 1);   // A/P MMAs
+        mbar_init(&mbar[2], 1);   // W and U~ MMAs
         mbar_fence_init();
     }
 #ifdef KDA_FAULT_INJECTION
@@ -308,7 +311,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
             for (int hc = 0; hc < 2; ++hc) {
                 const int c0 = col + 8 * hc;
                 *reinterpret_cast<uint4 *>(dst + IMG_W + rc_img_off(r, c0)) = pack8_h(w + 8 * hc);
-                *reinterpret_cast<uint4 *>(dst + IMG_U + (c0 >> 5) * 4096 + r * 64 + (c0 & 31) * 2) =
+                *reinterpret_cast<uint4 *>(dst + IMG_U + (c0 >> 5) * 4096 + u_img_off(r, (c0 & 31) >> 3)) =
                     pack8_h(u + 8 * hc);
             }
         }
@@ -335,7 +338,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
             for (int hc = 0; hc < 2; ++hc) {
                 const int c0 = col + 8 * hc;
                 *reinterpret_cast<uint4 *>(dst + IMG_W + rc_img_off(r, c0)) = pack8_h(w + 8 * hc);
-                *reinterpret_cast<uint4 *>(dst + IMG_U + (c0 >> 5) * 4096 + r * 64 + (c0 & 31) * 2) =
+                *reinterpret_cast<uint4 *>(dst + IMG_U + (c0 >> 5) * 4096 + u_img_off(r, (c0 & 31) >> 3)) =
                     pack8_h(u + 8 * hc);
             }
         }
@@ -402,17 +405,31 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         ok = __syncthreads_and(it == 0 || mbar_wait(&mbar[2], (it - 1) & 1));
         fence_after_sync();
         if (!ok) break;
-        const bool slow = __syncthreads_or(tid >= 384 && -gL[tid & 127] > RANGE_LIMIT);
+        const bool slow = __shfl_sync(0xffffffffu,
+                                      __syncthreads_or(tid >= 384 && -gL[tid & 127] > RANGE_LIMIT),
+                                      0) != 0;
         float dw[16], du[16];
         if (out_prev) drain_issue(0, dw, du);
 
-        // ---- element-wise prep: unit = (row r, channels c0..c0+7) -------------
-        // tf32 operands [K e^g ; Q e^g] and K e^-g for A / P (not on the slow
-        // path), fp16 K e^g and V for W / U~, the Q^ and Kbar workspace images.
+        // ---- element-wise prep in two channel halves: unit = (row r = tid / 8,
+        // channels c0..c0+7, c0 = 64 hh + 8 (tid % 8)).  tf32 operands
+        // [K e^g ; Q e^g] and K e^-g for A / P (not on the slow path), fp16
+        // K e^g and V for W / U~, the Q^ and Kbar workspace images.  Once the
+        // first half's operands are complete, warp 12 issues the A / P MMAs of
+        // channels 0-63; they run while the second half is prepared.
+        const uint32_t smb = warp_uniform(smem_addr(sm));
+        const uint32_t ap_acc = warp_uniform(tmem + AP_COL);
+        const uint64_t ap_da = sdesc_k_sw128(smb + S1_OPA);
+        const uint64_t ap_db = sdesc_k_sw128(smb + S1_OPB);
+        constexpr uint32_t ap_id = idesc(128, 64, FMT_TF32, FMT_TF32, 0, 0);
+        // K step s2 of the A / P product: channel atom s2 / 4, 8 channels per step
+        auto ap_mma = [&](int s2) {
+            mma_tf32(ap_acc, sdesc_add(ap_da, (s2 >> 2) * 16384 + (s2 & 3) * 32),
+                     sdesc_add(ap_db, (s2 >> 2) * 8192 + (s2 & 3) * 32), ap_id, s2 > 0);
+        };
 #pragma unroll 1
-        for (int jj = 0; jj < 2; ++jj) {
-            const int u = tid + K1_THREADS * jj;
-            const int r = u >> 4, c0 = (u & 15) * 8;
+        for (int hh = 0; hh < 2; ++hh) {
+            const int r = tid >> 3, c0 = 64 * hh + (tid & 7) * 8;
             float kf[8], qf[8], vf[8], gm[8], el[8];
             {
                 const uint4 kr = *reinterpret_cast<const uint4 *>(sm + S1_STG_K + r * 256 + c0 * 2);
@@ -459,9 +476,13 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
             *reinterpret_cast<uint4 *>(out + IMG_Q + ioff) = pack8_h(qg);
             *reinterpret_cast<uint4 *>(out + IMG_KT + ioff) = pack8_h(kb);
             if (!slow) {
+                // a unit's 8 channels are two 16-byte chunks of one channel atom;
+                // lanes 4-7 of each row write their chunks in the other order,
+                // so that one store instruction covers distinct bank groups
                 const uint32_t atom = (uint32_t)(c0 >> 5), ch0 = (uint32_t)(c0 & 31) >> 2;
 #pragma unroll
-                for (int hc = 0; hc < 2; ++hc) {
+                for (int hx = 0; hx < 2; ++hx) {
+                    const int hc = hx ^ ((tid >> 2) & 1);
                     const uint32_t cc = ch0 + hc;
                     *reinterpret_cast<float4 *>(sm + S1_OPA + atom * 16384 + sw128_off(r, cc)) =
                         make_float4(kg[4 * hc], kg[4 * hc + 1], kg[4 * hc + 2], kg[4 * hc + 3]);
@@ -471,9 +492,24 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
                         make_float4(kh[4 * hc], kh[4 * hc + 1], kh[4 * hc + 2], kh[4 * hc + 3]);
                 }
             }
-            if (jj == 0 && out_prev) {
-                drain_finish(out_prev, 0, dw, du);
-                drain_issue(1, dw, du);
+            if (hh == 0) {
+                if (out_prev) {
+                    drain_finish(out_prev, 0, dw, du);
+                    drain_issue(1, dw, du);
+                }
+                if (!slow) {   // channels 0-63 of the A / P operands are complete
+                    fence_async_smem();
+                    fence_before_sync();
+                    __syncthreads();
+                    if (warp == K1_ISSUER0) {
+                        fence_after_sync();
+                        if (elect_one()) {
+#pragma unroll
+                            for (int s2 = 0; s2 < 8; ++s2) ap_mma(s2);
+                        }
+                        __syncwarp();
+                    }
+                }
             }
         }
         if (out_prev) drain_finish(out_prev, 1, dw, du);
@@ -482,26 +518,19 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         fence_before_sync();
         __syncthreads();
 
-        // ---- A and P: tf32 MMAs, M = 128 ([K e^g ; Q e^g]), N = 64 (K e^-g).
-        // Issuing one keeps its thread busy for a few hundred cycles, so the
-        // 16 K steps are spread over four issuers (warps 12-15, accumulator =
-        // channel atom); warp 12 then starts the next task's loads (every
-        // staging tile is consumed).  Meanwhile every thread resolves the
-        // task after next.
-        if (!slow && warp >= K1_ISSUER0 && lane == 0) {
-            const int atom = warp - K1_ISSUER0;
+        // ---- A and P: the remaining 8 K steps (channels 64-127), issued by
+        // warp 12's elected lane right after it starts the next task's loads
+        // (every staging tile is consumed); one commit covers all 16.
+        // Meanwhile every thread resolves the task after next.
+        if (!slow && warp == K1_ISSUER0) {
             fence_after_sync();
-            const uint64_t da = sdesc_k_sw128(smem_addr(sm + S1_OPA));
-            const uint64_t db = sdesc_k_sw128(smem_addr(sm + S1_OPB));
-            const uint32_t id = idesc(128, 64, FMT_TF32, FMT_TF32, 0, 0);
+            if (elect_one()) {
+                if (next < ntask) { expect_tma(); tma_kqg(nxt); tma_v(nxt); }
 #pragma unroll
-            for (int s2 = 0; s2 < 4; ++s2) {   // 8 tf32 channels per step
-                const uint32_t wi = s2 * 32;
-                mma_tf32(tmem + AP_COL + 64 * atom, sdesc_add(da, atom * 16384 + wi),
-                         sdesc_add(db, atom * 8192 + wi), id, s2 > 0);
+                for (int s2 = 8; s2 < 16; ++s2) ap_mma(s2);
+                mma_commit(&mbar[1]);
             }
-            mma_commit(&mbar[1]);
-            if (atom == 0 && next < ntask) { expect_tma(); tma_kqg(nxt); tma_v(nxt); }
+            __syncwarp();
         }
         row_params(nxt, next, b_cur, gs_cur);              // consumed next task
         const PosRaw nn_raw = pos_fetch(next + stride);    // finished after the W/U MMA
@@ -517,14 +546,9 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
             {   // warp = (lane quadrant q, 16-column block cb); lane = row
                 const int q = warp & 3, cb = warp >> 2;
                 const int row = 32 * q + lane;
-                float d[16], d1[16], d2[16], d3[16];
+                float d[16];
                 tmem_ld16(tmem_at(tmem, q, AP_COL + 16 * cb), d);
-                tmem_ld16(tmem_at(tmem, q, AP_COL + 64 + 16 * cb), d1);
-                tmem_ld16(tmem_at(tmem, q, AP_COL + 128 + 16 * cb), d2);
-                tmem_ld16(tmem_at(tmem, q, AP_COL + 192 + 16 * cb), d3);
                 tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) d[e] = (d[e] + d1[e]) + (d2[e] + d3[e]);
                 if (row < 64) {
                     const float b = sB[row];
                     float4 *arow = reinterpret_cast<float4 *>(As + row * LD + 16 * cb);
@@ -585,19 +609,22 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         fence_before_sync();
         __syncthreads();
 
-        // ---- W = T' (K e^g), U~ = T' V on tcgen05 (fp16, B operands MN-major);
-        // warp 0 issues W, warp 1 issues U~
-        if (lane == 0 && warp < 2) {
+        // ---- [W | U~] = T' [K e^g | V] on tcgen05 (fp16, M = 64, N = 256: the
+        // two B operands sit side by side as four 64-column MN-major atoms, and
+        // the accumulators side by side in TMEM), issued by warp 0's elected lane
+        if (warp == 0) {
             fence_after_sync();
-            const uint64_t dt = sdesc_k_sw128(smem_addr(sm + S1_TP));
-            const uint64_t db = sdesc(smem_addr(sm + (warp == 0 ? S1_KG16 : S1_V16)), 8192, 1024,
-                                      LAYOUT_SW128);
-            const uint32_t id = idesc(64, 128, FMT_F16, FMT_F16, 0, 1);
-            const uint32_t col = warp == 0 ? W_COL : U_COL;
+            const uint32_t acc_wu = warp_uniform(tmem + W_COL);
+            const uint64_t dt = sdesc_k_sw128(smb + S1_TP);
+            const uint64_t dbwu = sdesc(smb + S1_KG16, 8192, 1024, LAYOUT_SW128);
+            constexpr uint32_t id = idesc(64, 256, FMT_F16, FMT_F16, 0, 1);
+            if (elect_one()) {
 #pragma unroll
-            for (int s2 = 0; s2 < 4; ++s2)
-                mma_f16(tmem + col, sdesc_add(dt, 32 * s2), sdesc_add(db, 2048 * s2), id, s2 > 0);
-            mma_commit(&mbar[2]);   // waited for after the next task's gate scan
+                for (int s2 = 0; s2 < 4; ++s2)
+                    mma_f16(acc_wu, sdesc_add(dt, 32 * s2), sdesc_add(dbwu, 2048 * s2), id, s2 > 0);
+                mma_commit(&mbar[2]);   // waited for after the next task's gate scan
+            }
+            __syncwarp();
         }
         out_prev = out;
         cur = nxt;

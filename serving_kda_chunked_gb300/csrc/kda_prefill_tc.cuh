@@ -66,7 +66,7 @@ constexpr uint32_t IMG_W = 0;          // W   [64 x 128] fp16, K-major SW128 (2 
 constexpr uint32_t IMG_Q = 16384;      // Q^  [64 x 128] fp16, K-major SW128 (2 atoms)
 constexpr uint32_t IMG_KT = 32768;     // Kb [64 x 128] fp16, [r][c] SW128 (MN-major A)
 constexpr uint32_t IMG_P = 49152;      // P   [64 x 64] fp16, K-major SW128
-constexpr uint32_t IMG_U = 57344;      // U~  [4 slices][64][32] fp16
+constexpr uint32_t IMG_U = 57344;      // U~  [4 slices][64][32] fp16 (u_img_off)
 constexpr uint32_t IMG_G = 73728;      // e^gamma_last [128] fp32
 constexpr uint32_t CH_STRIDE = 74240;  // bytes per (chunk, head)
 constexpr int WINDOW_CHUNKS = 2048;    // chunks per K1/K2 window
@@ -95,6 +95,14 @@ __device__ __forceinline__ int find_seq(const int32_t *chunk_base, int N, int c)
     return lo;
 }
 
+// U~ image of one 32-column state slice, [64 rows][32] fp16 (64 bytes a row):
+// byte offset of the 16-byte chunk q (columns 8q..8q+7) of row r.  The chunk
+// index is XOR-ed with bits 1-2 of the row, so that the 16-byte loads of 32
+// consecutive rows (one per lane) hit distinct bank groups.
+__host__ __device__ __forceinline__ uint32_t u_img_off(int r, int q) {
+    return (uint32_t)r * 64u + ((uint32_t)(q ^ ((r >> 1) & 3)) << 4);
+}
+
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
@@ -102,7 +110,7 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 
 // ---- per-chunk kernel: shared-memory layout and parameters ------------------
 constexpr int K1_THREADS = 512;
-constexpr int K1_ISSUER0 = 12;  // warps 12-15 issue the A/P MMAs
+constexpr int K1_ISSUER0 = 12;  // warp 12 issues the A/P MMAs
 constexpr uint32_t S1_STG_K = 0, S1_STG_Q = 16384, S1_STG_V = 32768;  // bf16 [64][128]
 constexpr uint32_t S1_STG_G = 49152;                                  // fp32 [64][128]
 constexpr uint32_t S1_OPA = 81920;    // tf32 [K e^g ; Q e^g]: 4 atoms x 128 rows x 128 B
@@ -120,7 +128,10 @@ constexpr uint32_t S1_TS = S1_OPA + TILE_BYTES;      // T    fp32 [64][LD]
 constexpr uint32_t S1_TT = S1_OPA + 2 * TILE_BYTES;  // T_RR transposed (diagonal blocks)
 constexpr uint32_t S1_FT = S1_OPA + 3 * TILE_BYTES;  // F = T_RR A_RJ, transposed
 static_assert(S1_FT + TILE_BYTES <= S1_KG16, "inverse scratch overlaps the fp16 operands");
-constexpr int AP_COL = 0, W_COL = 256, U_COL = 384;  // TMEM: 4 A/P partials of 64, W, U~
+constexpr int AP_COL = 0, W_COL = 256, U_COL = 384;  // TMEM: A/P (64 columns), W, U~
+// one N = 256 MMA covers W and U~: their B operands (fp16 K e^g, fp16 V) are
+// adjacent 64-column atoms, their accumulators adjacent TMEM columns
+static_assert(S1_V16 == S1_KG16 + 16384 && U_COL == W_COL + 128, "W / U~ operands must be adjacent");
 constexpr float RANGE_LIMIT = 80.f;                   // e^80 stays inside fp32
 
 struct K1Params {
@@ -137,19 +148,22 @@ struct K1Params {
 };
 
 // ---- chain kernel (one 32-column slice per CTA) ------------------------------
-constexpr int K2_THREADS = 128;
+constexpr int K2_THREADS = 160;       // warps 0-3: the state, warp 4: MMA and load issue
+constexpr int K2_ISSUER = 4;
 constexpr uint32_t S2_WQ = 0;          // [W ; Q^] K-major SW128, 2 atoms x 128 rows
 constexpr uint32_t S2_KB = 32768;      // Kbar [r][c] SW128 (MN-major A)
 constexpr uint32_t S2_PZ = 49152;      // [0 ; P] K-major SW128, 128 rows (rows 0-63 zero)
 constexpr uint32_t S2_U = 65536;       // U~ slice [64][32] fp16
 constexpr uint32_t S2_G = 69632;       // e^gamma_last [128] fp32
 constexpr uint32_t S2_STAGE = 70656;   // bytes per stage (multiple of 1024)
-constexpr uint32_t S2_SOP = 2 * S2_STAGE;                 // S fp16, K=128 x N=32, MN-major
+constexpr int S2_NSTAGE = 3;           // chunks in flight: loads run two chunks ahead
+constexpr uint32_t S2_SOP = S2_NSTAGE * S2_STAGE;         // S fp16, K=128 x N=32, MN-major
 constexpr uint32_t S2_UOP = S2_SOP + 8192;                // U fp16, K=64 x N=32, MN-major
 constexpr uint32_t S2_MISC = S2_UOP + 4096;
 constexpr uint32_t S2_BYTES = S2_MISC + 256 + 1024;
 constexpr uint32_t S2_TX = 4 * 8192 + 16384 + 8192 + 4096 + 512;   // bytes landing per stage
-// TMEM set s (0, 1) at column 128 s: D_A +0, D_B +32, D_S +64, D_S2 +96
+// TMEM set s (0, 1) at column 128 s: D_A +0 ([W ; Q^] S, then += [0 ; P] U),
+// D_S +64 (Kbar^T U)
 
 struct K2Params {
     const float *S0;

@@ -54,6 +54,25 @@ __host__ __device__ constexpr uint32_t idesc(uint32_t M, uint32_t N, uint32_t af
            (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// ---- warp-uniform values and one elected lane ---------------------------------
+// tcgen05.mma takes its TMEM address and matrix descriptors from uniform
+// registers.  A value the compiler cannot prove warp-uniform is converted
+// before every MMA, which measured ~150-200 cycles per instruction on GB300;
+// with uniform operands, an unrolled issue loop and one elected lane, eight
+// MMAs issue in ~350 cycles in total.  So every operand of an MMA is passed
+// through warp_uniform() in converged code, and the MMAs are issued inside
+// `if (elect_one())` by the whole (converged) warp's elected lane -- always the
+// same lane, so that its tcgen05.commit tracks every MMA it issued.
+__device__ __forceinline__ uint32_t warp_uniform(uint32_t x) {
+    return __shfl_sync(0xffffffffu, x, 0);
+}
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile("{\n.reg .b32 rx;\n.reg .pred px;\nelect.sync rx|px, 0xffffffff;\n"
+                 "selp.b32 %0, 1, 0, px;\n}" : "=r"(pred));
+    return pred != 0;
+}
+
 // ---- MMA -----------------------------------------------------------------------
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
                                         uint32_t accumulate) {
