@@ -270,14 +270,15 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     //   warps 0-1:      U = U~ - W S (rows 0-63), fp16 operand
     //   warps 2-3:      the O rows of chunk i - 1 (off the critical path)
     //   B2 (all):       U written
+    //   warp 4:         after round 1, the operands of chunk i + 2 into the
+    //                   stage of chunk i - 1 (once chunk i - 1's P U is done)
     //   warp 4:         round 2, D_S = Kbar^T U (4 K steps) -> MB_R2S, then
-    //                   D_A += [0 ; P] U (4 K steps) -> MB_R2O; then the
-    //                   operands of chunk i + 2 into the stage of chunk i - 1
+    //                   D_A += [0 ; P] U (4 K steps) -> MB_R2O
     //   warps 0-3:      S = Diag(e^gamma_last) S + D_S   (after MB_R2S)
     // Round 1 of chunk i completes after every MMA of chunk i - 1 (one
     // issuing thread, whose commits track all its earlier MMAs), so when B2
-    // passes, chunk i - 1's stage and the U operand's previous contents are
-    // free.  Loads therefore run two chunks ahead.
+    // passes, the U operand's previous contents are free.  Loads run two
+    // chunks ahead.
     bool ok = true, bad = false;
     int64_t prev_t0 = 0;
     int prev_L = 0;
@@ -313,6 +314,16 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
                     mma_f16(d_a, sdesc_add(dwq, (s >> 2) * 16384 + (s & 3) * 32),
                             sdesc_add(dso, 256 * s), id_wq, s > 0);
                 mma_commit(&mbar[MB_R1]);
+                // chunk i + 2's operands into the stage of chunk i - 1 (a stage
+                // not used yet when i = 0): its last reader, chunk i - 1's P U,
+                // has completed.  Issued here, where the issuer waits anyway
+                // for the U operand, so that they never delay round 2.
+                if (ch + 2 < b) {
+                    if (i == 0 || mbar_wait(&mbar[MB_R2O], (uint32_t)((i - 1) & 1)))
+                        issue_loads(ch + 2, (i + 2) % S2_NSTAGE);
+                    else
+                        bad = true;
+                }
             }
             __syncwarp();
         } else if (warp < 2) {            // U = U~ - W S for token rows 0-63
@@ -369,7 +380,6 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
                 for (int s = 0; s < 4; ++s)
                     mma_f16(d_a, sdesc_add(dpz, 32 * s), sdesc_add(duo, 256 * s), id_wq, 1);
                 mma_commit(&mbar[MB_R2O]);
-                if (ch + 2 < b) issue_loads(ch + 2, (i + 2) % S2_NSTAGE);
             }
             __syncwarp();
         } else {                          // S = Diag(e^gamma_last) S + Kbar^T U

@@ -417,15 +417,26 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         // K e^g and V for W / U~, the Q^ and Kbar workspace images.  Once the
         // first half's operands are complete, warp 12 issues the A / P MMAs of
         // channels 0-63; they run while the second half is prepared.
-        const uint32_t smb = warp_uniform(smem_addr(sm));
-        const uint32_t ap_acc = warp_uniform(tmem + AP_COL);
-        const uint64_t ap_da = sdesc_k_sw128(smb + S1_OPA);
-        const uint64_t ap_db = sdesc_k_sw128(smb + S1_OPB);
-        constexpr uint32_t ap_id = idesc(128, 64, FMT_TF32, FMT_TF32, 0, 0);
-        // K step s2 of the A / P product: channel atom s2 / 4, 8 channels per step
-        auto ap_mma = [&](int s2) {
-            mma_tf32(ap_acc, sdesc_add(ap_da, (s2 >> 2) * 16384 + (s2 & 3) * 32),
-                     sdesc_add(ap_db, (s2 >> 2) * 8192 + (s2 & 3) * 32), ap_id, s2 > 0);
+        // K steps [s0, s0 + 8) of the A / P product (channel atom s2 / 4, 8
+        // channels per step), from warp 12's elected lane; the second group
+        // first starts the next task's loads and ends with the commit
+        auto issue_ap = [&](int s0) {
+            fence_after_sync();
+            const uint32_t smb = warp_uniform(smem_addr(sm));
+            const uint32_t acc = warp_uniform(tmem + AP_COL);
+            const uint64_t da = sdesc_k_sw128(smb + S1_OPA);
+            const uint64_t db = sdesc_k_sw128(smb + S1_OPB);
+            constexpr uint32_t id = idesc(128, 64, FMT_TF32, FMT_TF32, 0, 0);
+            if (elect_one()) {
+                if (s0 > 0 && next < ntask) { expect_tma(); tma_kqg(nxt); tma_v(nxt); }
+#pragma unroll
+                for (int s2 = 0; s2 < 8; ++s2)
+                    mma_tf32(acc, sdesc_add(da, ((s0 + s2) >> 2) * 16384 + ((s0 + s2) & 3) * 32),
+                             sdesc_add(db, ((s0 + s2) >> 2) * 8192 + ((s0 + s2) & 3) * 32), id,
+                             s0 + s2 > 0);
+                if (s0 > 0) mma_commit(&mbar[1]);
+            }
+            __syncwarp();
         };
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {
@@ -480,16 +491,23 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
                 // lanes 4-7 of each row write their chunks in the other order,
                 // so that one store instruction covers distinct bank groups
                 const uint32_t atom = (uint32_t)(c0 >> 5), ch0 = (uint32_t)(c0 & 31) >> 2;
+                const bool swap = (tid >> 2) & 1;
+                const float4 kg0 = make_float4(kg[0], kg[1], kg[2], kg[3]);
+                const float4 kg1 = make_float4(kg[4], kg[5], kg[6], kg[7]);
+                const float4 qg0 = make_float4(qg[0], qg[1], qg[2], qg[3]);
+                const float4 qg1 = make_float4(qg[4], qg[5], qg[6], qg[7]);
+                const float4 kh0 = make_float4(kh[0], kh[1], kh[2], kh[3]);
+                const float4 kh1 = make_float4(kh[4], kh[5], kh[6], kh[7]);
 #pragma unroll
                 for (int hx = 0; hx < 2; ++hx) {
-                    const int hc = hx ^ ((tid >> 2) & 1);
-                    const uint32_t cc = ch0 + hc;
+                    const bool second = (hx == 1) != swap;   // chunk ch0 + 1 of the unit
+                    const uint32_t cc = ch0 + (second ? 1u : 0u);
                     *reinterpret_cast<float4 *>(sm + S1_OPA + atom * 16384 + sw128_off(r, cc)) =
-                        make_float4(kg[4 * hc], kg[4 * hc + 1], kg[4 * hc + 2], kg[4 * hc + 3]);
+                        second ? kg1 : kg0;
                     *reinterpret_cast<float4 *>(sm + S1_OPA + atom * 16384 + sw128_off(64 + r, cc)) =
-                        make_float4(qg[4 * hc], qg[4 * hc + 1], qg[4 * hc + 2], qg[4 * hc + 3]);
+                        second ? qg1 : qg0;
                     *reinterpret_cast<float4 *>(sm + S1_OPB + atom * 8192 + sw128_off(r, cc)) =
-                        make_float4(kh[4 * hc], kh[4 * hc + 1], kh[4 * hc + 2], kh[4 * hc + 3]);
+                        second ? kh1 : kh0;
                 }
             }
             if (hh == 0) {
@@ -501,14 +519,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
                     fence_async_smem();
                     fence_before_sync();
                     __syncthreads();
-                    if (warp == K1_ISSUER0) {
-                        fence_after_sync();
-                        if (elect_one()) {
-#pragma unroll
-                            for (int s2 = 0; s2 < 8; ++s2) ap_mma(s2);
-                        }
-                        __syncwarp();
-                    }
+                    if (warp == K1_ISSUER0) issue_ap(0);
                 }
             }
         }
@@ -522,16 +533,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         // warp 12's elected lane right after it starts the next task's loads
         // (every staging tile is consumed); one commit covers all 16.
         // Meanwhile every thread resolves the task after next.
-        if (!slow && warp == K1_ISSUER0) {
-            fence_after_sync();
-            if (elect_one()) {
-                if (next < ntask) { expect_tma(); tma_kqg(nxt); tma_v(nxt); }
-#pragma unroll
-                for (int s2 = 8; s2 < 16; ++s2) ap_mma(s2);
-                mma_commit(&mbar[1]);
-            }
-            __syncwarp();
-        }
+        if (!slow && warp == K1_ISSUER0) issue_ap(8);
         row_params(nxt, next, b_cur, gs_cur);              // consumed next task
         const PosRaw nn_raw = pos_fetch(next + stride);    // finished after the W/U MMA
 
@@ -614,6 +616,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         // the accumulators side by side in TMEM), issued by warp 0's elected lane
         if (warp == 0) {
             fence_after_sync();
+            const uint32_t smb = warp_uniform(smem_addr(sm));
             const uint32_t acc_wu = warp_uniform(tmem + W_COL);
             const uint64_t dt = sdesc_k_sw128(smb + S1_TP);
             const uint64_t dbwu = sdesc(smb + S1_KG16, 8192, 1024, LAYOUT_SW128);
