@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     const uint32_t smb = warp_uniform(smem_addr(sm));
 
     auto issue_loads = [&](int ch, int stage) {
-        const uint8_t *src = img_base + ((uint64_t)(ch - p.w0) * H + h) * CH_STRIDE;
+        const uint8_t *src = img_base + ((uint64_t)(ch - p.img0) * H + h) * CH_STRIDE;
         uint8_t *dst = sm + stage * S2_STAGE;
         uint64_t *mb = &mbar[stage];
         iss[stage] = ch - a;
@@ -499,36 +499,41 @@ __global__ void __launch_bounds__(COMB_THREADS) segment_combine_kernel(float *sm
 }
 
 // ------------------------------------------------------------------------------
-// K2, wide form: one CTA of 512 threads per (sequence, head), for batches
-// with more chains than the GPU runs at once.  Warpgroup s (warps 4s..4s+3)
-// owns state columns 32s..32s+31; its thread t (0..127) holds row t (a dk
-// channel) of those columns in fp32 registers.  Every MMA spans the whole
-// state (N = 128), so one SM carries a whole head.  Per chunk:
-//   round 1: A_s = [W ; Q^] S           (M = 128, K = dk; rows 0-63 W S,
-//            64-127 Q^ S)
-//   U = U~ - W S (fp16)                (rows 0-63: warps 0-1 of every warpgroup)
-//   round 2: B_s' = Kbar^T U           (M = 128, K = 64; committed on its own)
-//            A_s += [0 ; P] U          (rows 64-127 of A_s then hold O)
-//   S = Diag(e^gamma_last) S + B_s'.
-// All MMAs are issued by warp 0's elected lane.  TMEM holds two 128-column
-// accumulators per set; chunk c uses set s = c % 2 for round 1 and the other
-// set's B for Kbar^T U.  Operand images arrive with bulk async copies, double
-// buffered; a stage is reloaded once the next chunk's round 1 is issued, when
-// its last reader (the P U MMA) has long finished.
+// K2, wide form: one CTA per (sequence, head) carrying all 128 state
+// columns, for batches with more chains than the GPU runs at once and for the
+// state chain that runs beside the per-chunk kernel.  544 threads: warpgroup
+// s (warps 4s..4s+3) owns state columns 32s..32s+31, its thread t (0..127)
+// row t (a dk channel) of those columns in fp32 registers; warp 16 issues the
+// MMAs and the operand loads.  Every MMA spans the whole state (N = 128), so
+// one SM carries a whole head in about the period of one 32-column slice.
+// Per chunk i (stage and TMEM set i % 2; D_A = set columns 0-127, D_S = set
+// columns 128-255):
+//   B1 (all):         S (fp16 operand) written, chunk i's operands landed
+//   warp 16:          round 1, D_A = [W ; Q^] S (8 K steps) -> MB_R1; then
+//                     chunk i + 1's operands into the stage of chunk i - 1,
+//                     once that chunk's P U (its last reader) has completed
+//   rows 0-63:        U = U~ - W S, fp16 operand
+//   rows 64-127:      the O rows of chunk i - 1
+//   B2 (all):         U written
+//   warp 16:          round 2, D_S = Kbar^T U (4 K steps) -> MB_R2S, then
+//                     D_A += [0 ; P] U (4 K steps) -> MB_R2O
+//   all state warps:  S = Diag(e^gamma_last) S + D_S   (after MB_R2S)
 __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    // [0..1] loads, [2] round 1, [3] round 2 state, [4] round 2 outputs, [5] drain
+    // [0..1] loads, [2] round 1, [3] round 2 state part, [4] round 2 output part, [5] drain
     uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + S2W_MISC);
+    constexpr int MB_R1 = 2, MB_R2S = 3, MB_R2O = 4, MB_DRAIN = 5;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 6);
     int32_t *iss = reinterpret_cast<int32_t *>(tmem_slot + 1);   // [2] last chunk loaded per stage
 
     const int tid = threadIdx.x, lane = tid & 31;
     const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);   // warp-uniform for the compiler
-    const int wg = warp >> 2, wq = warp & 3;   // column block, TMEM lane quadrant
-    const int row = 32 * wq + lane;            // state row (dk channel) / TMEM lane
-    const int col0 = 32 * wg;                  // first state column of this thread
+    const bool issuer = warp == K2W_ISSUER;
+    const int wg = (warp >> 2) & 3, wq = warp & 3;   // column block, TMEM lane quadrant
+    const int row = 32 * wq + lane;                   // state row (dk channel) / TMEM lane
+    const int col0 = 32 * wg;                         // first state column of this thread
     const int H = p.H;
     const int h = blockIdx.x % H;
     int n = blockIdx.x / H;
@@ -545,7 +550,7 @@ __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Para
     const int a = max(cb, p.w0), b = min(ce, p.w1);
     const int64_t sbase = ((int64_t)n * H + h) * D * D + (int64_t)row * D + col0;
     if (cb == ce) {                       // empty sequence: pass the state through
-        if (p.w0 == 0) {
+        if (p.w0 == 0 && !issuer) {
             for (int j = 0; j < 32; j += 4) {
                 float4 x = p.S0 ? *reinterpret_cast<const float4 *>(p.S0 + sbase + j)
                                 : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -564,8 +569,8 @@ __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Para
         const float *src = (a == cb) ? p.S0 : p.S_T;
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
-            float4 x = src ? *reinterpret_cast<const float4 *>(src + sbase + j)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 x = (src && !issuer) ? *reinterpret_cast<const float4 *>(src + sbase + j)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
             S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
         }
     }
@@ -575,7 +580,7 @@ __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Para
         *reinterpret_cast<uint4 *>(sm + st * S2W_STAGE + S2W_PZ + off) = make_uint4(0u, 0u, 0u, 0u);
     }
     if (tid == 0) {
-        for (int j = 0; j < 6; ++j) mbar_init(&mbar[j], 1);
+        for (int j = 0; j <= MB_DRAIN; ++j) mbar_init(&mbar[j], 1);
         mbar_fence_init();
         iss[0] = iss[1] = -1;
     }
@@ -588,7 +593,7 @@ __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Para
     const uint32_t smb = warp_uniform(smem_addr(sm));
 
     auto issue_loads = [&](int ch, int stage) {
-        const uint8_t *src = img_base + ((uint64_t)(ch - p.w0) * H + h) * CH_STRIDE;
+        const uint8_t *src = img_base + ((uint64_t)(ch - p.img0) * H + h) * CH_STRIDE;
         uint8_t *dst = sm + stage * S2W_STAGE;
         uint64_t *mb = &mbar[stage];
         iss[stage] = ch - a;
@@ -602,156 +607,146 @@ __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Para
         bulk_g2s(dst + S2W_U, src + IMG_U, 16384, mb);
         bulk_g2s(dst + S2W_G, src + IMG_G, 512, mb);
     };
-    if (tid == 0) {
-        issue_loads(a, 0);
-        if (a + 1 < b) issue_loads(a + 1, 1);
+    if (issuer) {                 // chunks a and a + 1 up front
+        if (elect_one()) {
+            issue_loads(a, 0);
+            if (a + 1 < b) issue_loads(a + 1, 1);
+        }
+        __syncwarp();
     }
-    // chunk a + 1 is loaded up front; chunk c + 1 for c > a is loaded during
-    // chunk c (see round 1)
 
-    const uint32_t id_wq = idesc(128, 128, FMT_F16, FMT_F16, 0, 1);
-    const uint32_t id_kb = idesc(128, 128, FMT_F16, FMT_F16, 1, 1);
+    constexpr uint32_t id_wq = idesc(128, 128, FMT_F16, FMT_F16, 0, 1);
+    constexpr uint32_t id_kb = idesc(128, 128, FMT_F16, FMT_F16, 1, 1);
 
-    // O rows of a finished chunk (TMEM lanes 64-127: warps 2-3 of each group)
-    auto store_o = [&](int set, uint32_t phase, int64_t t0, int L) {
-        if (wq >= 2) {
-            const bool done = mbar_wait(&mbar[4], phase & 1);
-            fence_after_sync();
-            float oa[16], ob[16];
-            tmem_ld16(tmem_at(tmem, wq, 256 * set + col0), oa);
-            tmem_ld16(tmem_at(tmem, wq, 256 * set + col0 + 16), ob);
-            tmem_wait_ld();
-            const int r = row - 64;
-            if (done && r < L) {
-                __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * D + col0;
+    // the O rows of a finished chunk (rows 64-127), once its P U MMA has completed
+    auto store_o = [&](int set, int64_t t0, int L, uint32_t pu_parity) -> bool {
+        if (!mbar_wait(&mbar[MB_R2O], pu_parity)) return false;
+        fence_after_sync();
+        float oa[16], ob[16];
+        tmem_ld16(tmem_at(tmem, wq, 256 * set + col0), oa);
+        tmem_ld16(tmem_at(tmem, wq, 256 * set + col0 + 16), ob);
+        tmem_wait_ld();
+        const int r = row - 64;
+        if (r < L) {
+            __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * D + col0;
 #pragma unroll
-                for (int gq = 0; gq < 4; ++gq) {
-                    const float *src = gq < 2 ? oa + 8 * gq : ob + 8 * (gq - 2);
-                    __nv_bfloat162 b0 = __floats2bfloat162_rn(src[0], src[1]);
-                    __nv_bfloat162 b1 = __floats2bfloat162_rn(src[2], src[3]);
-                    __nv_bfloat162 b2 = __floats2bfloat162_rn(src[4], src[5]);
-                    __nv_bfloat162 b3 = __floats2bfloat162_rn(src[6], src[7]);
-                    *reinterpret_cast<uint4 *>(dst + 8 * gq) = make_uint4(
-                        *reinterpret_cast<uint32_t *>(&b0), *reinterpret_cast<uint32_t *>(&b1),
-                        *reinterpret_cast<uint32_t *>(&b2), *reinterpret_cast<uint32_t *>(&b3));
-                }
+            for (int gq = 0; gq < 4; ++gq) {
+                const float *src = gq < 2 ? oa + 8 * gq : ob + 8 * (gq - 2);
+                __nv_bfloat162 b0 = __floats2bfloat162_rn(src[0], src[1]);
+                __nv_bfloat162 b1 = __floats2bfloat162_rn(src[2], src[3]);
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(src[4], src[5]);
+                __nv_bfloat162 b3 = __floats2bfloat162_rn(src[6], src[7]);
+                *reinterpret_cast<uint4 *>(dst + 8 * gq) = make_uint4(
+                    *reinterpret_cast<uint32_t *>(&b0), *reinterpret_cast<uint32_t *>(&b1),
+                    *reinterpret_cast<uint32_t *>(&b2), *reinterpret_cast<uint32_t *>(&b3));
             }
-            return done;
         }
         return true;
     };
 
-    bool ok = true;
+    bool ok = true, bad = false;
     int64_t prev_t0 = 0;
     int prev_L = 0;
     for (int ch = a; ch < b; ++ch) {
         const int i = ch - a, stage = i & 1, set = i & 1;
         uint8_t *st = sm + stage * S2W_STAGE;
-        const uint32_t acc_a = tmem + 256 * set;                          // round 1
-        const uint32_t acc_s = tmem + 256 * (set ^ 1) + 128;              // Kbar^T U
         const int64_t t0 = bos + (int64_t)(ch - cb) * C;
         const int L = (int)((eos - t0) < C ? (eos - t0) : C);
-        ok = __syncthreads_and(mbar_wait(&mbar[stage], (i >> 1) & 1));
+        if (!issuer) {
+            // S (fp16) -> B operand [K = dk][N = 128], MN-major, 128-byte
+            // swizzle: two 64-column atoms of 128 rows x 128 bytes
+#pragma unroll
+            for (int gq = 0; gq < 4; ++gq) {
+                uint4 v4 = make_uint4(pack_h2(S[8 * gq + 0], S[8 * gq + 1]), pack_h2(S[8 * gq + 2], S[8 * gq + 3]),
+                                      pack_h2(S[8 * gq + 4], S[8 * gq + 5]), pack_h2(S[8 * gq + 6], S[8 * gq + 7]));
+                *reinterpret_cast<uint4 *>(sm + S2W_SOP + (wg >> 1) * 16384 +
+                                           sw128_off(row, (wg & 1) * 4 + gq)) = v4;
+            }
+            fence_async_smem();
+        }
+        fence_before_sync();
+        ok = __syncthreads_and(!bad && mbar_wait(&mbar[stage], (uint32_t)((i >> 1) & 1)));
+        fence_after_sync();
         if (!ok) break;
 
-        // S (fp16) -> B operand [K = dk][N = 128], MN-major, no swizzle:
-        // core matrix (8 K rows x 8 N) at (n/8) * 2048 + (k/8) * 128
-#pragma unroll
-        for (int gq = 0; gq < 4; ++gq) {
-            uint4 v4 = make_uint4(pack_h2(S[8 * gq + 0], S[8 * gq + 1]), pack_h2(S[8 * gq + 2], S[8 * gq + 3]),
-                                  pack_h2(S[8 * gq + 4], S[8 * gq + 5]), pack_h2(S[8 * gq + 6], S[8 * gq + 7]));
-            *reinterpret_cast<uint4 *>(sm + S2W_SOP + (4 * wg + gq) * 2048 + (row >> 3) * 128 + (row & 7) * 16) = v4;
-        }
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
-        if (warp == 0) {                  // round 1
-            fence_after_sync();
+        if (issuer) {                     // round 1, then the loads of chunk i + 1
             const uint32_t stb = warp_uniform(smb + (uint32_t)stage * S2W_STAGE);
-            const uint32_t d_a = warp_uniform(acc_a);
+            const uint32_t d_a = warp_uniform(tmem + 256u * (uint32_t)set);
             const uint64_t dwq = sdesc_k_sw128(stb + S2W_WQ);
-            const uint64_t dso = sdesc(smb + S2W_SOP, 128, 2048, LAYOUT_NONE);
+            const uint64_t dso = sdesc(smb + S2W_SOP, 16384, 1024, LAYOUT_SW128);
             if (elect_one()) {
 #pragma unroll
                 for (int s8 = 0; s8 < 8; ++s8)
                     mma_f16(d_a, sdesc_add(dwq, (s8 >> 2) * 16384 + (s8 & 3) * 32),
-                            sdesc_add(dso, 256 * s8), id_wq, s8 > 0);
-                mma_commit(&mbar[2]);
-                // the previous chunk's P U MMA was the last reader of the other
-                // stage: reload it with the chunk after next
+                            sdesc_add(dso, 2048 * s8), id_wq, s8 > 0);
+                mma_commit(&mbar[MB_R1]);
                 if (i > 0 && ch + 1 < b) {
-                    if (mbar_wait(&mbar[4], (i - 1) & 1)) issue_loads(ch + 1, stage ^ 1);
-                    else ws_fail(ws_hdr, 2);
+                    if (mbar_wait(&mbar[MB_R2O], (uint32_t)((i - 1) & 1)))
+                        issue_loads(ch + 1, stage ^ 1);
+                    else
+                        bad = true;
                 }
             }
             __syncwarp();
-        }
-        bool o_ok = true;
-        if (i > 0) o_ok = store_o(set ^ 1, (uint32_t)(i - 1), prev_t0, prev_L);
-        ok = __syncthreads_and(mbar_wait(&mbar[2], i & 1) && o_ok);
-        fence_after_sync();
-        if (!ok) break;
-
-        // U = U~ - W S for token rows 0-63 (warps 0-1 of each group)
-        if (wq < 2) {
+        } else if (wq < 2) {              // U = U~ - W S for token rows 0-63
+            if (!mbar_wait(&mbar[MB_R1], i & 1)) bad = true;
+            fence_after_sync();
             float w0[16], w1[16];
             tmem_ld16(tmem_at(tmem, wq, 256 * set + col0), w0);
             tmem_ld16(tmem_at(tmem, wq, 256 * set + col0 + 16), w1);
             tmem_wait_ld();
-            const int r = row;
             float u[32];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
-                const uint4 x = *reinterpret_cast<const uint4 *>(st + S2W_U + wg * 4096 + u_img_off(r, q4));
+                const uint4 x = *reinterpret_cast<const uint4 *>(st + S2W_U + wg * 4096 + u_img_off(row, q4));
                 const __half2 *h2 = reinterpret_cast<const __half2 *>(&x);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 f = __half22float2(h2[e]);
                     const int j = 8 * q4 + 2 * e;
-                    const float wa = j < 16 ? w0[j] : w1[j - 16];
-                    const float wb = j + 1 < 16 ? w0[j + 1] : w1[j - 15];
-                    u[j] = f.x - wa;
-                    u[j + 1] = f.y - wb;
+                    u[j] = f.x - (j < 16 ? w0[j] : w1[j - 16]);
+                    u[j + 1] = f.y - (j + 1 < 16 ? w0[j + 1] : w1[j - 15]);
                 }
             }
 #pragma unroll
             for (int gq = 0; gq < 4; ++gq) {
                 uint4 v4 = make_uint4(pack_h2(u[8 * gq + 0], u[8 * gq + 1]), pack_h2(u[8 * gq + 2], u[8 * gq + 3]),
                                       pack_h2(u[8 * gq + 4], u[8 * gq + 5]), pack_h2(u[8 * gq + 6], u[8 * gq + 7]));
-                *reinterpret_cast<uint4 *>(sm + S2W_UOP + (4 * wg + gq) * 1024 + (r >> 3) * 128 + (r & 7) * 16) = v4;
+                *reinterpret_cast<uint4 *>(sm + S2W_UOP + (wg >> 1) * 8192 +
+                                           sw128_off(row, (wg & 1) * 4 + gq)) = v4;
             }
+            fence_async_smem();
+        } else if (i > 0) {               // rows 64-127: the previous chunk's outputs
+            if (!store_o(set ^ 1, prev_t0, prev_L, (uint32_t)((i - 1) & 1))) bad = true;
         }
-        fence_async_smem();
+        // B2 (all): U is in shared memory; every thread has seen chunk i - 1's
+        // P U complete before the issuer commits chunk i's
         fence_before_sync();
         __syncthreads();
-        if (warp == 0) {                  // round 2: Kbar^T U, then [0 ; P] U
-            fence_after_sync();
+        fence_after_sync();
+        if (issuer) {                     // round 2
             const uint32_t stb = warp_uniform(smb + (uint32_t)stage * S2W_STAGE);
-            const uint32_t d_a = warp_uniform(acc_a), d_s = warp_uniform(acc_s);
+            const uint32_t d_a = warp_uniform(tmem + 256u * (uint32_t)set);
             const uint64_t dkb = sdesc(stb + S2W_KB, 8192, 1024, LAYOUT_SW128);
             const uint64_t dpz = sdesc_k_sw128(stb + S2W_PZ);
-            const uint64_t duo = sdesc(smb + S2W_UOP, 128, 1024, LAYOUT_NONE);
+            const uint64_t duo = sdesc(smb + S2W_UOP, 8192, 1024, LAYOUT_SW128);
             if (elect_one()) {
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(d_s, sdesc_add(dkb, 2048 * ks), sdesc_add(duo, 256 * ks), id_kb, ks > 0);
-                mma_commit(&mbar[3]);
+                    mma_f16(d_a + 128, sdesc_add(dkb, 2048 * ks), sdesc_add(duo, 2048 * ks), id_kb, ks > 0);
+                mma_commit(&mbar[MB_R2S]);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(d_a, sdesc_add(dpz, 32 * ks), sdesc_add(duo, 256 * ks), id_wq, 1);
-                mma_commit(&mbar[4]);
+                    mma_f16(d_a, sdesc_add(dpz, 32 * ks), sdesc_add(duo, 2048 * ks), id_wq, 1);
+                mma_commit(&mbar[MB_R2O]);
             }
             __syncwarp();
-        }
-        ok = __syncthreads_and(mbar_wait(&mbar[3], i & 1));
-        fence_after_sync();
-        if (!ok) break;
-
-        // S = Diag(e^gamma_last) S + Kbar^T U
-        {
+        } else {                          // S = Diag(e^gamma_last) S + Kbar^T U
+            if (!mbar_wait(&mbar[MB_R2S], i & 1)) bad = true;
+            fence_after_sync();
             float da[16], db[16];
-            tmem_ld16(tmem_at(tmem, wq, 256 * (set ^ 1) + 128 + col0), da);
-            tmem_ld16(tmem_at(tmem, wq, 256 * (set ^ 1) + 128 + col0 + 16), db);
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + 128 + col0), da);
+            tmem_ld16(tmem_at(tmem, wq, 256 * set + 128 + col0 + 16), db);
             tmem_wait_ld();
             const float gl = reinterpret_cast<const float *>(st + S2W_G)[row];
 #pragma unroll
@@ -762,30 +757,37 @@ __global__ void __launch_bounds__(K2W_THREADS, 1) chain_wide_kernel(const K2Para
         }
         prev_t0 = t0;
         prev_L = L;
-        fence_before_sync();
-        __syncthreads();   // every thread is done with this stage's images
     }
-    if (ok) ok = __syncthreads_and(store_o((b - 1 - a) & 1, (uint32_t)(b - 1 - a), prev_t0, prev_L));
+    ok = ok && __syncthreads_and(!bad);
+    // the last chunk's outputs (its P U is the last MMA issued, so TMEM is
+    // idle afterwards)
+    if (ok && !issuer && wq >= 2) {
+        if (!store_o((b - 1 - a) & 1, prev_t0, prev_L, (uint32_t)((b - 1 - a) & 1))) bad = true;
+    }
+    ok = __syncthreads_and(ok && !bad);
 
     if (!ok) {
         // a bounded wait gave up: record it, and let the copies and MMAs this
         // CTA issued finish (bounded waits) before its shared memory and TMEM
         // are released
-        __syncthreads();
         if (tid == 0) {
             ws_fail(ws_hdr, 2);
             for (int s2 = 0; s2 < 2; ++s2)
                 if (iss[s2] >= 0) mbar_wait(&mbar[s2], (uint32_t)((iss[s2] >> 1) & 1), 1u << 20);
         }
-        if (warp == 0) {
-            if (elect_one()) mma_commit(&mbar[5]);
+        if (issuer) {
+            if (elect_one()) {
+                mma_commit(&mbar[MB_DRAIN]);
+                mbar_wait(&mbar[MB_DRAIN], 0, 1u << 20);
+            }
             __syncwarp();
-            if (lane == 0) mbar_wait(&mbar[5], 0, 1u << 20);
         }
     }
+    if (!issuer) {
 #pragma unroll
-    for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4 *>(p.S_T + sbase + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4 *>(p.S_T + sbase + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc<512>(tmem);

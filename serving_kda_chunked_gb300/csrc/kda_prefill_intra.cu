@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
     for (; task < ntask; task += stride, ++it) {
         const int L = cur.L;
         const int next = task + stride;
-        uint8_t *out = img_base + (uint64_t)task * CH_STRIDE;
+        uint8_t *out = img_base + ((uint64_t)(p.w0 - p.img0) * H + (uint64_t)task) * CH_STRIDE;
         if (tid < C) {
             sB[tid] = b_cur;
             sGs[tid] = gs_cur;

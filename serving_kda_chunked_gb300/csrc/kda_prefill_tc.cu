@@ -149,7 +149,14 @@ cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, bo
     p1.beta = a.beta; p1.cu = a.cu_seqlens; p1.ws = ws; p1.N = a.N; p1.H = a.H; p1.T = a.T;
     for (int64_t w0 = 0; w0 < bound; w0 += window) {
         const int64_t w1 = w0 + window;
-        p1.w0 = (int)w0; p1.w1 = (int)w1;
+        p1.w0 = (int)w0; p1.w1 = (int)w1; p1.img0 = (int)w0;
+        const int64_t wch = (bound - w0) < window ? (bound - w0) : window;
+        K2Params p2;
+        p2.S0 = a.S0; p2.S_T = a.S_T; p2.o = (__nv_bfloat16 *)a.o; p2.cu = a.cu_seqlens;
+        p2.ws = ws; p2.N = a.N; p2.H = a.H; p2.T = a.T; p2.w0 = (int)w0; p2.w1 = (int)w1;
+        p2.img0 = (int)w0;
+        p2.nseg = 0; p2.seg_len = 0; p2.phase = 0; p2.smaps = smaps; p2.plan = nullptr;
+        const SegPlan pl = smaps ? segment_plan(a.N, a.H, wch) : SegPlan{0, 0};
         if (a.T > 0) {
             const int64_t tasks = (w1 - w0) * a.H;
             const int g1 = (int)(tasks < nsm ? tasks : nsm);
@@ -157,12 +164,6 @@ cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, bo
             e = cudaGetLastError();
             if (e != cudaSuccess) return e;
         }
-        K2Params p2;
-        p2.S0 = a.S0; p2.S_T = a.S_T; p2.o = (__nv_bfloat16 *)a.o; p2.cu = a.cu_seqlens;
-        p2.ws = ws; p2.N = a.N; p2.H = a.H; p2.T = a.T; p2.w0 = (int)w0; p2.w1 = (int)w1;
-        p2.nseg = 0; p2.seg_len = 0; p2.phase = 0; p2.smaps = smaps; p2.plan = nullptr;
-        const int64_t wch = (bound - w0) < window ? (bound - w0) : window;
-        const SegPlan pl = smaps ? segment_plan(a.N, a.H, wch) : SegPlan{0, 0};
         if (pl.nseg) {            // chunk-affine scan over this window
             p2.nseg = pl.nseg; p2.seg_len = pl.seg_len; p2.phase = 0;
             chain_kernel<<<(unsigned)(a.H * (4 + 8 * (pl.nseg - 1))), K2_THREADS, S2_BYTES, st>>>(p2);

@@ -142,7 +142,8 @@ struct K1Params {
     uint8_t *ws;
     int N, H;
     int64_t T;
-    int w0, w1;
+    int w0, w1;        // chunks [w0, w1) of this launch
+    int img0;          // chunk whose operand images sit at the start of the image area
     int scalar_gate;
     int force_timeout;   // fault-injection test build only (see fault_force_timeout)
 };
@@ -173,7 +174,8 @@ struct K2Params {
     uint8_t *ws;
     int N, H;
     int64_t T;
-    int w0, w1;
+    int w0, w1;        // chunks [w0, w1) of this launch
+    int img0;          // chunk whose operand images sit at the start of the image area
     // chunk-affine scan of one sequence (N = 1), see segment_launch_plan
     int nseg;          // 0: off; else the window's chunks in nseg segments
     int seg_len;       // chunks per segment
@@ -197,19 +199,21 @@ constexpr int COMB_THREADS = 512;
 constexpr int SSH_LD = 40;
 constexpr uint32_t COMB_BYTES = (128 * 129 + 128 * SSH_LD) * sizeof(float);
 // ---- chain kernel, wide form (all 128 columns per CTA) ------------------------
-constexpr int K2W_THREADS = 512;
+constexpr int K2W_THREADS = 544;       // warps 0-15: the state, warp 16: MMA and load issue
+constexpr int K2W_ISSUER = 16;
 constexpr uint32_t S2W_WQ = 0;          // [W ; Q^] K-major SW128, 2 atoms x 128 rows
 constexpr uint32_t S2W_KB = 32768;      // Kbar [r][c] SW128 (MN-major A)
 constexpr uint32_t S2W_PZ = 49152;      // [0 ; P] K-major SW128, 128 rows (rows 0-63 zero)
 constexpr uint32_t S2W_U = 65536;       // U~ [4 column blocks][64][32] fp16
 constexpr uint32_t S2W_G = 81920;       // e^gamma_last [128] fp32
 constexpr uint32_t S2W_STAGE = 82944;   // bytes per stage (multiple of 1024)
-constexpr uint32_t S2W_SOP = 2 * S2W_STAGE;                 // S fp16, K = 128 x N = 128, MN-major
-constexpr uint32_t S2W_UOP = S2W_SOP + 32768;               // U fp16, K = 64 x N = 128, MN-major
+constexpr uint32_t S2W_SOP = 2 * S2W_STAGE;   // S fp16, K = 128 x N = 128, MN-major SW128 (2 atoms of 16 KB)
+constexpr uint32_t S2W_UOP = S2W_SOP + 32768; // U fp16, K = 64 x N = 128, MN-major SW128 (2 atoms of 8 KB)
 constexpr uint32_t S2W_MISC = S2W_UOP + 16384;
 constexpr uint32_t S2W_BYTES = S2W_MISC + 256 + 1024;
 constexpr uint32_t S2W_TX = 4 * 8192 + 16384 + 8192 + 16384 + 512;   // bytes landing per stage
-// TMEM set s (0, 1) at column 256 s: A_s +0, B_s +128
+// TMEM set s (0, 1) at column 256 s: D_A +0 ([W ; Q^] S, then += [0 ; P] U),
+// D_S +128 (Kbar^T U)
 
 
 // ---- kernels -----------------------------------------------------------------
