@@ -367,6 +367,21 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         ok = __syncthreads_and(mbar_wait(&mbar[0], it & 1));
         if (!ok) break;
         ++n_landed;
+        if (L < C) {
+            // the chunk ends inside the tile: rows L..63 become no-op tokens
+            // (k = q = v = 0, g = 0; beta is already 0 there), so that the
+            // scan and the prep need no per-row test
+            const int nrow = C - L;
+            for (int e = tid; e < nrow * 80; e += K1_THREADS) {
+                const int r = L + e / 80, x = e % 80;   // 16-byte pieces: 16 k, 16 q, 16 v, 32 g
+                uint8_t *dst = x < 16 ? sm + S1_STG_K + r * 256 + x * 16
+                             : x < 32 ? sm + S1_STG_Q + r * 256 + (x - 16) * 16
+                             : x < 48 ? sm + S1_STG_V + r * 256 + (x - 32) * 16
+                                      : sm + S1_STG_G + r * 512 + (x - 48) * 16;
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncthreads();
+        }
 
         // ---- cumulative log-gate, in place (rows past the sequence: g = 0) ----
         // thread = (channel c, 16-row segment sg)
@@ -384,7 +399,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
             float acc = 0.f;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                acc += 16 * sg + j < L ? v[j] : 0.f;
+                acc += v[j];
                 v[j] = acc;
             }
             tot[sg * 128 + c] = acc;
@@ -449,14 +464,13 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
                 const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kr);
                 const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qr);
                 const __nv_bfloat162 *v2 = reinterpret_cast<const __nv_bfloat162 *>(&vr);
-                const bool live = r < L;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 a = __bfloat1622float2(k2[e]), b2 = __bfloat1622float2(q2[e]),
                                  c2 = __bfloat1622float2(v2[e]);
-                    kf[2 * e] = live ? a.x : 0.f; kf[2 * e + 1] = live ? a.y : 0.f;
-                    qf[2 * e] = live ? b2.x : 0.f; qf[2 * e + 1] = live ? b2.y : 0.f;
-                    vf[2 * e] = live ? c2.x : 0.f; vf[2 * e + 1] = live ? c2.y : 0.f;
+                    kf[2 * e] = a.x; kf[2 * e + 1] = a.y;
+                    qf[2 * e] = b2.x; qf[2 * e + 1] = b2.y;
+                    vf[2 * e] = c2.x; vf[2 * e + 1] = c2.y;
                 }
                 const float4 g0 = *reinterpret_cast<const float4 *>(sm + S1_STG_G + r * 512 + c0 * 4);
                 const float4 g1 = *reinterpret_cast<const float4 *>(sm + S1_STG_G + r * 512 + c0 * 4 + 16);
@@ -539,12 +553,12 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
 
         float *As = reinterpret_cast<float *>(sm + S1_AS);
         if (!slow) {
-            if (tid == 0 && next < ntask) ++n_issued;
             fence_before_sync();
             ok = __syncthreads_and(mbar_wait(&mbar[1], ap_it & 1));
             ++ap_it;
             fence_after_sync();
             if (!ok) break;
+            if (tid == 0 && next < ntask) ++n_issued;
             {   // warp = (lane quadrant q, 16-column block cb); lane = row
                 const int q = warp & 3, cb = warp >> 2;
                 const int row = 32 * q + lane;
