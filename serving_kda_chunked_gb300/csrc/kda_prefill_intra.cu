@@ -289,13 +289,23 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
     auto expect_tma = [&]() {
         mbar_arrive_expect_tx(&mbar[0], 3 * TILE_BF16 + (p.scalar_gate ? 0 : TILE_G));
     };
+    // boxes of 128 bytes of channels: two per bf16 tile, four per fp32 tile
     auto tma_kqg = [&](const Pos &q) {
-        tma_load_3d(sm + S1_STG_K, &p.tm_k, 0, q.h, (int)q.t0, &mbar[0]);
-        tma_load_3d(sm + S1_STG_Q, &p.tm_q, 0, q.h, (int)q.t0, &mbar[0]);
-        if (!p.scalar_gate) tma_load_3d(sm + S1_STG_G, &p.tm_g, 0, q.h, (int)q.t0, &mbar[0]);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            tma_load_3d(sm + S1_STG_K + 8192 * b, &p.tm_k, 64 * b, q.h, (int)q.t0, &mbar[0]);
+            tma_load_3d(sm + S1_STG_Q + 8192 * b, &p.tm_q, 64 * b, q.h, (int)q.t0, &mbar[0]);
+        }
+        if (!p.scalar_gate) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                tma_load_3d(sm + S1_STG_G + 8192 * b, &p.tm_g, 32 * b, q.h, (int)q.t0, &mbar[0]);
+        }
     };
     auto tma_v = [&](const Pos &q) {
-        tma_load_3d(sm + S1_STG_V, &p.tm_v, 0, q.h, (int)q.t0, &mbar[0]);
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+            tma_load_3d(sm + S1_STG_V + 8192 * b, &p.tm_v, 64 * b, q.h, (int)q.t0, &mbar[0]);
     };
     // W and U~ of a finished task: TMEM -> fp16 workspace images.  Row r of
     // the M = 64 accumulators sits in lane r % 16 of quadrant r / 16; a warp
@@ -371,14 +381,16 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
             // the chunk ends inside the tile: rows L..63 become no-op tokens
             // (k = q = v = 0, g = 0; beta is already 0 there), so that the
             // scan and the prep need no per-row test
+            // (a token row is one 128-byte line in each of the ten boxes)
             const int nrow = C - L;
             for (int e = tid; e < nrow * 80; e += K1_THREADS) {
-                const int r = L + e / 80, x = e % 80;   // 16-byte pieces: 16 k, 16 q, 16 v, 32 g
-                uint8_t *dst = x < 16 ? sm + S1_STG_K + r * 256 + x * 16
-                             : x < 32 ? sm + S1_STG_Q + r * 256 + (x - 16) * 16
-                             : x < 48 ? sm + S1_STG_V + r * 256 + (x - 32) * 16
-                                      : sm + S1_STG_G + r * 512 + (x - 48) * 16;
-                *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+                const int r = L + e / 80, bx = (e % 80) >> 3, x = e & 7;
+                const uint32_t box = bx < 2 ? S1_STG_K + 8192 * bx
+                                   : bx < 4 ? S1_STG_Q + 8192 * (bx - 2)
+                                   : bx < 6 ? S1_STG_V + 8192 * (bx - 4)
+                                            : S1_STG_G + 8192 * (bx - 6);
+                *reinterpret_cast<uint4 *>(sm + box + (r >> 3) * 1024 + (r & 7) * 128 + x * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
             }
             __syncthreads();
         }
@@ -387,14 +399,16 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         // thread = (channel c, 16-row segment sg)
         {
             const int c = tid & 127, sg = tid >> 7;
-            float *G = reinterpret_cast<float *>(sm + S1_STG_G);
+            auto G = [&](int r) -> float & {
+                return *reinterpret_cast<float *>(sm + S1_STG_G + stg32_off(r, c));
+            };
             float v[16];
             if (p.scalar_gate) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] = sGs[16 * sg + j];
             } else {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = G[(16 * sg + j) * 128 + c];
+                for (int j = 0; j < 16; ++j) v[j] = G(16 * sg + j);
             }
             float acc = 0.f;
 #pragma unroll
@@ -407,7 +421,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
             float off = 0.f;
             for (int s2 = 0; s2 < sg; ++s2) off += tot[s2 * 128 + c];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) G[(16 * sg + j) * 128 + c] = v[j] + off;
+            for (int j = 0; j < 16; ++j) G(16 * sg + j) = v[j] + off;
             if (sg == 3) {
                 gL[c] = acc + off;
                 eL[c] = __expf(acc + off);
@@ -426,128 +440,124 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         float dw[16], du[16];
         if (out_prev) drain_issue(0, dw, du);
 
-        // ---- element-wise prep in two channel halves: unit = (row r = tid / 8,
-        // channels c0..c0+7, c0 = 64 hh + 8 (tid % 8)).  tf32 operands
-        // [K e^g ; Q e^g] and K e^-g for A / P (not on the slow path), fp16
-        // K e^g and V for W / U~, the Q^ and Kbar workspace images.  Once the
-        // first half's operands are complete, warp 12 issues the A / P MMAs of
-        // channels 0-63; they run while the second half is prepared.
-        // K steps [s0, s0 + 8) of the A / P product (channel atom s2 / 4, 8
-        // channels per step), from warp 12's elected lane; the second group
-        // first starts the next task's loads and ends with the commit
-        auto issue_ap = [&](int s0) {
-            fence_after_sync();
-            const uint32_t smb = warp_uniform(smem_addr(sm));
-            const uint32_t acc = warp_uniform(tmem + AP_COL);
-            const uint64_t da = sdesc_k_sw128(smb + S1_OPA);
-            const uint64_t db = sdesc_k_sw128(smb + S1_OPB);
-            constexpr uint32_t id = idesc(128, 64, FMT_TF32, FMT_TF32, 0, 0);
-            if (elect_one()) {
-                if (s0 > 0 && next < ntask) { expect_tma(); tma_kqg(nxt); tma_v(nxt); }
+        // ---- element-wise prep, one token row of 32 channels per thread: warp
+        // w owns TMEM lane quadrant w % 4 -- rows 32 (w % 4) .. + 31 of the
+        // M = 128 A operand [K e^g ; Q e^g] -- and channels 32 (w / 4) .. + 31,
+        // in two passes of 16 channels.  K rows (lanes 0-63, token t = lane):
+        // K e^g into the TMEM operand and the fp16 W operand, V into the fp16
+        // U~ operand.  Q rows (lanes 64-127, token t = lane - 64): Q e^g into
+        // the TMEM operand and the Q^ image, and for the same token K e^-g (the
+        // tf32 B operand of A / P, not on the slow path) and the Kbar image.
+        // A warp's 32 lanes read and write 32 consecutive token rows at one
+        // 16-byte chunk position, which the 128-byte swizzle spreads over all
+        // banks.
+        {
+            const int quad = warp & 3, cq = warp >> 2;
+            const int rr = 32 * quad + lane;
+            const bool krow = rr < 64;
+            const int t = krow ? rr : rr - 64;
+            float aop[32];
 #pragma unroll
-                for (int s2 = 0; s2 < 8; ++s2)
-                    mma_tf32(acc, sdesc_add(da, ((s0 + s2) >> 2) * 16384 + ((s0 + s2) & 3) * 32),
-                             sdesc_add(db, ((s0 + s2) >> 2) * 8192 + ((s0 + s2) & 3) * 32), id,
-                             s0 + s2 > 0);
-                if (s0 > 0) mma_commit(&mbar[1]);
-            }
-            __syncwarp();
-        };
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-            const int r = tid >> 3, c0 = 64 * hh + (tid & 7) * 8;
-            float kf[8], qf[8], vf[8], gm[8], el[8];
-            {
-                const uint4 kr = *reinterpret_cast<const uint4 *>(sm + S1_STG_K + r * 256 + c0 * 2);
-                const uint4 qr = *reinterpret_cast<const uint4 *>(sm + S1_STG_Q + r * 256 + c0 * 2);
-                const uint4 vr = *reinterpret_cast<const uint4 *>(sm + S1_STG_V + r * 256 + c0 * 2);
-                const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kr);
-                const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qr);
-                const __nv_bfloat162 *v2 = reinterpret_cast<const __nv_bfloat162 *>(&vr);
+            for (int hp = 0; hp < 2; ++hp) {
+                const int c0 = 32 * cq + 16 * hp;        // first channel of this pass
+                float gm[16], x[16];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 a = __bfloat1622float2(k2[e]), b2 = __bfloat1622float2(q2[e]),
-                                 c2 = __bfloat1622float2(v2[e]);
-                    kf[2 * e] = a.x; kf[2 * e + 1] = a.y;
-                    qf[2 * e] = b2.x; qf[2 * e + 1] = b2.y;
-                    vf[2 * e] = c2.x; vf[2 * e + 1] = c2.y;
+                for (int j = 0; j < 4; ++j) {
+                    const float4 g4 = *reinterpret_cast<const float4 *>(
+                        sm + S1_STG_G + stg32_off(t, c0 + 4 * j));
+                    gm[4 * j] = g4.x; gm[4 * j + 1] = g4.y; gm[4 * j + 2] = g4.z; gm[4 * j + 3] = g4.w;
                 }
-                const float4 g0 = *reinterpret_cast<const float4 *>(sm + S1_STG_G + r * 512 + c0 * 4);
-                const float4 g1 = *reinterpret_cast<const float4 *>(sm + S1_STG_G + r * 512 + c0 * 4 + 16);
-                gm[0] = g0.x; gm[1] = g0.y; gm[2] = g0.z; gm[3] = g0.w;
-                gm[4] = g1.x; gm[5] = g1.y; gm[6] = g1.z; gm[7] = g1.w;
-                const float4 e0 = *reinterpret_cast<const float4 *>(eL + c0);
-                const float4 e1 = *reinterpret_cast<const float4 *>(eL + c0 + 4);
-                el[0] = e0.x; el[1] = e0.y; el[2] = e0.z; el[3] = e0.w;
-                el[4] = e1.x; el[5] = e1.y; el[6] = e1.z; el[7] = e1.w;
-            }
-            float kg[8], qg[8], kh[8], kb[8];
+                auto load16 = [&](uint32_t tile, float (&dst)[16]) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float ep = __expf(gm[e]);
-                kg[e] = kf[e] * ep;
-                qg[e] = qf[e] * ep;
-                if (!slow) {   // e^-gamma <= e^80 here: Kbar = (K e^-g) e^gamma_last
-                    kh[e] = kf[e] * __expf(-gm[e]);
-                    kb[e] = kh[e] * el[e];
+                    for (int j = 0; j < 2; ++j) {
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(
+                            sm + tile + stg16_off(t, c0 + 8 * j));
+                        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __bfloat1622float2(b2[e]);
+                            dst[8 * j + 2 * e] = f.x;
+                            dst[8 * j + 2 * e + 1] = f.y;
+                        }
+                    }
+                };
+                load16(krow ? S1_STG_K : S1_STG_Q, x);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) aop[16 * hp + e] = x[e] * __expf(gm[e]);
+                if (krow) {
+                    // fp16 K e^g: B operand of W = T' (K e^g)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        *reinterpret_cast<uint4 *>(sm + S1_KG16 + rc_img_off(t, c0 + 8 * j)) =
+                            pack8_h(aop + 16 * hp + 8 * j);
+                    // fp16 V: B operand of U~ = T' V
+                    load16(S1_STG_V, x);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        *reinterpret_cast<uint4 *>(sm + S1_V16 + rc_img_off(t, c0 + 8 * j)) =
+                            pack8_h(x + 8 * j);
                 } else {
-                    kh[e] = 0.f;
-                    kb[e] = kf[e] * __expf(gL[c0 + e] - gm[e]);
-                }
-            }
-            const uint32_t ioff = rc_img_off(r, c0);
-            *reinterpret_cast<uint4 *>(sm + S1_KG16 + ioff) = pack8_h(kg);
-            *reinterpret_cast<uint4 *>(sm + S1_V16 + ioff) = pack8_h(vf);
-            *reinterpret_cast<uint4 *>(out + IMG_Q + ioff) = pack8_h(qg);
-            *reinterpret_cast<uint4 *>(out + IMG_KT + ioff) = pack8_h(kb);
-            if (!slow) {
-                // a unit's 8 channels are two 16-byte chunks of one channel atom;
-                // lanes 4-7 of each row write their chunks in the other order,
-                // so that one store instruction covers distinct bank groups
-                const uint32_t atom = (uint32_t)(c0 >> 5), ch0 = (uint32_t)(c0 & 31) >> 2;
-                const bool swap = (tid >> 2) & 1;
-                const float4 kg0 = make_float4(kg[0], kg[1], kg[2], kg[3]);
-                const float4 kg1 = make_float4(kg[4], kg[5], kg[6], kg[7]);
-                const float4 qg0 = make_float4(qg[0], qg[1], qg[2], qg[3]);
-                const float4 qg1 = make_float4(qg[4], qg[5], qg[6], qg[7]);
-                const float4 kh0 = make_float4(kh[0], kh[1], kh[2], kh[3]);
-                const float4 kh1 = make_float4(kh[4], kh[5], kh[6], kh[7]);
 #pragma unroll
-                for (int hx = 0; hx < 2; ++hx) {
-                    const bool second = (hx == 1) != swap;   // chunk ch0 + 1 of the unit
-                    const uint32_t cc = ch0 + (second ? 1u : 0u);
-                    *reinterpret_cast<float4 *>(sm + S1_OPA + atom * 16384 + sw128_off(r, cc)) =
-                        second ? kg1 : kg0;
-                    *reinterpret_cast<float4 *>(sm + S1_OPA + atom * 16384 + sw128_off(64 + r, cc)) =
-                        second ? qg1 : qg0;
-                    *reinterpret_cast<float4 *>(sm + S1_OPB + atom * 8192 + sw128_off(r, cc)) =
-                        second ? kh1 : kh0;
+                    for (int j = 0; j < 2; ++j)
+                        *reinterpret_cast<uint4 *>(out + IMG_Q + rc_img_off(t, c0 + 8 * j)) =
+                            pack8_h(aop + 16 * hp + 8 * j);
+                    // K e^-g and Kbar = K e^(gamma_last - gamma) of token t
+                    load16(S1_STG_K, x);
+                    float kb[16];
+                    if (!slow) {   // e^-gamma <= e^80 here: Kbar = (K e^-g) e^gamma_last
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            x[e] *= __expf(-gm[e]);
+                            kb[e] = x[e] * eL[c0 + e];
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            *reinterpret_cast<float4 *>(sm + S1_OPB + cq * 8192 +
+                                                        sw128_off(t, 4 * hp + j)) =
+                                make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) kb[e] = x[e] * __expf(gL[c0 + e] - gm[e]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        *reinterpret_cast<uint4 *>(out + IMG_KT + rc_img_off(t, c0 + 8 * j)) =
+                            pack8_h(kb + 8 * j);
                 }
-            }
-            if (hh == 0) {
-                if (out_prev) {
+                if (hp == 0 && out_prev) {
                     drain_finish(out_prev, 0, dw, du);
                     drain_issue(1, dw, du);
                 }
-                if (!slow) {   // channels 0-63 of the A / P operands are complete
-                    fence_async_smem();
-                    fence_before_sync();
-                    __syncthreads();
-                    if (warp == K1_ISSUER0) issue_ap(0);
-                }
             }
+            tmem_st32(tmem_at(tmem, quad, AOP_COL + 32 * cq), aop);
         }
         if (out_prev) drain_finish(out_prev, 1, dw, du);
         if (tid < 128) reinterpret_cast<float *>(out + IMG_G)[tid] = eL[tid];
+        tmem_wait_st();
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
 
-        // ---- A and P: the remaining 8 K steps (channels 64-127), issued by
-        // warp 12's elected lane right after it starts the next task's loads
-        // (every staging tile is consumed); one commit covers all 16.
-        // Meanwhile every thread resolves the task after next.
-        if (!slow && warp == K1_ISSUER0) issue_ap(8);
+        // ---- A and P: 16 tf32 K steps of 8 channels, A from TMEM, B (K e^-g)
+        // from shared memory, one accumulator, issued by warp 12's elected lane
+        // right after it starts the next task's loads (every staging tile is
+        // consumed).  Meanwhile every thread resolves the task after next.
+        if (!slow && warp == K1_ISSUER0) {
+            fence_after_sync();
+            const uint32_t acc = warp_uniform(tmem + AP_COL);
+            const uint32_t aop_t = warp_uniform(tmem + AOP_COL);
+            const uint64_t db = sdesc_k_sw128(warp_uniform(smem_addr(sm)) + S1_OPB);
+            constexpr uint32_t id = idesc(128, 64, FMT_TF32, FMT_TF32, 0, 0);
+            if (elect_one()) {
+                if (next < ntask) { expect_tma(); tma_kqg(nxt); tma_v(nxt); }
+#pragma unroll
+                for (int s2 = 0; s2 < 16; ++s2)   // channel atom s2 / 4 of the B operand
+                    mma_tf32_tmem_a(acc, aop_t + 8 * s2,
+                                    sdesc_add(db, (s2 >> 2) * 8192 + (s2 & 3) * 32), id, s2 > 0);
+                mma_commit(&mbar[1]);
+            }
+            __syncwarp();
+        }
         row_params(nxt, next, b_cur, gs_cur);              // consumed next task
         const PosRaw nn_raw = pos_fetch(next + stride);    // finished after the W/U MMA
 
@@ -589,18 +599,21 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
             }
         } else {
             // ---- exact pairwise path for chunks whose decay leaves fp32 range
-            const __nv_bfloat16 *Kb = reinterpret_cast<const __nv_bfloat16 *>(sm + S1_STG_K);
-            const __nv_bfloat16 *Qb = reinterpret_cast<const __nv_bfloat16 *>(sm + S1_STG_Q);
-            const float *Gm = reinterpret_cast<const float *>(sm + S1_STG_G);
+            auto kq = [&](uint32_t tile, int t, int c) {
+                return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                    sm + tile + stg16_off(t, c)));
+            };
+            auto gm = [&](int t, int c) {
+                return *reinterpret_cast<const float *>(sm + S1_STG_G + stg32_off(t, c));
+            };
             for (int e = tid; e < C * C; e += K1_THREADS) {
                 const int r = e >> 6, i = e & 63;
                 float a = 0.f, pp = 0.f;
                 if (i <= r && r < L) {
                     for (int c = 0; c < D; ++c) {
-                        const float ki = __bfloat162float(Kb[i * 128 + c]) *
-                                         __expf(Gm[r * 128 + c] - Gm[i * 128 + c]);
-                        a += __bfloat162float(Kb[r * 128 + c]) * ki;
-                        pp += __bfloat162float(Qb[r * 128 + c]) * ki;
+                        const float ki = kq(S1_STG_K, i, c) * __expf(gm(r, c) - gm(i, c));
+                        a += kq(S1_STG_K, r, c) * ki;
+                        pp += kq(S1_STG_Q, r, c) * ki;
                     }
                 }
                 As[r * LD + i] = i < r ? sB[r] * a : 0.f;

@@ -22,17 +22,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 3D map over a token-major [T][H][128] tensor; one box = 64 tokens of one head.
+// 3D map over a token-major [T][H][128] tensor; one box = 64 tokens of one
+// head by 128 bytes of channels (64 bf16 or 32 fp32), landing with the
+// 128-byte swizzle (16-byte chunk c of token row t at chunk c ^ (t % 8)).
 bool token_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, uint32_t esize, int H,
                int64_t T) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
     cuuint64_t strides[2] = {(cuuint64_t)D * esize, (cuuint64_t)H * D * esize};
-    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)C};
+    cuuint32_t box[3] = {128u / esize, 1, (cuuint32_t)C};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -103,6 +103,17 @@ __host__ __device__ __forceinline__ uint32_t u_img_off(int r, int q) {
     return (uint32_t)r * 64u + ((uint32_t)(q ^ ((r >> 1) & 3)) << 4);
 }
 
+// byte offsets in the staging tiles: token t, channel c of a bf16 tile (boxes
+// of 64 channels) and of an fp32 tile (boxes of 32 channels)
+__host__ __device__ __forceinline__ uint32_t stg16_off(int t, int c) {
+    return (uint32_t)(c >> 6) * 8192u + sw128_off((uint32_t)t, (uint32_t)(c & 63) >> 3) +
+           (uint32_t)(c & 7) * 2u;
+}
+__host__ __device__ __forceinline__ uint32_t stg32_off(int t, int c) {
+    return (uint32_t)(c >> 5) * 8192u + sw128_off((uint32_t)t, (uint32_t)(c & 31) >> 2) +
+           (uint32_t)(c & 3) * 4u;
+}
+
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
@@ -111,9 +122,11 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 // ---- per-chunk kernel: shared-memory layout and parameters ------------------
 constexpr int K1_THREADS = 512;
 constexpr int K1_ISSUER0 = 12;  // warp 12 issues the A/P MMAs
-constexpr uint32_t S1_STG_K = 0, S1_STG_Q = 16384, S1_STG_V = 32768;  // bf16 [64][128]
-constexpr uint32_t S1_STG_G = 49152;                                  // fp32 [64][128]
-constexpr uint32_t S1_OPA = 81920;    // tf32 [K e^g ; Q e^g]: 4 atoms x 128 rows x 128 B
+// staging of one (chunk, head): tiles brought by TMA with 128-byte swizzle, in
+// boxes of 128-byte rows (64 bf16 or 32 fp32 channels) of the 64 tokens
+constexpr uint32_t S1_STG_K = 0, S1_STG_Q = 16384, S1_STG_V = 32768;  // bf16: 2 boxes of 8 KB
+constexpr uint32_t S1_STG_G = 49152;                                  // fp32: 4 boxes of 8 KB
+constexpr uint32_t S1_OPA = 81920;    // scratch of the inverse (A, T, T_RR^T, F)
 constexpr uint32_t S1_OPB = 147456;   // tf32 K e^-g: 4 atoms x 64 rows x 128 B
 constexpr uint32_t S1_KG16 = 180224;  // fp16 K e^g, [r][c] 128B-swizzled (MN-major B)
 constexpr uint32_t S1_V16 = 196608;   // fp16 V, same layout
@@ -128,7 +141,9 @@ constexpr uint32_t S1_TS = S1_OPA + TILE_BYTES;      // T    fp32 [64][LD]
 constexpr uint32_t S1_TT = S1_OPA + 2 * TILE_BYTES;  // T_RR transposed (diagonal blocks)
 constexpr uint32_t S1_FT = S1_OPA + 3 * TILE_BYTES;  // F = T_RR A_RJ, transposed
 static_assert(S1_FT + TILE_BYTES <= S1_KG16, "inverse scratch overlaps the fp16 operands");
-constexpr int AP_COL = 0, W_COL = 256, U_COL = 384;  // TMEM: A/P (64 columns), W, U~
+// TMEM: A/P accumulator (64 columns), the tf32 A operand [K e^g ; Q e^g]
+// (128 columns, one channel each), W, U~
+constexpr int AP_COL = 0, AOP_COL = 128, W_COL = 256, U_COL = 384;
 // one N = 256 MMA covers W and U~: their B operands (fp16 K e^g, fp16 V) are
 // adjacent 64-column atoms, their accumulators adjacent TMEM columns
 static_assert(S1_V16 == S1_KG16 + 16384 && U_COL == W_COL + 128, "W / U~ operands must be adjacent");
