@@ -439,6 +439,15 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
                                       0) != 0;
         float dw[16], du[16];
         if (out_prev) drain_issue(0, dw, du);
+        // the A / P issuer's operands, formed before the prep: after it, the
+        // prep's burst of global stores holds up shuffles for ~1k cycles
+        uint32_t ap_acc = 0, ap_aop = 0;
+        uint64_t ap_db = 0;
+        if (warp == K1_ISSUER0) {
+            ap_acc = warp_uniform(tmem + AP_COL);
+            ap_aop = warp_uniform(tmem + AOP_COL);
+            ap_db = sdesc_k_sw128(warp_uniform(smem_addr(sm)) + S1_OPB);
+        }
 
         // ---- element-wise prep, one token row of 32 channels per thread: warp
         // w owns TMEM lane quadrant w % 4 -- rows 32 (w % 4) .. + 31 of the
@@ -539,22 +548,21 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         __syncthreads();
 
         // ---- A and P: 16 tf32 K steps of 8 channels, A from TMEM, B (K e^-g)
-        // from shared memory, one accumulator, issued by warp 12's elected lane
-        // right after it starts the next task's loads (every staging tile is
+        // from shared memory, one accumulator, issued by warp 12's elected lane,
+        // which then starts the next task's loads (every staging tile is
         // consumed).  Meanwhile every thread resolves the task after next.
         if (!slow && warp == K1_ISSUER0) {
             fence_after_sync();
-            const uint32_t acc = warp_uniform(tmem + AP_COL);
-            const uint32_t aop_t = warp_uniform(tmem + AOP_COL);
-            const uint64_t db = sdesc_k_sw128(warp_uniform(smem_addr(sm)) + S1_OPB);
             constexpr uint32_t id = idesc(128, 64, FMT_TF32, FMT_TF32, 0, 0);
             if (elect_one()) {
-                if (next < ntask) { expect_tma(); tma_kqg(nxt); tma_v(nxt); }
 #pragma unroll
                 for (int s2 = 0; s2 < 16; ++s2)   // channel atom s2 / 4 of the B operand
-                    mma_tf32_tmem_a(acc, aop_t + 8 * s2,
-                                    sdesc_add(db, (s2 >> 2) * 8192 + (s2 & 3) * 32), id, s2 > 0);
+                    mma_tf32_tmem_a(ap_acc, ap_aop + 8 * s2,
+                                    sdesc_add(ap_db, (s2 >> 2) * 8192 + (s2 & 3) * 32), id, s2 > 0);
                 mma_commit(&mbar[1]);
+                // after the MMAs: the copies' issue can wait behind the prep's
+                // global stores, the MMAs' cannot
+                if (next < ntask) { expect_tma(); tma_kqg(nxt); tma_v(nxt); }
             }
             __syncwarp();
         }
