@@ -63,19 +63,20 @@ chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int cap,
 //      has consumed the staging tiles.
 //   2. Per-channel cumulative log-gate (in place), e^gamma_last, range check;
 //      the previous task's W/U MMA finishes underneath.
-//   3. Element-wise prep, 8 channels of one row per unit: tf32 operands
-//      [K e^g ; Q e^g] and K e^-g for A / P, fp16 K e^g and V for W / U~, the
-//      Q^ and Kbar workspace images; the previous task's W and U~ leave TMEM
-//      for the workspace in two rounds hidden behind it.
+//   3. Element-wise prep, one token row of 32 channels per thread: tf32
+//      operands [K e^g ; Q e^g] (into TMEM) and K e^-g for A / P, fp16 K e^g
+//      and V for W / U~, the Q^ and Kbar workspace images.
 //   4. One M = 128 tf32 MMA group (16 K steps, one issuer): rows 0-63 give
 //      A / beta, rows 64-127 give P.  A chunk whose decay
 //      exceeds e^80 on some channel would overflow those factors, so it takes
 //      an exact pairwise CUDA-core path instead.
 //   5. T = (I + A)^-1 on CUDA cores by warps 0-5 (fp32, 16 x 16 blocks,
 //      register-tiled block forward substitution), written as the fp16 image
-//      of T' = T Diag(beta).
-//   6. W = T' (K e^g), U~ = T' V on tcgen05 (fp16), waited for in step 2 of
-//      the next task.
+//      of T' = T Diag(beta).  Meanwhile warps 6-13 move the previous task's
+//      W and U~ from TMEM to the workspace (in the prep, their global stores
+//      slowed it by more than the inverse takes with them).
+//   6. W = T' (K e^g), U~ = T' V on tcgen05 (fp16, issued by warp 12),
+//      waited for in step 2 of the next task.
 __device__ __forceinline__ void tma_load_3d(uint8_t *dst, const CUtensorMap *map, int c0, int c1,
                                             int c2, uint64_t *mbar) {
     asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
@@ -330,30 +331,31 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) store_wu_cols(dst, warp & 3, 32 * (warp >> 2) + 16 * hh);
     };
-    // The same, split so that the TMEM loads' latency overlaps other work:
-    // round hh (0, 1) of warp w covers columns 32 (w / 4) + 16 hh.
-    auto drain_issue = [&](int hh, float (&w)[16], float (&u)[16]) {
-        const int col = 32 * (warp >> 2) + 16 * hh;
-        tmem_ld16(tmem_at(tmem, warp & 3, W_COL + col), w);
-        tmem_ld16(tmem_at(tmem, warp & 3, U_COL + col), u);
-    };
-    auto drain_finish = [&](uint8_t *dst, int hh, float (&w)[16], float (&u)[16]) {
-        tmem_wait_ld();
-        reg_fence(w);
-        reg_fence(u);
-        const int col = 32 * (warp >> 2) + 16 * hh;
+    // W (or U~) of a finished task, the 16 rows of this warp's lane quadrant,
+    // by the warps that sit out the inverse
+    auto drain_half = [&](uint8_t *dst, bool is_u) {
         const int r = 16 * (warp & 3) + lane;
-        if (lane < 16) {
+        const uint32_t col0 = is_u ? U_COL : W_COL;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+            float x[2][16];
+            tmem_ld16(tmem_at(tmem, warp, col0 + c), x[0]);
+            tmem_ld16(tmem_at(tmem, warp, col0 + c + 16), x[1]);
+            tmem_wait_ld();
+            if (lane < 16) {
 #pragma unroll
-            for (int hc = 0; hc < 2; ++hc) {
-                const int c0 = col + 8 * hc;
-                *reinterpret_cast<uint4 *>(dst + IMG_W + rc_img_off(r, c0)) = pack8_h(w + 8 * hc);
-                *reinterpret_cast<uint4 *>(dst + IMG_U + (c0 >> 5) * 4096 + u_img_off(r, (c0 & 31) >> 3)) =
-                    pack8_h(u + 8 * hc);
+                for (int hc = 0; hc < 4; ++hc) {
+                    const int c0 = c + 8 * hc;
+                    const uint4 v = pack8_h(x[hc >> 1] + 8 * (hc & 1));
+                    if (is_u)
+                        *reinterpret_cast<uint4 *>(dst + IMG_U + (c0 >> 5) * 4096 +
+                                                   u_img_off(r, (c0 & 31) >> 3)) = v;
+                    else
+                        *reinterpret_cast<uint4 *>(dst + IMG_W + rc_img_off(r, c0)) = v;
+                }
             }
         }
     };
-
     // positions are resolved one task ahead of the one being loaded, so the
     // offset-table lookups never sit on the critical path
     int task = blockIdx.x;
@@ -428,17 +430,14 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
             }
         }
         // The previous task's W/U MMA ran under the scan; it must be done before
-        // the prep rewrites its B operands and before its results leave TMEM
-        // (this task's W/U MMA reuses the columns), in two rounds hidden behind
-        // the prep.
+        // the prep rewrites its B operands (its results leave TMEM during this
+        // task's inverse, before this task's W/U MMA reuses the columns).
         ok = __syncthreads_and(it == 0 || mbar_wait(&mbar[2], (it - 1) & 1));
         fence_after_sync();
         if (!ok) break;
         const bool slow = __shfl_sync(0xffffffffu,
                                       __syncthreads_or(tid >= 384 && -gL[tid & 127] > RANGE_LIMIT),
                                       0) != 0;
-        float dw[16], du[16];
-        if (out_prev) drain_issue(0, dw, du);
         // the A / P issuer's operands, formed before the prep: after it, the
         // prep's burst of global stores holds up shuffles for ~1k cycles
         uint32_t ap_acc = 0, ap_aop = 0;
@@ -533,14 +532,9 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
                         *reinterpret_cast<uint4 *>(out + IMG_KT + rc_img_off(t, c0 + 8 * j)) =
                             pack8_h(kb + 8 * j);
                 }
-                if (hp == 0 && out_prev) {
-                    drain_finish(out_prev, 0, dw, du);
-                    drain_issue(1, dw, du);
-                }
             }
             tmem_st32(tmem_at(tmem, quad, AOP_COL + 32 * cq), aop);
         }
-        if (out_prev) drain_finish(out_prev, 1, dw, du);
         if (tid < 128) reinterpret_cast<float *>(out + IMG_G)[tid] = eL[tid];
         tmem_wait_st();
         fence_async_smem();
@@ -637,29 +631,40 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         }
         __syncthreads();
 
-        // ---- T = (I + A)^-1 and the fp16 image of T' = T Diag(beta) (warps 0-5)
-        if (warp < 6)
+        // ---- T = (I + A)^-1 and the fp16 image of T' = T Diag(beta) (warps 0-5);
+        // meanwhile warp 12 forms the W / U~ MMA operands (formed right before
+        // the issue, their shuffles wait behind the inverse's stores)
+        uint32_t wu_acc = 0;
+        uint64_t wu_dt = 0, wu_db = 0;
+        if (warp < 6) {
             invert_unit_lower(As, reinterpret_cast<float *>(sm + S1_TS),
                               reinterpret_cast<float *>(sm + S1_TT),
                               reinterpret_cast<float *>(sm + S1_FT), sB, sm + S1_TP, tid);
+        } else {
+            if (warp == K1_ISSUER0) {
+                const uint32_t smb = warp_uniform(smem_addr(sm));
+                wu_acc = warp_uniform(tmem + W_COL);
+                wu_dt = sdesc_k_sw128(smb + S1_TP);
+                wu_db = sdesc(smb + S1_KG16, 8192, 1024, LAYOUT_SW128);
+            }
+            // the previous task's W (warps 6-9) and U~ (warps 10-13) leave
+            // TMEM for the workspace, one lane quadrant per warp
+            if (out_prev && warp < 14) drain_half(out_prev, warp >= 10);
+        }
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
 
         // ---- [W | U~] = T' [K e^g | V] on tcgen05 (fp16, M = 64, N = 256: the
         // two B operands sit side by side as four 64-column MN-major atoms, and
-        // the accumulators side by side in TMEM), issued by warp 0's elected lane
-        if (warp == 0) {
+        // the accumulators side by side in TMEM), issued by warp 12's elected lane
+        if (warp == K1_ISSUER0) {
             fence_after_sync();
-            const uint32_t smb = warp_uniform(smem_addr(sm));
-            const uint32_t acc_wu = warp_uniform(tmem + W_COL);
-            const uint64_t dt = sdesc_k_sw128(smb + S1_TP);
-            const uint64_t dbwu = sdesc(smb + S1_KG16, 8192, 1024, LAYOUT_SW128);
             constexpr uint32_t id = idesc(64, 256, FMT_F16, FMT_F16, 0, 1);
             if (elect_one()) {
 #pragma unroll
                 for (int s2 = 0; s2 < 4; ++s2)
-                    mma_f16(acc_wu, sdesc_add(dt, 32 * s2), sdesc_add(dbwu, 2048 * s2), id, s2 > 0);
+                    mma_f16(wu_acc, sdesc_add(wu_dt, 32 * s2), sdesc_add(wu_db, 2048 * s2), id, s2 > 0);
                 mma_commit(&mbar[2]);   // waited for after the next task's gate scan
             }
             __syncwarp();
