@@ -57,26 +57,29 @@ chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int cap,
 // ------------------------------------------------------------------------------
 // K1: intra-chunk kernel
 // ------------------------------------------------------------------------------
-// One CTA per SM walks (chunk, head) tasks, chunk-major.  Per task:
+// One CTA per SM walks (chunk, head) tasks, chunk-major, two tasks at a time
+// in a software pipeline.  Per task:
 //   1. TMA brings k, q, v (bf16) and g (fp32) rows [t0, t0 + 64) of head h
-//      into staging; issued during the previous task, as soon as its prep
-//      has consumed the staging tiles.
-//   2. Per-channel cumulative log-gate (in place), e^gamma_last, range check;
-//      the previous task's W/U MMA finishes underneath.
-//   3. Element-wise prep, one token row of 32 channels per thread: tf32
-//      operands [K e^g ; Q e^g] (into TMEM) and K e^-g for A / P, fp16 K e^g
-//      and V for W / U~, the Q^ and Kbar workspace images.
-//   4. One M = 128 tf32 MMA group (16 K steps, one issuer): rows 0-63 give
-//      A / beta, rows 64-127 give P.  A chunk whose decay
-//      exceeds e^80 on some channel would overflow those factors, so it takes
-//      an exact pairwise CUDA-core path instead.
-//   5. T = (I + A)^-1 on CUDA cores by warps 0-5 (fp32, 16 x 16 blocks,
+//      into staging, issued as soon as the previous task's prep has consumed
+//      the staging tiles.
+//   2. Per-channel cumulative log-gate (in place), e^gamma_last, range check.
+//   3. Element-wise prep, one token row per thread: tf32 operands
+//      [K e^g ; Q e^g] (into TMEM) and K e^-g for A / P, fp16 K e^g and V for
+//      W / U~ (one buffer per task parity), the Q^ and Kbar workspace images.
+//   4. One M = 128 tf32 MMA group (16 K steps): rows 0-63 give A / beta,
+//      rows 64-127 give P.  A chunk whose decay exceeds e^80 on some channel
+//      would overflow those factors, so it takes an exact pairwise CUDA-core
+//      path instead.
+//   5. A / P leave TMEM (A to shared memory, P to the workspace image), then
+//      T = (I + A)^-1 on CUDA cores by warps 0-5 (fp32, 16 x 16 blocks,
 //      register-tiled block forward substitution), written as the fp16 image
-//      of T' = T Diag(beta).  Meanwhile warps 6-13 move the previous task's
-//      W and U~ from TMEM to the workspace (in the prep, their global stores
-//      slowed it by more than the inverse takes with them).
-//   6. W = T' (K e^g), U~ = T' V on tcgen05 (fp16, issued by warp 12),
-//      waited for in step 2 of the next task.
+//      of T' = T Diag(beta).
+//   6. W = T' (K e^g), U~ = T' V on tcgen05 (fp16), moved from TMEM to the
+//      workspace during the next task's inverse.
+// Steps 2-4 of task k + 1 run on warps 8-15 while warps 0-5 run the inverse
+// of task k and warps 0-7 move task k - 1's W and U~ out; warp 12 issues
+// every MMA and copy.  The inverse then hides the prep's latency instead of
+// adding to it.
 __device__ __forceinline__ void tma_load_3d(uint8_t *dst, const CUtensorMap *map, int c0, int c1,
                                             int c2, uint64_t *mbar) {
     asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
@@ -125,9 +128,16 @@ __device__ __forceinline__ void tp_store1(uint8_t *img, int r, int i, float x) {
 // whole inverse is: diagonal blocks | F | three passes.  Run by warps 0-5
 // only (named barrier 1), leaving the other warps free.  The image's blocks
 // above the diagonal are not written (they hold zeros).
+// Scratch: two 64 x LD fp32 tiles.  A (lower blocks) and T (diagonal and
+// lower blocks) keep their strictly upper blocks free, so F_RI^T goes to A's
+// upper block (I, R) and T_RR^T to one upper block of T (tt_block).
 constexpr int INV_THREADS = 192;
-__device__ __forceinline__ void invert_unit_lower(const float *As, float *Ts, float *Tt, float *Ft,
-                                                  const float *sB, uint8_t *tp_img, int tid) {
+__device__ __forceinline__ float *tt_block(float *Ts, int R) {
+    // R = 0..3 -> blocks (0, 2), (0, 1), (1, 2), (2, 3) of T
+    return Ts + (16 * (R == 0 ? 0 : R - 1)) * LD + 16 * (R == 0 ? 2 : R);
+}
+__device__ __forceinline__ void invert_unit_lower(float *As, float *Ts, const float *sB,
+                                                  uint8_t *tp_img, int tid) {
     const int warp = tid >> 5, lane = tid & 31;
     // diagonal blocks: thread (R, column j) by forward substitution in registers
     if (tid < 64) {
@@ -148,7 +158,7 @@ __device__ __forceinline__ void invert_unit_lower(const float *As, float *Ts, fl
             Ts[(16 * R + m) * LD + 16 * R + j] = x[m];
             tp_store1(tp_img, 16 * R + m, 16 * R + j, x[m] * bj);
         }
-        float4 *trow = reinterpret_cast<float4 *>(Tt + (16 * R + j) * LD + 16 * R);
+        float4 *trow = reinterpret_cast<float4 *>(tt_block(Ts, R) + j * LD);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
             trow[q4] = make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
@@ -161,10 +171,10 @@ __device__ __forceinline__ void invert_unit_lower(const float *As, float *Ts, fl
     const int m0 = 2 * (lane >> 2), n0 = 4 * (lane & 3);
     {   // F_RI = T_RR A_RI, stored transposed
         float f[2][4] = {};
-        mm16_2x4(f, Tt + (16 * R) * LD + 16 * R + m0, As + (16 * R) * LD + 16 * I + n0);
+        mm16_2x4(f, tt_block(Ts, R) + m0, As + (16 * R) * LD + 16 * I + n0);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            *reinterpret_cast<float2 *>(Ft + (16 * I + n0 + e) * LD + 16 * R + m0) =
+            *reinterpret_cast<float2 *>(As + (16 * I + n0 + e) * LD + 16 * R + m0) =
                 make_float2(f[0][e], f[1][e]);
     }
     bar_sync(1, INV_THREADS);
@@ -173,7 +183,7 @@ __device__ __forceinline__ void invert_unit_lower(const float *As, float *Ts, fl
     for (int pass = 0; pass < 3; ++pass) {
         const int J = I + pass;
         if (J < R) {
-            mm16_2x4(acc, Ft + (16 * J) * LD + 16 * R + m0, Ts + (16 * J) * LD + 16 * I + n0);
+            mm16_2x4(acc, As + (16 * J) * LD + 16 * R + m0, Ts + (16 * J) * LD + 16 * I + n0);
             if (J == R - 1) {
                 const float4 b4 = *reinterpret_cast<const float4 *>(sB + 16 * I + n0);
 #pragma unroll
@@ -197,16 +207,20 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
     uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     float *gL = reinterpret_cast<float *>(sm + S1_MISC);   // [128] gamma_last
     float *eL = gL + 128;                                  // [128] e^gamma_last
-    float *sB = eL + 128;                                  // [64] beta
-    float *tot = sB + 64;                                  // [4][128] segment totals
-    float *sGs = tot + 512;                                // [64] scalar gates (scalar_gate)
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(sGs + 64);   // [0] TMA, [1] A/P, [2] W/U
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 3);
+    float *sB2 = eL + 128;                                 // [2][64] beta, by task parity
+    float *tot = sB2 + 128;                                // [2][128] scan segment totals
+    float *sGs = tot + 256;                                // [64] scalar gates (scalar_gate)
+    int32_t *sflag = reinterpret_cast<int32_t *>(sGs + 64);   // [2] out-of-range chunk, by parity
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(sflag + 2);  // [0] TMA, [1] A/P, [2] W/U, [3] drain
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 4);
+    float *As = reinterpret_cast<float *>(sm + S1_AS);
+    float *Ts = reinterpret_cast<float *>(sm + S1_TS);
 
     const int tid = threadIdx.x, lane = tid & 31;
     // warp index the compiler knows to be warp-uniform, so that an issuing
     // warp's branch keeps the MMA operands in uniform registers
     const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
+    const int lt = tid - 256;            // index within warps 8-15 (the prep group)
     int32_t *ws_hdr = reinterpret_cast<int32_t *>(p.ws);
     const int32_t *chunk_base = reinterpret_cast<const int32_t *>(p.ws + WS_HEADER);
     uint8_t *img_base = p.ws + ws_images_offset(p.N);
@@ -216,6 +230,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         mbar_init(&mbar[0], 1);
         mbar_init(&mbar[1], 1);   // A/P MMAs
         mbar_init(&mbar[2], 1);   // W and U~ MMAs
+        mbar_init(&mbar[3], 1);   // drain after a failed wait
         mbar_fence_init();
     }
 #ifdef KDA_FAULT_INJECTION
@@ -248,22 +263,29 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
     const int c_end = min(p.w1, total);
     const int ntask = (c_end > p.w0 ? c_end - p.w0 : 0) * H;
     const int stride = gridDim.x;
+    // this CTA's tasks: k = 0 .. n - 1 is task blockIdx.x + k * stride
+    const int n = (int)blockIdx.x < ntask ? (ntask - (int)blockIdx.x + stride - 1) / stride : 0;
+    auto task_of = [&](int k) { return (int)blockIdx.x + k * stride; };
+    auto img_of = [&](int k) {
+        return img_base + ((uint64_t)(p.w0 - p.img0) * H + (uint64_t)task_of(k)) * CH_STRIDE;
+    };
 
     struct Pos { int h, L; int64_t t0; };
     // A task's position in two steps: fetch issues the offset-table loads,
-    // finish is their first use (placed a phase later, so that the loads'
+    // finish is their first use (placed an iteration later, so that the loads'
     // latency is hidden).  Together they give the sequence bounds clamped into
     // [0, T] (as seq_bounds does) and the chunk's first token and length.
     struct PosRaw { int ch, h; int32_t c0, c1, cb; };
-    auto pos_fetch = [&](int task) {
+    auto pos_fetch = [&](int k) {
         PosRaw r{-1, 0, 0, 0, 0};
-        if (task >= ntask) return r;
+        if (k >= n) return r;
+        const int task = task_of(k);
         r.ch = p.w0 + task / H;
         r.h = task % H;
-        const int n = find_seq(chunk_base, p.N, r.ch);
-        r.c0 = p.cu[n];
-        r.c1 = p.cu[n + 1];
-        r.cb = chunk_base[n];
+        const int sq = find_seq(chunk_base, p.N, r.ch);
+        r.c0 = p.cu[sq];
+        r.c1 = p.cu[sq + 1];
+        r.cb = chunk_base[sq];
         return r;
     };
     auto pos_finish = [&](const PosRaw &r) {
@@ -277,25 +299,24 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         q.L = (int)((eos - q.t0) < C ? (eos - q.t0) : C);
         return q;
     };
-    auto task_pos = [&](int task) { return pos_finish(pos_fetch(task)); };
-    // beta (and the scalar gate) of row `tid` of a task, read ahead into registers
-    auto row_params = [&](const Pos &q, int task, float &b, float &gs) {
+    // beta (and the scalar gate) of row lt of task k, read ahead into registers
+    auto row_params = [&](const Pos &q, int k, float &b, float &gs) {
         b = 0.f; gs = 0.f;
-        if (tid < C && task < ntask && tid < q.L) {
-            b = p.beta[(q.t0 + tid) * H + q.h];
-            if (p.scalar_gate) gs = p.g[(q.t0 + tid) * H + q.h];
+        if (lt >= 0 && lt < C && k < n && lt < q.L) {
+            b = p.beta[(q.t0 + lt) * H + q.h];
+            if (p.scalar_gate) gs = p.g[(q.t0 + lt) * H + q.h];
         }
     };
     constexpr uint32_t TILE_BF16 = 16384, TILE_G = 32768;
-    auto expect_tma = [&]() {
+    // the staging loads of one task (one thread)
+    auto issue_tma = [&](const Pos &q) {
         mbar_arrive_expect_tx(&mbar[0], 3 * TILE_BF16 + (p.scalar_gate ? 0 : TILE_G));
-    };
-    // boxes of 128 bytes of channels: two per bf16 tile, four per fp32 tile
-    auto tma_kqg = [&](const Pos &q) {
+        // boxes of 128 bytes of channels: two per bf16 tile, four per fp32 tile
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
             tma_load_3d(sm + S1_STG_K + 8192 * b, &p.tm_k, 64 * b, q.h, (int)q.t0, &mbar[0]);
             tma_load_3d(sm + S1_STG_Q + 8192 * b, &p.tm_q, 64 * b, q.h, (int)q.t0, &mbar[0]);
+            tma_load_3d(sm + S1_STG_V + 8192 * b, &p.tm_v, 64 * b, q.h, (int)q.t0, &mbar[0]);
         }
         if (!p.scalar_gate) {
 #pragma unroll
@@ -303,36 +324,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
                 tma_load_3d(sm + S1_STG_G + 8192 * b, &p.tm_g, 32 * b, q.h, (int)q.t0, &mbar[0]);
         }
     };
-    auto tma_v = [&](const Pos &q) {
-#pragma unroll
-        for (int b = 0; b < 2; ++b)
-            tma_load_3d(sm + S1_STG_V + 8192 * b, &p.tm_v, 64 * b, q.h, (int)q.t0, &mbar[0]);
-    };
-    // W and U~ of a finished task: TMEM -> fp16 workspace images.  Row r of
-    // the M = 64 accumulators sits in lane r % 16 of quadrant r / 16; a warp
-    // reads its own quadrant.
-    auto store_wu_cols = [&](uint8_t *dst, int q, int col) {   // 16 columns
-        const int r = 16 * q + lane;
-        float w[16], u[16];
-        tmem_ld16(tmem_at(tmem, q, W_COL + col), w);
-        tmem_ld16(tmem_at(tmem, q, U_COL + col), u);
-        tmem_wait_ld();
-        if (lane < 16) {
-#pragma unroll
-            for (int hc = 0; hc < 2; ++hc) {
-                const int c0 = col + 8 * hc;
-                *reinterpret_cast<uint4 *>(dst + IMG_W + rc_img_off(r, c0)) = pack8_h(w + 8 * hc);
-                *reinterpret_cast<uint4 *>(dst + IMG_U + (c0 >> 5) * 4096 + u_img_off(r, (c0 & 31) >> 3)) =
-                    pack8_h(u + 8 * hc);
-            }
-        }
-    };
-    auto store_wu = [&](uint8_t *dst) {        // all 16 warps: 32 columns each
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) store_wu_cols(dst, warp & 3, 32 * (warp >> 2) + 16 * hh);
-    };
-    // W (or U~) of a finished task, the 16 rows of this warp's lane quadrant,
-    // by the warps that sit out the inverse
+    // W (or U~) of a finished task: the 16 rows of this warp's lane quadrant
+    // (row r of the M = 64 accumulators sits in lane r % 16 of quadrant r / 16)
     auto drain_half = [&](uint8_t *dst, bool is_u) {
         const int r = 16 * (warp & 3) + lane;
         const uint32_t col0 = is_u ? U_COL : W_COL;
@@ -356,237 +349,52 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
             }
         }
     };
-    // positions are resolved one task ahead of the one being loaded, so the
-    // offset-table lookups never sit on the critical path
-    int task = blockIdx.x;
-    Pos cur = task_pos(task), nxt = task_pos(task + stride);
-    float b_cur, gs_cur;
-    row_params(cur, task, b_cur, gs_cur);
-    uint32_t n_issued = 0, n_landed = 0;   // TMA phases (meaningful in thread 0, the issuer)
-    if (tid == 0 && task < ntask) { expect_tma(); tma_kqg(cur); tma_v(cur); n_issued = 1; }
 
-    bool ok = true;
-    uint32_t it = 0, ap_it = 0;
-    uint8_t *out_prev = nullptr;
-    for (; task < ntask; task += stride, ++it) {
-        const int L = cur.L;
-        const int next = task + stride;
-        uint8_t *out = img_base + ((uint64_t)(p.w0 - p.img0) * H + (uint64_t)task) * CH_STRIDE;
-        if (tid < C) {
-            sB[tid] = b_cur;
-            sGs[tid] = gs_cur;
-        }
-        ok = __syncthreads_and(mbar_wait(&mbar[0], it & 1));
-        if (!ok) break;
-        ++n_landed;
-        if (L < C) {
-            // the chunk ends inside the tile: rows L..63 become no-op tokens
-            // (k = q = v = 0, g = 0; beta is already 0 there), so that the
-            // scan and the prep need no per-row test
-            // (a token row is one 128-byte line in each of the ten boxes)
-            const int nrow = C - L;
-            for (int e = tid; e < nrow * 80; e += K1_THREADS) {
-                const int r = L + e / 80, bx = (e % 80) >> 3, x = e & 7;
-                const uint32_t box = bx < 2 ? S1_STG_K + 8192 * bx
-                                   : bx < 4 ? S1_STG_Q + 8192 * (bx - 2)
-                                   : bx < 6 ? S1_STG_V + 8192 * (bx - 4)
-                                            : S1_STG_G + 8192 * (bx - 6);
-                *reinterpret_cast<uint4 *>(sm + box + (r >> 3) * 1024 + (r & 7) * 128 + x * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-            __syncthreads();
-        }
-
-        // ---- cumulative log-gate, in place (rows past the sequence: g = 0) ----
-        // thread = (channel c, 16-row segment sg)
-        {
-            const int c = tid & 127, sg = tid >> 7;
-            auto G = [&](int r) -> float & {
-                return *reinterpret_cast<float *>(sm + S1_STG_G + stg32_off(r, c));
-            };
-            float v[16];
-            if (p.scalar_gate) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = sGs[16 * sg + j];
-            } else {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = G(16 * sg + j);
-            }
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                acc += v[j];
-                v[j] = acc;
-            }
-            tot[sg * 128 + c] = acc;
-            __syncthreads();
-            float off = 0.f;
-            for (int s2 = 0; s2 < sg; ++s2) off += tot[s2 * 128 + c];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) G(16 * sg + j) = v[j] + off;
-            if (sg == 3) {
-                gL[c] = acc + off;
-                eL[c] = __expf(acc + off);
-            }
-        }
-        // The previous task's W/U MMA ran under the scan; it must be done before
-        // the prep rewrites its B operands (its results leave TMEM during this
-        // task's inverse, before this task's W/U MMA reuses the columns).
-        ok = __syncthreads_and(it == 0 || mbar_wait(&mbar[2], (it - 1) & 1));
-        fence_after_sync();
-        if (!ok) break;
-        const bool slow = __shfl_sync(0xffffffffu,
-                                      __syncthreads_or(tid >= 384 && -gL[tid & 127] > RANGE_LIMIT),
-                                      0) != 0;
-        // the A / P issuer's operands, formed before the prep: after it, the
-        // prep's burst of global stores holds up shuffles for ~1k cycles
-        uint32_t ap_acc = 0, ap_aop = 0;
-        uint64_t ap_db = 0;
-        if (warp == K1_ISSUER0) {
-            ap_acc = warp_uniform(tmem + AP_COL);
-            ap_aop = warp_uniform(tmem + AOP_COL);
-            ap_db = sdesc_k_sw128(warp_uniform(smem_addr(sm)) + S1_OPB);
-        }
-
-        // ---- element-wise prep, one token row of 32 channels per thread: warp
-        // w owns TMEM lane quadrant w % 4 -- rows 32 (w % 4) .. + 31 of the
-        // M = 128 A operand [K e^g ; Q e^g] -- and channels 32 (w / 4) .. + 31,
-        // in two passes of 16 channels.  K rows (lanes 0-63, token t = lane):
-        // K e^g into the TMEM operand and the fp16 W operand, V into the fp16
-        // U~ operand.  Q rows (lanes 64-127, token t = lane - 64): Q e^g into
-        // the TMEM operand and the Q^ image, and for the same token K e^-g (the
-        // tf32 B operand of A / P, not on the slow path) and the Kbar image.
-        // A warp's 32 lanes read and write 32 consecutive token rows at one
-        // 16-byte chunk position, which the 128-byte swizzle spreads over all
-        // banks.
-        {
-            const int quad = warp & 3, cq = warp >> 2;
-            const int rr = 32 * quad + lane;
-            const bool krow = rr < 64;
-            const int t = krow ? rr : rr - 64;
-            float aop[32];
-#pragma unroll
-            for (int hp = 0; hp < 2; ++hp) {
-                const int c0 = 32 * cq + 16 * hp;        // first channel of this pass
-                float gm[16], x[16];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float4 g4 = *reinterpret_cast<const float4 *>(
-                        sm + S1_STG_G + stg32_off(t, c0 + 4 * j));
-                    gm[4 * j] = g4.x; gm[4 * j + 1] = g4.y; gm[4 * j + 2] = g4.z; gm[4 * j + 3] = g4.w;
-                }
-                auto load16 = [&](uint32_t tile, float (&dst)[16]) {
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(
-                            sm + tile + stg16_off(t, c0 + 8 * j));
-                        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = __bfloat1622float2(b2[e]);
-                            dst[8 * j + 2 * e] = f.x;
-                            dst[8 * j + 2 * e + 1] = f.y;
-                        }
-                    }
-                };
-                load16(krow ? S1_STG_K : S1_STG_Q, x);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) aop[16 * hp + e] = x[e] * __expf(gm[e]);
-                if (krow) {
-                    // fp16 K e^g: B operand of W = T' (K e^g)
-#pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        *reinterpret_cast<uint4 *>(sm + S1_KG16 + rc_img_off(t, c0 + 8 * j)) =
-                            pack8_h(aop + 16 * hp + 8 * j);
-                    // fp16 V: B operand of U~ = T' V
-                    load16(S1_STG_V, x);
-#pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        *reinterpret_cast<uint4 *>(sm + S1_V16 + rc_img_off(t, c0 + 8 * j)) =
-                            pack8_h(x + 8 * j);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        *reinterpret_cast<uint4 *>(out + IMG_Q + rc_img_off(t, c0 + 8 * j)) =
-                            pack8_h(aop + 16 * hp + 8 * j);
-                    // K e^-g and Kbar = K e^(gamma_last - gamma) of token t
-                    load16(S1_STG_K, x);
-                    float kb[16];
-                    if (!slow) {   // e^-gamma <= e^80 here: Kbar = (K e^-g) e^gamma_last
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            x[e] *= __expf(-gm[e]);
-                            kb[e] = x[e] * eL[c0 + e];
-                        }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            *reinterpret_cast<float4 *>(sm + S1_OPB + cq * 8192 +
-                                                        sw128_off(t, 4 * hp + j)) =
-                                make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) kb[e] = x[e] * __expf(gL[c0 + e] - gm[e]);
-                    }
-#pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        *reinterpret_cast<uint4 *>(out + IMG_KT + rc_img_off(t, c0 + 8 * j)) =
-                            pack8_h(kb + 8 * j);
-                }
-            }
-            tmem_st32(tmem_at(tmem, quad, AOP_COL + 32 * cq), aop);
-        }
-        if (tid < 128) reinterpret_cast<float *>(out + IMG_G)[tid] = eL[tid];
-        tmem_wait_st();
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
-
-        // ---- A and P: 16 tf32 K steps of 8 channels, A from TMEM, B (K e^-g)
-        // from shared memory, one accumulator, issued by warp 12's elected lane,
-        // which then starts the next task's loads (every staging tile is
-        // consumed).  Meanwhile every thread resolves the task after next.
-        if (!slow && warp == K1_ISSUER0) {
-            fence_after_sync();
-            constexpr uint32_t id = idesc(128, 64, FMT_TF32, FMT_TF32, 0, 0);
-            if (elect_one()) {
-#pragma unroll
-                for (int s2 = 0; s2 < 16; ++s2)   // channel atom s2 / 4 of the B operand
-                    mma_tf32_tmem_a(ap_acc, ap_aop + 8 * s2,
-                                    sdesc_add(ap_db, (s2 >> 2) * 8192 + (s2 & 3) * 32), id, s2 > 0);
-                mma_commit(&mbar[1]);
-                // after the MMAs: the copies' issue can wait behind the prep's
-                // global stores, the MMAs' cannot
-                if (next < ntask) { expect_tma(); tma_kqg(nxt); tma_v(nxt); }
-            }
-            __syncwarp();
-        }
-        row_params(nxt, next, b_cur, gs_cur);              // consumed next task
-        const PosRaw nn_raw = pos_fetch(next + stride);    // finished after the W/U MMA
-
-        float *As = reinterpret_cast<float *>(sm + S1_AS);
-        if (!slow) {
-            fence_before_sync();
-            ok = __syncthreads_and(mbar_wait(&mbar[1], ap_it & 1));
-            ++ap_it;
-            fence_after_sync();
-            if (!ok) break;
-            if (tid == 0 && next < ntask) ++n_issued;
-            {   // warp = (lane quadrant q, 16-column block cb); lane = row
+    // Task k passes through: stage P (iteration k - 1: gate scan and prep by
+    // warps 8-15, then the A/P MMA), stage I (iteration k: A/P readout by all
+    // warps, then the inverse by warps 0-5 while warps 8-15 run stage P of
+    // task k + 1; then the W/U MMA), and its W and U~ leave TMEM in iteration
+    // k + 1.  Positions: p0 = task i, pA = i + 1, pB = i + 2, rC = i + 3.
+    Pos p0{0, 0, 0}, pA = pos_finish(pos_fetch(0)), pB = pos_finish(pos_fetch(1));
+    PosRaw rC = pos_fetch(2);
+    float b_reg, gs_reg;
+    row_params(pA, 0, b_reg, gs_reg);
+    int last_tma = -1;      // the last task whose staging loads were issued (uniform)
+    if (n > 0) {
+        if (tid == 0) issue_tma(pA);
+        last_tma = 0;
+    }
+    bool ok = true, bad = false;
+    uint32_t ap_it = 0;     // A/P MMAs waited for (uniform)
+    int i = -1;
+    for (; i < n; ++i) {
+        // ---- stage I, part 1: A and P of task i ------------------------------
+        if (i >= 0) {
+            const bool slow_i = __shfl_sync(0xffffffffu, sflag[i & 1], 0) != 0;
+            uint8_t *out_i = img_of(i);
+            const float *sBi = sB2 + 64 * (i & 1);
+            if (!slow_i) {
+                fence_before_sync();
+                ok = __syncthreads_and(!bad && mbar_wait(&mbar[1], ap_it & 1));
+                ++ap_it;
+                fence_after_sync();
+                if (!ok) break;
+                // warp = (lane quadrant q, 16-column block cb); lane = row
                 const int q = warp & 3, cb = warp >> 2;
                 const int row = 32 * q + lane;
                 float d[16];
                 tmem_ld16(tmem_at(tmem, q, AP_COL + 16 * cb), d);
                 tmem_wait_ld();
                 if (row < 64) {
-                    const float b = sB[row];
+                    const float b = sBi[row];
                     float4 *arow = reinterpret_cast<float4 *>(As + row * LD + 16 * cb);
 #pragma unroll
                     for (int e4 = 0; e4 < 4; ++e4) {
                         float a4[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int i = 16 * cb + 4 * e4 + e;
-                            a4[e] = row > i ? b * d[4 * e4 + e] : 0.f;
+                            const int c = 16 * cb + 4 * e4 + e;
+                            a4[e] = row > c ? b * d[4 * e4 + e] : 0.f;
                         }
                         arow[e4] = make_float4(a4[0], a4[1], a4[2], a4[3]);
                     }
@@ -595,96 +403,295 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
                     float pv[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) pv[e] = (16 * cb + e) <= r ? d[e] : 0.f;
-                    *reinterpret_cast<uint4 *>(out + IMG_P + sw128_off(r, 2 * cb)) = pack8_h(pv);
-                    *reinterpret_cast<uint4 *>(out + IMG_P + sw128_off(r, 2 * cb + 1)) = pack8_h(pv + 8);
+                    *reinterpret_cast<uint4 *>(out_i + IMG_P + sw128_off(r, 2 * cb)) = pack8_h(pv);
+                    *reinterpret_cast<uint4 *>(out_i + IMG_P + sw128_off(r, 2 * cb + 1)) = pack8_h(pv + 8);
+                }
+            } else {
+                // ---- exact pairwise path for chunks whose decay leaves fp32
+                // range (their staging is still in place: the next task's
+                // loads wait for this)
+                const int L = p0.L;
+                auto kq = [&](uint32_t tile, int t, int c) {
+                    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                        sm + tile + stg16_off(t, c)));
+                };
+                auto gm = [&](int t, int c) {
+                    return *reinterpret_cast<const float *>(sm + S1_STG_G + stg32_off(t, c));
+                };
+                for (int e = tid; e < C * C; e += K1_THREADS) {
+                    const int r = e >> 6, c2 = e & 63;
+                    float a = 0.f, pp = 0.f;
+                    if (c2 <= r && r < L) {
+                        for (int c = 0; c < D; ++c) {
+                            const float ki = kq(S1_STG_K, c2, c) * __expf(gm(r, c) - gm(c2, c));
+                            a += kq(S1_STG_K, r, c) * ki;
+                            pp += kq(S1_STG_Q, r, c) * ki;
+                        }
+                    }
+                    As[r * LD + c2] = c2 < r ? sBi[r] * a : 0.f;
+                    *reinterpret_cast<__half *>(out_i + IMG_P + sw128_off(r, c2 >> 3) + (c2 & 7) * 2) =
+                        __float2half_rn(pp);
+                }
+                fence_before_sync();
+                __syncthreads();
+                if (i + 1 < n) {      // staging is consumed
+                    if (tid == 0) issue_tma(pA);
+                    last_tma = i + 1;
                 }
             }
-        } else {
-            // ---- exact pairwise path for chunks whose decay leaves fp32 range
-            auto kq = [&](uint32_t tile, int t, int c) {
-                return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                    sm + tile + stg16_off(t, c)));
-            };
-            auto gm = [&](int t, int c) {
-                return *reinterpret_cast<const float *>(sm + S1_STG_G + stg32_off(t, c));
-            };
-            for (int e = tid; e < C * C; e += K1_THREADS) {
-                const int r = e >> 6, i = e & 63;
-                float a = 0.f, pp = 0.f;
-                if (i <= r && r < L) {
-                    for (int c = 0; c < D; ++c) {
-                        const float ki = kq(S1_STG_K, i, c) * __expf(gm(r, c) - gm(i, c));
-                        a += kq(S1_STG_K, r, c) * ki;
-                        pp += kq(S1_STG_Q, r, c) * ki;
+        }
+        __syncthreads();
+
+        // ---- stage I, part 2 (task i) beside stage P (task i + 1) ------------
+        if (warp < 8) {
+            if (i >= 0) {
+                // task i - 1's W/U MMA done: T' is free, its W and U~ can leave TMEM
+                if (i >= 1 && !mbar_wait(&mbar[2], (uint32_t)((i - 1) & 1))) bad = true;
+                fence_after_sync();
+                if (warp < 6)
+                    invert_unit_lower(As, Ts, sB2 + 64 * (i & 1), sm + S1_TP, tid);
+                // W by warps 0-3, U~ by warps 4-7 (one lane quadrant each)
+                if (i >= 1) drain_half(img_of(i - 1), warp >= 4);
+            }
+        } else if (i + 1 < n) {
+            const int k = i + 1;
+            uint8_t *out = img_of(k);
+            const int L = pA.L;
+            const bool need_wu = k >= 2;   // W/U MMA of task k - 2 reads this B buffer
+            const uint32_t kgv = (k & 1) ? S1_KGV1 : S1_KGV0;
+            if (lt < C) {
+                sB2[64 * (k & 1) + lt] = b_reg;
+                sGs[lt] = gs_reg;
+            }
+            if (lt == 0) sflag[k & 1] = 0;
+            row_params(pB, k + 1, b_reg, gs_reg);   // consumed next iteration
+            if (!mbar_wait(&mbar[0], (uint32_t)(k & 1))) bad = true;
+            if (need_wu && !mbar_wait(&mbar[2], (uint32_t)((k - 2) & 1))) bad = true;
+            if (L < C) {
+                // the chunk ends inside the tile: rows L..63 become no-op tokens
+                // (k = q = v = 0, g = 0; beta is already 0 there), so that the
+                // scan and the prep need no per-row test
+                // (a token row is one 128-byte line in each of the ten boxes)
+                const int nrow = C - L;
+                for (int e = lt; e < nrow * 80; e += 256) {
+                    const int r = L + e / 80, bx = (e % 80) >> 3, x = e & 7;
+                    const uint32_t box = bx < 2 ? S1_STG_K + 8192 * bx
+                                       : bx < 4 ? S1_STG_Q + 8192 * (bx - 2)
+                                       : bx < 6 ? S1_STG_V + 8192 * (bx - 4)
+                                                : S1_STG_G + 8192 * (bx - 6);
+                    *reinterpret_cast<uint4 *>(sm + box + (r >> 3) * 1024 + (r & 7) * 128 + x * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            bar_sync(2, 256);
+
+            // cumulative log-gate, in place (rows past the sequence: g = 0);
+            // thread = (channel c, 32-row segment sg)
+            {
+                const int c = lt & 127, sg = lt >> 7;
+                auto G = [&](int r) -> float & {
+                    return *reinterpret_cast<float *>(sm + S1_STG_G + stg32_off(r, c));
+                };
+                float v[32];
+                if (p.scalar_gate) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = sGs[32 * sg + j];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = G(32 * sg + j);
+                }
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    acc += v[j];
+                    v[j] = acc;
+                }
+                tot[sg * 128 + c] = acc;
+                bar_sync(2, 256);
+                const float off = sg ? tot[c] : 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) G(32 * sg + j) = v[j] + off;
+                if (sg == 1) {
+                    gL[c] = acc + off;
+                    eL[c] = __expf(acc + off);
+                    if (-(acc + off) > RANGE_LIMIT) sflag[k & 1] = 1;
+                }
+            }
+            bar_sync(2, 256);
+            const bool slow = __shfl_sync(0xffffffffu, sflag[k & 1], 0) != 0;
+
+            // element-wise prep, one token row per thread: warp w owns TMEM
+            // lane quadrant w % 4 -- rows 32 (w % 4) .. + 31 of the M = 128 A
+            // operand [K e^g ; Q e^g] -- and channels 64 ((w - 8) / 4) .. + 63,
+            // in four passes of 16.  K rows (lanes 0-63, token t = lane):
+            // K e^g into the TMEM operand and the fp16 W operand, V into the
+            // fp16 U~ operand.  Q rows (lanes 64-127, token t = lane - 64):
+            // Q e^g into the TMEM operand and the Q^ image, and for the same
+            // token K e^-g (the tf32 B operand of A / P, not on the slow path)
+            // and the Kbar image.  A warp's 32 lanes read and write 32
+            // consecutive token rows at one 16-byte chunk position, which the
+            // 128-byte swizzle spreads over all banks.
+            const int quad = warp & 3;
+            const int rr = 32 * quad + lane;
+            const bool krow = rr < 64;
+            const int t = krow ? rr : rr - 64;
+#pragma unroll 1
+            for (int cqi = 0; cqi < 2; ++cqi) {
+                const int cq = 2 * ((warp - 8) >> 2) + cqi;
+                float aop[32];
+#pragma unroll
+                for (int hp = 0; hp < 2; ++hp) {
+                    const int c0 = 32 * cq + 16 * hp;        // first channel of this pass
+                    float gm[16], x[16];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float4 g4 = *reinterpret_cast<const float4 *>(
+                            sm + S1_STG_G + stg32_off(t, c0 + 4 * j));
+                        gm[4 * j] = g4.x; gm[4 * j + 1] = g4.y; gm[4 * j + 2] = g4.z; gm[4 * j + 3] = g4.w;
+                    }
+                    auto load16 = [&](uint32_t tile, float (&dst)[16]) {
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const uint4 raw = *reinterpret_cast<const uint4 *>(
+                                sm + tile + stg16_off(t, c0 + 8 * j));
+                            const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = __bfloat1622float2(b2[e]);
+                                dst[8 * j + 2 * e] = f.x;
+                                dst[8 * j + 2 * e + 1] = f.y;
+                            }
+                        }
+                    };
+                    load16(krow ? S1_STG_K : S1_STG_Q, x);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) aop[16 * hp + e] = x[e] * __expf(gm[e]);
+                    if (krow) {
+                        // fp16 K e^g: B operand of W = T' (K e^g)
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+                            *reinterpret_cast<uint4 *>(sm + kgv + rc_img_off(t, c0 + 8 * j)) =
+                                pack8_h(aop + 16 * hp + 8 * j);
+                        // fp16 V: B operand of U~ = T' V
+                        load16(S1_STG_V, x);
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+                            *reinterpret_cast<uint4 *>(sm + kgv + 16384 + rc_img_off(t, c0 + 8 * j)) =
+                                pack8_h(x + 8 * j);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+                            *reinterpret_cast<uint4 *>(out + IMG_Q + rc_img_off(t, c0 + 8 * j)) =
+                                pack8_h(aop + 16 * hp + 8 * j);
+                        // K e^-g and Kbar = K e^(gamma_last - gamma) of token t
+                        load16(S1_STG_K, x);
+                        float kb[16];
+                        if (!slow) {   // e^-gamma <= e^80 here: Kbar = (K e^-g) e^gamma_last
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                x[e] *= __expf(-gm[e]);
+                                kb[e] = x[e] * eL[c0 + e];
+                            }
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                *reinterpret_cast<float4 *>(sm + S1_OPB + cq * 8192 +
+                                                            sw128_off(t, 4 * hp + j)) =
+                                    make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) kb[e] = x[e] * __expf(gL[c0 + e] - gm[e]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+                            *reinterpret_cast<uint4 *>(out + IMG_KT + rc_img_off(t, c0 + 8 * j)) =
+                                pack8_h(kb + 8 * j);
                     }
                 }
-                As[r * LD + i] = i < r ? sB[r] * a : 0.f;
-                *reinterpret_cast<__half *>(out + IMG_P + sw128_off(r, i >> 3) + (i & 7) * 2) =
-                    __float2half_rn(pp);
+                tmem_st32(tmem_at(tmem, quad, AOP_COL + 32 * cq), aop);
             }
+            if (lt < 128) reinterpret_cast<float *>(out + IMG_G)[lt] = eL[lt];
+            tmem_wait_st();
+            fence_async_smem();
+            // the prep group is done with the staging and the A / P operands:
+            // warp 12 starts task k's A/P MMA and task k + 1's staging loads
+            // at once (a chunk out of range keeps its staging for the pairwise
+            // path, which issues the loads itself)
             fence_before_sync();
-            __syncthreads();
-            if (tid == 0 && next < ntask) {   // staging is consumed
-                expect_tma(); tma_kqg(nxt); tma_v(nxt);
-                ++n_issued;
-            }
-        }
-        __syncthreads();
-
-        // ---- T = (I + A)^-1 and the fp16 image of T' = T Diag(beta) (warps 0-5);
-        // meanwhile warp 12 forms the W / U~ MMA operands (formed right before
-        // the issue, their shuffles wait behind the inverse's stores)
-        uint32_t wu_acc = 0;
-        uint64_t wu_dt = 0, wu_db = 0;
-        if (warp < 6) {
-            invert_unit_lower(As, reinterpret_cast<float *>(sm + S1_TS),
-                              reinterpret_cast<float *>(sm + S1_TT),
-                              reinterpret_cast<float *>(sm + S1_FT), sB, sm + S1_TP, tid);
-        } else {
+            bar_sync(2, 256);
             if (warp == K1_ISSUER0) {
-                const uint32_t smb = warp_uniform(smem_addr(sm));
-                wu_acc = warp_uniform(tmem + W_COL);
-                wu_dt = sdesc_k_sw128(smb + S1_TP);
-                wu_db = sdesc(smb + S1_KG16, 8192, 1024, LAYOUT_SW128);
-            }
-            // the previous task's W (warps 6-9) and U~ (warps 10-13) leave
-            // TMEM for the workspace, one lane quadrant per warp
-            if (out_prev && warp < 14) drain_half(out_prev, warp >= 10);
-        }
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
-
-        // ---- [W | U~] = T' [K e^g | V] on tcgen05 (fp16, M = 64, N = 256: the
-        // two B operands sit side by side as four 64-column MN-major atoms, and
-        // the accumulators side by side in TMEM), issued by warp 12's elected lane
-        if (warp == K1_ISSUER0) {
-            fence_after_sync();
-            constexpr uint32_t id = idesc(64, 256, FMT_F16, FMT_F16, 0, 1);
-            if (elect_one()) {
+                fence_after_sync();
+                const uint32_t ap_acc = warp_uniform(tmem + AP_COL);
+                const uint32_t ap_aop = warp_uniform(tmem + AOP_COL);
+                const uint64_t ap_db = sdesc_k_sw128(warp_uniform(smem_addr(sm)) + S1_OPB);
+                if (elect_one() && !slow) {
+                    constexpr uint32_t id = idesc(128, 64, FMT_TF32, FMT_TF32, 0, 0);
 #pragma unroll
-                for (int s2 = 0; s2 < 4; ++s2)
-                    mma_f16(wu_acc, sdesc_add(wu_dt, 32 * s2), sdesc_add(wu_db, 2048 * s2), id, s2 > 0);
-                mma_commit(&mbar[2]);   // waited for after the next task's gate scan
+                    for (int s2 = 0; s2 < 16; ++s2)   // channel atom s2 / 4 of the B operand
+                        mma_tf32_tmem_a(ap_acc, ap_aop + 8 * s2,
+                                        sdesc_add(ap_db, (s2 >> 2) * 8192 + (s2 & 3) * 32), id, s2 > 0);
+                    mma_commit(&mbar[1]);
+                    if (k + 1 < n) issue_tma(pB);
+                }
+                __syncwarp();
+            }
+        }
+        fence_before_sync();
+        ok = __syncthreads_and(!bad);
+        fence_after_sync();
+        if (!ok) break;
+
+        // ---- W/U MMA of task i (warp 12's elected lane, after its A/P MMA of
+        // task i + 1)
+        const bool slow_n = i + 1 < n && __shfl_sync(0xffffffffu, sflag[(i + 1) & 1], 0) != 0;
+        if (warp == K1_ISSUER0) {
+            const uint32_t smb = warp_uniform(smem_addr(sm));
+            const uint32_t wu_acc = warp_uniform(tmem + W_COL);
+            const uint64_t wu_dt = sdesc_k_sw128(smb + S1_TP);
+            if (elect_one()) {
+                if (i >= 0) {
+                    // [W | U~] = T' [K e^g | V] (fp16, M = 64, N = 256: the two B
+                    // operands sit side by side as four 64-column MN-major
+                    // atoms, and the accumulators side by side in TMEM)
+                    const uint64_t wu_db = sdesc(smb + ((i & 1) ? S1_KGV1 : S1_KGV0), 8192, 1024,
+                                                 LAYOUT_SW128);
+                    constexpr uint32_t id = idesc(64, 256, FMT_F16, FMT_F16, 0, 1);
+#pragma unroll
+                    for (int s2 = 0; s2 < 4; ++s2)
+                        mma_f16(wu_acc, sdesc_add(wu_dt, 32 * s2), sdesc_add(wu_db, 2048 * s2), id, s2 > 0);
+                    mma_commit(&mbar[2]);
+                }
             }
             __syncwarp();
         }
-        out_prev = out;
-        cur = nxt;
-        nxt = pos_finish(nn_raw);
+        if (i + 2 < n && !slow_n) last_tma = i + 2;
+        p0 = pA;
+        pA = pB;
+        pB = pos_finish(rC);
+        rC = pos_fetch(i + 4);
     }
     // the last W/U MMA, then its results
-    if (ok && it > 0) {
-        ok = __syncthreads_and(mbar_wait(&mbar[2], (it - 1) & 1));
-        fence_after_sync();
-        if (ok) store_wu(out_prev);
+    if (ok && n > 0) {
+        if (warp < 8) {
+            if (!mbar_wait(&mbar[2], (uint32_t)((n - 1) & 1))) bad = true;
+            fence_after_sync();
+            drain_half(img_of(n - 1), warp >= 4);
+        }
+        ok = __syncthreads_and(!bad);
     }
-    if (!ok && tid == 0) {
-        ws_fail(ws_hdr, 1);
-        // let copies and MMAs still in flight finish before the CTA's shared
-        // memory and TMEM are released (bounded waits)
-        if (n_issued > n_landed) mbar_wait(&mbar[0], (n_issued - 1) & 1, 1u << 20);
-        if (it > 0) mbar_wait(&mbar[2], (it - 1) & 1, 1u << 20);
+    if (!ok) {
+        if (tid == 0) {
+            ws_fail(ws_hdr, 1);
+            // let copies still in flight finish before the CTA's shared memory
+            // is released (at most one set of staging loads is in flight)
+            if (last_tma >= 0) mbar_wait(&mbar[0], (uint32_t)(last_tma & 1), 1u << 20);
+        }
+        if (warp == K1_ISSUER0) {   // and the MMAs, before TMEM is released
+            if (elect_one()) {
+                mma_commit(&mbar[3]);
+                mbar_wait(&mbar[3], 0, 1u << 20);
+            }
+            __syncwarp();
+        }
     }
     fence_before_sync();
     __syncthreads();

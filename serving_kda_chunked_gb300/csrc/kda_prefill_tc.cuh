@@ -121,32 +121,34 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 
 // ---- per-chunk kernel: shared-memory layout and parameters ------------------
 constexpr int K1_THREADS = 512;
-constexpr int K1_ISSUER0 = 12;  // warp 12 issues the A/P MMAs
+constexpr int K1_ISSUER0 = 12;  // warp 12 issues the MMAs and the staging loads
 // staging of one (chunk, head): tiles brought by TMA with 128-byte swizzle, in
 // boxes of 128-byte rows (64 bf16 or 32 fp32 channels) of the 64 tokens
 constexpr uint32_t S1_STG_K = 0, S1_STG_Q = 16384, S1_STG_V = 32768;  // bf16: 2 boxes of 8 KB
 constexpr uint32_t S1_STG_G = 49152;                                  // fp32: 4 boxes of 8 KB
-constexpr uint32_t S1_OPA = 81920;    // scratch of the inverse (A, T, T_RR^T, F)
-constexpr uint32_t S1_OPB = 147456;   // tf32 K e^-g: 4 atoms x 64 rows x 128 B
-constexpr uint32_t S1_KG16 = 180224;  // fp16 K e^g, [r][c] 128B-swizzled (MN-major B)
-constexpr uint32_t S1_V16 = 196608;   // fp16 V, same layout
-constexpr uint32_t S1_TP = 212992;    // fp16 T', K-major SW128 [r][i]
-constexpr uint32_t S1_MISC = 221184;
-constexpr uint32_t S1_BYTES = S1_MISC + 4096 + 1024;
-// after the A/P MMA has completed the operand area is reused by the inverse:
 constexpr int LD = 68;                          // fp32 row stride of the 64 x 64 tiles
 constexpr uint32_t TILE_BYTES = 64 * LD * 4;    // 17,408
-constexpr uint32_t S1_AS = S1_OPA;                   // A    fp32 [64][LD]
-constexpr uint32_t S1_TS = S1_OPA + TILE_BYTES;      // T    fp32 [64][LD]
-constexpr uint32_t S1_TT = S1_OPA + 2 * TILE_BYTES;  // T_RR transposed (diagonal blocks)
-constexpr uint32_t S1_FT = S1_OPA + 3 * TILE_BYTES;  // F = T_RR A_RJ, transposed
-static_assert(S1_FT + TILE_BYTES <= S1_KG16, "inverse scratch overlaps the fp16 operands");
+constexpr uint32_t S1_AS = 81920;               // A fp32 [64][LD] (then F^T in its upper blocks)
+constexpr uint32_t S1_TS = S1_AS + TILE_BYTES;  // T fp32 [64][LD] (T_RR^T in its upper blocks)
+// fp16 K e^g and V, [r][c] 128B-swizzled (MN-major B), side by side: one
+// buffer per task parity (the prep of task k + 1 runs while the W/U MMA of
+// task k - 1 may still read the other buffer)
+constexpr uint32_t S1_KGV1 = 116736;
+constexpr uint32_t S1_OPB = 149504;   // tf32 K e^-g: 4 atoms x 64 rows x 128 B
+constexpr uint32_t S1_KGV0 = 182272;
+constexpr uint32_t S1_TP = 215040;    // fp16 T', K-major SW128 [r][i]
+constexpr uint32_t S1_MISC = 223232;
+constexpr uint32_t S1_BYTES = S1_MISC + 4096 + 1024;
+static_assert(S1_TS + TILE_BYTES <= S1_KGV1 && S1_KGV1 + 32768 <= S1_OPB &&
+              S1_OPB + 32768 <= S1_KGV0 && S1_KGV0 + 32768 <= S1_TP && S1_TP + 8192 <= S1_MISC &&
+              S1_KGV1 % 1024 == 0 && S1_OPB % 1024 == 0 && S1_KGV0 % 1024 == 0 &&
+              S1_TP % 1024 == 0 && S1_BYTES <= 232448, "per-chunk kernel shared-memory layout");
 // TMEM: A/P accumulator (64 columns), the tf32 A operand [K e^g ; Q e^g]
 // (128 columns, one channel each), W, U~
 constexpr int AP_COL = 0, AOP_COL = 128, W_COL = 256, U_COL = 384;
 // one N = 256 MMA covers W and U~: their B operands (fp16 K e^g, fp16 V) are
 // adjacent 64-column atoms, their accumulators adjacent TMEM columns
-static_assert(S1_V16 == S1_KG16 + 16384 && U_COL == W_COL + 128, "W / U~ operands must be adjacent");
+static_assert(U_COL == W_COL + 128, "W / U~ accumulators must be adjacent");
 constexpr float RANGE_LIMIT = 80.f;                   // e^80 stays inside fp32
 
 struct K1Params {
