@@ -77,9 +77,10 @@ chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int cap,
 //   6. W = T' (K e^g), U~ = T' V on tcgen05 (fp16), moved from TMEM to the
 //      workspace during the next task's inverse.
 // Steps 2-4 of task k + 1 run on warps 8-15 while warps 0-5 run the inverse
-// of task k and warps 0-7 move task k - 1's W and U~ out; warp 12 issues
-// every MMA and copy.  The inverse then hides the prep's latency instead of
-// adding to it.
+// of task k and warps 0-7 move task k - 1's W and U~ out.  Warp 12 issues the
+// A/P MMAs, warp 13 the staging loads and warp 6 the W/U MMAs, each from one
+// elected lane.  The inverse then hides the prep's latency instead of adding
+// to it.
 __device__ __forceinline__ void tma_load_3d(uint8_t *dst, const CUtensorMap *map, int c0, int c1,
                                             int c2, uint64_t *mbar) {
     asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
@@ -211,8 +212,9 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
     float *tot = sB2 + 128;                                // [2][128] scan segment totals
     float *sGs = tot + 256;                                // [64] scalar gates (scalar_gate)
     int32_t *sflag = reinterpret_cast<int32_t *>(sGs + 64);   // [2] out-of-range chunk, by parity
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(sflag + 2);  // [0] TMA, [1] A/P, [2] W/U, [3] drain
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 4);
+    // [0] TMA, [1] A/P, [2] W/U, [3] [4] drains of the two MMA issuers
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(sflag + 2);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 5);
     float *As = reinterpret_cast<float *>(sm + S1_AS);
     float *Ts = reinterpret_cast<float *>(sm + S1_TS);
 
@@ -230,7 +232,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         mbar_init(&mbar[0], 1);
         mbar_init(&mbar[1], 1);   // A/P MMAs
         mbar_init(&mbar[2], 1);   // W and U~ MMAs
-        mbar_init(&mbar[3], 1);   // drain after a failed wait
+        mbar_init(&mbar[3], 1);   // drains after a failed wait
+        mbar_init(&mbar[4], 1);
         mbar_fence_init();
     }
 #ifdef KDA_FAULT_INJECTION
@@ -613,9 +616,9 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
             tmem_wait_st();
             fence_async_smem();
             // the prep group is done with the staging and the A / P operands:
-            // warp 12 starts task k's A/P MMA and task k + 1's staging loads
-            // at once (a chunk out of range keeps its staging for the pairwise
-            // path, which issues the loads itself)
+            // warp 12 starts task k's A/P MMA and, beside it, warp 13 task
+            // k + 1's staging loads (a chunk out of range keeps its staging
+            // for the pairwise path, which issues the loads itself)
             fence_before_sync();
             bar_sync(2, 256);
             if (warp == K1_ISSUER0) {
@@ -630,8 +633,10 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
                         mma_tf32_tmem_a(ap_acc, ap_aop + 8 * s2,
                                         sdesc_add(ap_db, (s2 >> 2) * 8192 + (s2 & 3) * 32), id, s2 > 0);
                     mma_commit(&mbar[1]);
-                    if (k + 1 < n) issue_tma(pB);
                 }
+                __syncwarp();
+            } else if (warp == K1_ISSUER0 + 1) {
+                if (elect_one() && !slow && k + 1 < n) issue_tma(pB);
                 __syncwarp();
             }
         }
@@ -640,10 +645,10 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         fence_after_sync();
         if (!ok) break;
 
-        // ---- W/U MMA of task i (warp 12's elected lane, after its A/P MMA of
-        // task i + 1)
+        // ---- W/U MMA of task i (warp 6's elected lane; warp 12 meanwhile
+        // joins the A/P wait)
         const bool slow_n = i + 1 < n && __shfl_sync(0xffffffffu, sflag[(i + 1) & 1], 0) != 0;
-        if (warp == K1_ISSUER0) {
+        if (warp == K1_WU) {
             const uint32_t smb = warp_uniform(smem_addr(sm));
             const uint32_t wu_acc = warp_uniform(tmem + W_COL);
             const uint64_t wu_dt = sdesc_k_sw128(smb + S1_TP);
@@ -685,10 +690,11 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
             // is released (at most one set of staging loads is in flight)
             if (last_tma >= 0) mbar_wait(&mbar[0], (uint32_t)(last_tma & 1), 1u << 20);
         }
-        if (warp == K1_ISSUER0) {   // and the MMAs, before TMEM is released
+        if (warp == K1_ISSUER0 || warp == K1_WU) {   // and the MMAs, before TMEM is released
+            uint64_t *mb = &mbar[warp == K1_WU ? 4 : 3];
             if (elect_one()) {
-                mma_commit(&mbar[3]);
-                mbar_wait(&mbar[3], 0, 1u << 20);
+                mma_commit(mb);
+                mbar_wait(mb, 0, 1u << 20);
             }
             __syncwarp();
         }

@@ -121,7 +121,8 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 
 // ---- per-chunk kernel: shared-memory layout and parameters ------------------
 constexpr int K1_THREADS = 512;
-constexpr int K1_ISSUER0 = 12;  // warp 12 issues the MMAs and the staging loads
+constexpr int K1_ISSUER0 = 12;  // warp 12 issues the A/P MMAs, warp 13 the staging loads
+constexpr int K1_WU = 6;        // warp 6 issues the W/U MMAs
 // staging of one (chunk, head): tiles brought by TMA with 128-byte swizzle, in
 // boxes of 128-byte rows (64 bf16 or 32 fp32 channels) of the 64 tokens
 constexpr uint32_t S1_STG_K = 0, S1_STG_Q = 16384, S1_STG_V = 32768;  // bf16: 2 boxes of 8 KB
