@@ -86,10 +86,10 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    // [0..2] loads of the three stages, [3] round 1, [4] round 2 state part,
-    // [5] round 2 output part, [6] drain
+    // [0..2] loads of the three stages, [3] W S, [4] Kbar^T U, [5..6] the
+    // outputs of TMEM set 0 / 1 (their P U), [7] drain
     uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + S2_MISC);
-    constexpr int MB_R1 = S2_NSTAGE, MB_R2S = MB_R1 + 1, MB_R2O = MB_R1 + 2, MB_DRAIN = MB_R1 + 3;
+    constexpr int MB_R1 = S2_NSTAGE, MB_R2S = MB_R1 + 1, MB_R2O = MB_R1 + 2, MB_DRAIN = MB_R1 + 4;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + MB_DRAIN + 1);
     int32_t *iss = reinterpret_cast<int32_t *>(tmem_slot + 1);   // [3] last chunk loaded per stage
 
@@ -190,11 +190,6 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     }
     const bool write_o = role == SEG_FULL;
     const float u_scale = role == SEG_M ? 0.f : 1.f;   // the homogeneous map drops U~
-    // the zero half of [0 ; P] in every stage
-    for (int e = tid; e < S2_NSTAGE * 8192 / 16; e += K2_THREADS) {
-        const int st = e / 512, off = (e % 512) * 16;
-        *reinterpret_cast<uint4 *>(sm + st * S2_STAGE + S2_PZ + off) = make_uint4(0u, 0u, 0u, 0u);
-    }
     if (tid == 0) {
         for (int j = 0; j <= MB_DRAIN; ++j) mbar_init(&mbar[j], 1);
         mbar_fence_init();
@@ -231,24 +226,25 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
         __syncwarp();
     }
 
-    const uint32_t id_wq = idesc(128, DVS, FMT_F16, FMT_F16, 0, 1);
+    const uint32_t id_m64 = idesc(64, DVS, FMT_F16, FMT_F16, 0, 1);   // W S, Q^ S, P U
     const uint32_t id_kb = idesc(128, DVS, FMT_F16, FMT_F16, 1, 1);
 
-    // the O rows of a finished chunk (warps 2-3: row - 64), once its P U MMA
-    // (the last to accumulate into them) has completed
-    auto store_o = [&](int set, int64_t t0, int L, uint32_t pu_parity) -> bool {
-        if (!mbar_wait(&mbar[MB_R2O], pu_parity)) return false;
+    // Half (16 columns) of the O rows of a finished chunk, once its P U MMA
+    // (the last to accumulate into them) has completed: row r = 16 warp + lane
+    // of the M = 64 accumulator sits in lane r % 16 of quadrant r / 16 (lanes
+    // 0-15 store).
+    auto store_o = [&](int set, int64_t t0, int L, uint32_t pu_parity, int half) -> bool {
+        if (!mbar_wait(&mbar[MB_R2O + set], pu_parity)) return false;
         fence_after_sync();
-        float oa[16], ob[16];
-        tmem_ld16(tmem_at(tmem, warp, 128 * set), oa);
-        tmem_ld16(tmem_at(tmem, warp, 128 * set + 16), ob);
+        float oa[16];
+        tmem_ld16(tmem_at(tmem, warp, 128 * set + 32 + 16 * half), oa);
         tmem_wait_ld();
-        const int r = row - 64;
-        if (r < L) {
-            __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * D + slice * DVS;
+        const int r = 16 * warp + lane;
+        if (lane < 16 && r < L) {
+            __nv_bfloat16 *dst = p.o + ((t0 + r) * H + h) * D + slice * DVS + 16 * half;
 #pragma unroll
-            for (int gq = 0; gq < DVS / 8; ++gq) {
-                const float *src = gq < 2 ? oa + 8 * gq : ob + 8 * (gq - 2);
+            for (int gq = 0; gq < 2; ++gq) {
+                const float *src = oa + 8 * gq;
                 __nv_bfloat162 b0 = __floats2bfloat162_rn(src[0], src[1]);
                 __nv_bfloat162 b1 = __floats2bfloat162_rn(src[2], src[3]);
                 __nv_bfloat162 b2 = __floats2bfloat162_rn(src[4], src[5]);
@@ -261,24 +257,31 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
         return true;
     };
 
-    // Per chunk i (stage i % 3, TMEM set i % 2; D_A = set columns 0-31, D_S =
-    // set columns 64-95).  Warps 0-3 hold the fp32 state (thread = row); warp
-    // 4 issues every MMA and load from its elected lane, so no state-holding
-    // warp ever blocks on an issue:
+    // Per chunk i (stage i % 3, TMEM set i % 2: D_W = set columns 0-31 (W S,
+    // M = 64), D_O = columns 32-63 (Q^ S + P U, M = 64), D_S = columns 64-95
+    // (Kbar^T U, M = 128)).  Warps 0-3 hold the fp32 state (thread = row);
+    // warp 4 issues every MMA and load from its elected lane, so no
+    // state-holding warp ever blocks on an issue:
     //   B1 (all):       S (fp16 operand) written, chunk i's operands landed
-    //   warp 4:         round 1, D_A = [W ; Q^] S (8 K steps) -> MB_R1
-    //   warps 0-1:      U = U~ - W S (rows 0-63), fp16 operand
-    //   warps 2-3:      the O rows of chunk i - 1 (off the critical path)
+    //   warp 4:         D_W = W S (8 K steps, M = 64: half the operand reads
+    //                   of the M = 128 [W ; Q^] S, and on the critical path)
+    //                   -> MB_R1, then D_O = Q^ S, then the operands of chunk
+    //                   i + 2 into the stage of chunk i - 1 (once chunk i - 1's
+    //                   P U is done)
+    //   warps 0-3:      half the O rows of chunk i - 1 (while W S runs), then
+    //                   U = U~ - W S (token rows 16 warp + lane, lanes 0-15)
     //   B2 (all):       U written
-    //   warp 4:         after round 1, the operands of chunk i + 2 into the
-    //                   stage of chunk i - 1 (once chunk i - 1's P U is done)
-    //   warp 4:         round 2, D_S = Kbar^T U (4 K steps) -> MB_R2S, then
-    //                   D_A += [0 ; P] U (4 K steps) -> MB_R2O
-    //   warps 0-3:      S = Diag(e^gamma_last) S + D_S   (after MB_R2S)
-    // Round 1 of chunk i completes after every MMA of chunk i - 1 (one
-    // issuing thread, whose commits track all its earlier MMAs), so when B2
-    // passes, the U operand's previous contents are free.  Loads run two
-    // chunks ahead.
+    //   warp 4:         D_S = Kbar^T U (4 K steps) -> MB_R2S, then
+    //                   D_O += P U (4 K steps, M = 64) -> MB_R2O of the set
+    //   warps 0-3:      the other half (while Kbar^T U runs), then
+    //                   S = Diag(e^gamma_last) S + D_S   (after MB_R2S)
+    // W S of chunk i completes after every MMA of chunk i - 1 (one issuing
+    // thread, whose commits track all its earlier MMAs), so when B2 passes,
+    // the U operand's previous contents are free.  The output barrier of a
+    // set completes once every two chunks, and its waiters (the issuer before
+    // the loads, warps 0-3 before the O rows) wait for it before B2 of the
+    // next chunk, whose P U completes its next phase.  Loads run two chunks
+    // ahead.
     bool ok = true, bad = false;
     int64_t prev_t0 = 0;
     int prev_L = 0;
@@ -305,38 +308,48 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
 
         if (issuer) {                     // round 1
             const uint32_t stb = warp_uniform(smb + (uint32_t)stage * S2_STAGE);
-            const uint32_t d_a = warp_uniform(tmem + 128u * (uint32_t)set);
+            const uint32_t d_w = warp_uniform(tmem + 128u * (uint32_t)set);
             const uint64_t dwq = sdesc_k_sw128(stb + S2_WQ);
             const uint64_t dso = sdesc(smb + S2_SOP, 128, 2048, LAYOUT_NONE);
             if (elect_one()) {
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    mma_f16(d_a, sdesc_add(dwq, (s >> 2) * 16384 + (s & 3) * 32),
-                            sdesc_add(dso, 256 * s), id_wq, s > 0);
+                    mma_f16(d_w, sdesc_add(dwq, (s >> 2) * 16384 + (s & 3) * 32),
+                            sdesc_add(dso, 256 * s), id_m64, s > 0);
                 mma_commit(&mbar[MB_R1]);
+#pragma unroll
+                for (int s = 0; s < 8; ++s)   // Q^ rows sit 8 KB after the W rows of each atom
+                    mma_f16(d_w + 32, sdesc_add(dwq, 8192 + (s >> 2) * 16384 + (s & 3) * 32),
+                            sdesc_add(dso, 256 * s), id_m64, s > 0);
                 // chunk i + 2's operands into the stage of chunk i - 1 (a stage
                 // not used yet when i = 0): its last reader, chunk i - 1's P U,
                 // has completed.  Issued here, where the issuer waits anyway
                 // for the U operand, so that they never delay round 2.
                 if (ch + 2 < b) {
-                    if (i == 0 || mbar_wait(&mbar[MB_R2O], (uint32_t)((i - 1) & 1)))
+                    if (i == 0 || mbar_wait(&mbar[MB_R2O + (set ^ 1)], (uint32_t)(((i - 1) >> 1) & 1)))
                         issue_loads(ch + 2, (i + 2) % S2_NSTAGE);
                     else
                         bad = true;
                 }
             }
             __syncwarp();
-        } else if (warp < 2) {            // U = U~ - W S for token rows 0-63
+        } else {
+            // the first half of the previous chunk's O rows, while W S runs
+            if (i > 0 && write_o &&
+                !store_o(set ^ 1, prev_t0, prev_L, (uint32_t)(((i - 1) >> 1) & 1), 0))
+                bad = true;
+            // U = U~ - W S for token row 16 warp + lane (lanes 0-15)
             if (!mbar_wait(&mbar[MB_R1], i & 1)) bad = true;
             fence_after_sync();
             float w0[16], w1[16];
             tmem_ld16(tmem_at(tmem, warp, 128 * set), w0);
             tmem_ld16(tmem_at(tmem, warp, 128 * set + 16), w1);
             tmem_wait_ld();
+            const int ur = 16 * warp + (lane & 15);
             float u[DVS];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const uint4 x = *reinterpret_cast<const uint4 *>(st + S2_U + u_img_off(row, q));
+                const uint4 x = *reinterpret_cast<const uint4 *>(st + S2_U + u_img_off(ur, q));
                 const __half2 *h2 = reinterpret_cast<const __half2 *>(&x);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -346,43 +359,46 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
                     u[j + 1] = u_scale * f.y - (j + 1 < 16 ? w0[j + 1] : w1[j - 15]);
                 }
             }
+            if (lane < 16) {
 #pragma unroll
-            for (int gq = 0; gq < DVS / 8; ++gq) {
-                uint4 v4 = make_uint4(pack_h2(u[8 * gq + 0], u[8 * gq + 1]), pack_h2(u[8 * gq + 2], u[8 * gq + 3]),
-                                      pack_h2(u[8 * gq + 4], u[8 * gq + 5]), pack_h2(u[8 * gq + 6], u[8 * gq + 7]));
-                *reinterpret_cast<uint4 *>(sm + S2_UOP + gq * 1024 + (row >> 3) * 128 + (row & 7) * 16) = v4;
+                for (int gq = 0; gq < DVS / 8; ++gq) {
+                    uint4 v4 = make_uint4(pack_h2(u[8 * gq + 0], u[8 * gq + 1]), pack_h2(u[8 * gq + 2], u[8 * gq + 3]),
+                                          pack_h2(u[8 * gq + 4], u[8 * gq + 5]), pack_h2(u[8 * gq + 6], u[8 * gq + 7]));
+                    *reinterpret_cast<uint4 *>(sm + S2_UOP + gq * 1024 + (ur >> 3) * 128 + (ur & 7) * 16) = v4;
+                }
             }
             fence_async_smem();
-        } else if (i > 0) {               // warps 2-3: the previous chunk's outputs
-            const uint32_t par = (uint32_t)((i - 1) & 1);
-            const bool okp = write_o ? store_o(set ^ 1, prev_t0, prev_L, par)
-                                     : mbar_wait(&mbar[MB_R2O], par);
-            if (!okp) bad = true;
         }
-        // B2 (all): U is in shared memory.  Warps 2-3 take part too: they have
-        // then seen chunk i - 1's P U complete before the issuer commits chunk
-        // i's, so no barrier phase runs two ahead of a thread that waits on it.
+        // B2 (all): U is in shared memory.
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
         if (issuer) {                     // round 2, then the loads of chunk i + 2
             const uint32_t stb = warp_uniform(smb + (uint32_t)stage * S2_STAGE);
-            const uint32_t d_a = warp_uniform(tmem + 128u * (uint32_t)set);
+            const uint32_t d_w = warp_uniform(tmem + 128u * (uint32_t)set);
             const uint64_t dkb = sdesc(stb + S2_KB, 8192, 1024, LAYOUT_SW128);
-            const uint64_t dpz = sdesc_k_sw128(stb + S2_PZ);
+            const uint64_t dp = sdesc_k_sw128(stb + S2_PZ + 8192);
             const uint64_t duo = sdesc(smb + S2_UOP, 128, 1024, LAYOUT_NONE);
             if (elect_one()) {
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_f16(d_a + 64, sdesc_add(dkb, 2048 * s), sdesc_add(duo, 256 * s), id_kb, s > 0);
+                    mma_f16(d_w + 64, sdesc_add(dkb, 2048 * s), sdesc_add(duo, 256 * s), id_kb, s > 0);
                 mma_commit(&mbar[MB_R2S]);
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_f16(d_a, sdesc_add(dpz, 32 * s), sdesc_add(duo, 256 * s), id_wq, 1);
-                mma_commit(&mbar[MB_R2O]);
+                    mma_f16(d_w + 32, sdesc_add(dp, 32 * s), sdesc_add(duo, 256 * s), id_m64, 1);
+                mma_commit(&mbar[MB_R2O + set]);
             }
             __syncwarp();
-        } else {                          // S = Diag(e^gamma_last) S + Kbar^T U
+        } else {
+            // the second half, while Kbar^T U runs
+            if (i > 0) {
+                const uint32_t par = (uint32_t)(((i - 1) >> 1) & 1);
+                const bool okp = write_o ? store_o(set ^ 1, prev_t0, prev_L, par, 1)
+                                         : mbar_wait(&mbar[MB_R2O + (set ^ 1)], par);
+                if (!okp) bad = true;
+            }
+            // S = Diag(e^gamma_last) S + Kbar^T U
             if (!mbar_wait(&mbar[MB_R2S], i & 1)) bad = true;
             fence_after_sync();
             float d2a[16], d2b[16];
@@ -402,10 +418,12 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     ok = ok && __syncthreads_and(!bad);
     // the last chunk's outputs (and, in any case, its P U MMA -- the last MMA
     // issued -- before TMEM is freed)
-    if (ok && a < b && (warp == 2 || warp == 3)) {
-        const uint32_t par = (uint32_t)((b - 1 - a) & 1);
-        const bool okp = write_o ? store_o((b - 1 - a) & 1, prev_t0, prev_L, par)
-                                 : mbar_wait(&mbar[MB_R2O], par);
+    if (ok && a < b && !issuer) {
+        const int il = b - 1 - a;
+        const uint32_t par = (uint32_t)((il >> 1) & 1);
+        const bool okp = write_o ? (store_o(il & 1, prev_t0, prev_L, par, 0) &&
+                                    store_o(il & 1, prev_t0, prev_L, par, 1))
+                                 : mbar_wait(&mbar[MB_R2O + (il & 1)], par);
         if (!okp) bad = true;
     }
     ok = __syncthreads_and(ok && !bad);

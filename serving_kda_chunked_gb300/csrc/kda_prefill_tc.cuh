@@ -171,7 +171,7 @@ constexpr int K2_THREADS = 160;       // warps 0-3: the state, warp 4: MMA and l
 constexpr int K2_ISSUER = 4;
 constexpr uint32_t S2_WQ = 0;          // [W ; Q^] K-major SW128, 2 atoms x 128 rows
 constexpr uint32_t S2_KB = 32768;      // Kbar [r][c] SW128 (MN-major A)
-constexpr uint32_t S2_PZ = 49152;      // [0 ; P] K-major SW128, 128 rows (rows 0-63 zero)
+constexpr uint32_t S2_PZ = 49152;      // P K-major SW128 at +8192 (64 rows)
 constexpr uint32_t S2_U = 65536;       // U~ slice [64][32] fp16
 constexpr uint32_t S2_G = 69632;       // e^gamma_last [128] fp32
 constexpr uint32_t S2_STAGE = 70656;   // bytes per stage (multiple of 1024)
@@ -181,8 +181,8 @@ constexpr uint32_t S2_UOP = S2_SOP + 8192;                // U fp16, K=64 x N=32
 constexpr uint32_t S2_MISC = S2_UOP + 4096;
 constexpr uint32_t S2_BYTES = S2_MISC + 256 + 1024;
 constexpr uint32_t S2_TX = 4 * 8192 + 16384 + 8192 + 4096 + 512;   // bytes landing per stage
-// TMEM set s (0, 1) at column 128 s: D_A +0 ([W ; Q^] S, then += [0 ; P] U),
-// D_S +64 (Kbar^T U)
+// TMEM set s (0, 1) at column 128 s: D_W +0 (W S, M = 64), D_O +32 (Q^ S,
+// then += P U, M = 64), D_S +64 (Kbar^T U)
 
 struct K2Params {
     const float *S0;
