@@ -336,6 +336,42 @@ def test_prefill_strong_gates(dtype):
     assert_close("S_T", S_T, S_ref, TOL[DT[dtype]])
 
 
+def _strong_every_third_chunk(inp, scale=8.0):
+    """Multiply the log-gate of every third 64-token chunk of each sequence
+    (chunk index 1, 4, 7, ...) by ``scale``: those chunks leave the range of
+    the single-reference factors, their neighbours do not."""
+    g = inp["g"]
+    for n, (a, b) in enumerate(zip(inp["cu_seqlens"][:-1].tolist(), inp["cu_seqlens"][1:].tolist())):
+        for c0 in range(a + 64, b, 3 * 64):
+            g[c0:min(c0 + 64, b)] *= scale
+    return inp
+
+
+@pytest.mark.parametrize("variant", ["kda", "gdn"])
+def test_prefill_mixed_strong_chunks(variant):
+    """Out-of-range chunks between ordinary ones, with several (chunk, head)
+    tasks per CTA: a chunk on the pairwise path keeps its staging tiles until
+    that path has read them, and the next task's loads start after it; the
+    ordinary chunks around it take the tensor-core path in the same CTA."""
+    lengths = [9000, 7000, 130, 64]
+    cfg = ki.PrefillConfig("mixed", H=2, d=128, dtype="bf16", n_seqs=len(lengths), s0_std=0.3)
+    inp = _strong_every_third_chunk(ki.prefill_inputs(cfg, device=DEV, seed=23, lengths=lengths))
+    tasks = sum((L + 63) // 64 for L in lengths) * 2
+    assert tasks > 3 * torch.cuda.get_device_properties(0).multi_processor_count
+    if variant == "kda":
+        o, S_T = _run_prefill(inp)
+        o_ref, S_ref = _oracle_prefill(inp)
+    else:
+        gh = inp["g"][..., 0].contiguous()
+        o, S_T = gdn_prefill(inp["q"], inp["k"], inp["v"], gh, inp["beta"], inp["cu_seqlens"],
+                             inp["S0"])
+        torch.cuda.synchronize()
+        o_ref, S_ref, _ = oracle.gdn_prefill(inp["q"], inp["k"], inp["v"], gh, inp["beta"],
+                                             inp["S0"], inp["cu_seqlens"])
+    assert_close("o", o, o_ref, 2e-3)
+    assert_close("S_T", S_T, S_ref, 2e-3)
+
+
 # ---------------------------------------------------------------------------
 # Gated DeltaNet: one gate per head and token
 # ---------------------------------------------------------------------------
