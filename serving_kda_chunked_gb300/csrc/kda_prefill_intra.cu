@@ -643,11 +643,14 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         fence_before_sync();
         ok = __syncthreads_and(!bad);
         fence_after_sync();
+        // task i + 2's staging loads left with the A/P MMA unless task i + 1 is
+        // out of range: counted before a possible exit, which waits for them
+        const bool slow_n = i + 1 < n && __shfl_sync(0xffffffffu, sflag[(i + 1) & 1], 0) != 0;
+        if (i + 2 < n && !slow_n) last_tma = i + 2;
         if (!ok) break;
 
         // ---- W/U MMA of task i (warp 6's elected lane; warp 12 meanwhile
         // joins the A/P wait)
-        const bool slow_n = i + 1 < n && __shfl_sync(0xffffffffu, sflag[(i + 1) & 1], 0) != 0;
         if (warp == K1_WU) {
             const uint32_t smb = warp_uniform(smem_addr(sm));
             const uint32_t wu_acc = warp_uniform(tmem + W_COL);
@@ -668,7 +671,6 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
             }
             __syncwarp();
         }
-        if (i + 2 < n && !slow_n) last_tma = i + 2;
         p0 = pA;
         pA = pB;
         pB = pos_finish(rC);
