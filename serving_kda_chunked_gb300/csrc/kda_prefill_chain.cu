@@ -111,9 +111,16 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     int32_t *ws_hdr = reinterpret_cast<int32_t *>(p.ws);
     const int32_t *chunk_base = reinterpret_cast<const int32_t *>(p.ws + WS_HEADER);
     const uint8_t *img_base = p.ws + ws_images_offset(p.N);
-    // a per-chunk kernel of this call gave up on a wait: its images are
-    // incomplete, so leave o and S_T untouched (the status reports it)
-    if (*reinterpret_cast<volatile int32_t *>(ws_hdr) != 0) return;
+    // This kernel may run as the per-chunk kernel's programmatic dependent:
+    // its CTAs then start while that kernel's last CTAs still run, and wait
+    // for its completion (griddepcontrol.wait) before the first read of what
+    // it wrote -- the images and the status word.  A per-chunk kernel of this
+    // call that gave up on a wait left its images incomplete: o and S_T stay
+    // untouched (the status reports it).
+    auto upstream_failed = [&]() {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        return *reinterpret_cast<volatile int32_t *>(ws_hdr) != 0;
+    };
 
     // A segment launch (one sequence): phase 0 runs, per head, segment 0
     // itself (slices 0-3) and, for each later segment, its state
@@ -151,6 +158,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     }
     const int64_t sbase_g = ((int64_t)n * H + h) * D * D + (int64_t)row * D + slice * DVS;
     if (cb == ce && !p.nseg) {            // empty sequence: pass the state through
+        if (upstream_failed()) return;
         if (p.w0 == 0 && !issuer) {
             for (int j = 0; j < DVS; j += 4) {
                 float4 x = p.S0 ? *reinterpret_cast<const float4 *>(p.S0 + sbase_g + j)
@@ -202,6 +210,12 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     fence_after_sync();
     const uint32_t tmem = warp_uniform(*tmem_slot);
     const uint32_t smb = warp_uniform(smem_addr(sm));
+    if (upstream_failed()) {
+        fence_before_sync();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc<256>(tmem);
+        return;
+    }
 
     auto issue_loads = [&](int ch, int stage) {
         const uint8_t *src = img_base + ((uint64_t)(ch - p.img0) * H + h) * CH_STRIDE;

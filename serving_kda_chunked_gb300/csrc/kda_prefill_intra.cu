@@ -249,6 +249,10 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         }
     }
 #endif
+    // the chain kernel that follows may launch now: its CTAs take SMs as this
+    // kernel's CTAs finish, and wait for this kernel's completion before
+    // reading its results
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (warp == 0) tmem_alloc<512>(tmem_slot);
     fence_before_sync();
     __syncthreads();

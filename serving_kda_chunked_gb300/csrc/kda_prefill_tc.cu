@@ -193,6 +193,24 @@ cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, bo
             p2.plan = plan;
             chain_wide_kernel<<<(unsigned)((int64_t)a.N * a.H), K2W_THREADS, S2W_BYTES, st>>>(p2);
             chain_kernel<<<(unsigned)(2 * nsm), K2_THREADS, S2_BYTES, st>>>(p2);
+        } else if (a.T > 0) {
+            // right behind the per-chunk kernel: launched as its programmatic
+            // dependent, so that its CTAs take the SMs the per-chunk kernel
+            // frees while that kernel's last CTAs still run; they wait for
+            // its completion (griddepcontrol.wait) before reading anything it
+            // wrote
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)slices);
+            cfg.blockDim = dim3(K2_THREADS);
+            cfg.dynamicSmemBytes = S2_BYTES;
+            cfg.stream = st;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = cudaLaunchKernelEx(&cfg, chain_kernel, p2);
+            if (e != cudaSuccess) return e;
         } else {
             chain_kernel<<<(unsigned)slices, K2_THREADS, S2_BYTES, st>>>(p2);
         }
