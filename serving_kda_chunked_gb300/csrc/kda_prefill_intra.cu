@@ -17,6 +17,9 @@ chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int cap,
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry_s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // the per-chunk kernel may launch now (it waits for this kernel's
+    // completion before reading the table)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid == 0) { carry_s = 0; ws_hdr[0] = 0; }
     __syncthreads();
     for (int base = 0; base < N; base += 1024) {
@@ -242,6 +245,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
     // any MMA, so the bounded wait gives up with nothing in flight; the CTA
     // records the timeout and returns.
     if (p.force_timeout) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         __syncthreads();
         if (!__syncthreads_and(mbar_wait(&mbar[0], 0, 64))) {
             if (tid == 0) ws_fail(ws_hdr, 1);
@@ -249,10 +253,6 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         }
     }
 #endif
-    // the chain kernel that follows may launch now: its CTAs take SMs as this
-    // kernel's CTAs finish, and wait for this kernel's completion before
-    // reading its results
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (warp == 0) tmem_alloc<512>(tmem_slot);
     fence_before_sync();
     __syncthreads();
@@ -265,6 +265,14 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         if (ch >= 2 * ((r >> 4) + 1))
             *reinterpret_cast<uint4 *>(sm + S1_TP + sw128_off(r, ch)) = make_uint4(0, 0, 0, 0);
     }
+    // This kernel may run as the chunk table's programmatic dependent: the
+    // setup above overlaps it, and its results (the chunk offsets, the status
+    // word it clears) are read after its completion.  The chain kernel that
+    // follows may then launch: its CTAs take SMs as this kernel's CTAs
+    // finish, and wait for this kernel's completion before reading its
+    // results.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int total = chunk_base[p.N];
     const int c_end = min(p.w1, total);

@@ -162,8 +162,20 @@ cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, bo
         if (a.T > 0) {
             const int64_t tasks = (w1 - w0) * a.H;
             const int g1 = (int)(tasks < nsm ? tasks : nsm);
-            intra_kernel<<<g1, K1_THREADS, S1_BYTES, st>>>(p1);
-            e = cudaGetLastError();
+            // a programmatic dependent of the kernel before it (the chunk
+            // table, or the previous window's chain, which allows no early
+            // launch): its setup overlaps the chunk table
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)g1);
+            cfg.blockDim = dim3(K1_THREADS);
+            cfg.dynamicSmemBytes = S1_BYTES;
+            cfg.stream = st;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = cudaLaunchKernelEx(&cfg, intra_kernel, p1);
             if (e != cudaSuccess) return e;
         }
         if (pl.nseg) {            // chunk-affine scan over this window
