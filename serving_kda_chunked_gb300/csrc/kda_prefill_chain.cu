@@ -279,14 +279,15 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     //   B1 (all):       S (fp16 operand) written, chunk i's operands landed
     //   warp 4:         D_W = W S (8 K steps, M = 64: half the operand reads
     //                   of the M = 128 [W ; Q^] S, and on the critical path)
-    //                   -> MB_R1, then D_O = Q^ S, then the operands of chunk
-    //                   i + 2 into the stage of chunk i - 1 (once chunk i - 1's
-    //                   P U is done)
+    //                   -> MB_R1, then the first QS_ROUND1 K steps of
+    //                   D_O = Q^ S, then the operands of chunk i + 2 into the
+    //                   stage of chunk i - 1 (once chunk i - 1's P U is done)
     //   warps 0-3:      half the O rows of chunk i - 1 (while W S runs), then
     //                   U = U~ - W S (token rows 16 warp + lane, lanes 0-15)
     //   B2 (all):       U written
     //   warp 4:         D_S = Kbar^T U (4 K steps) -> MB_R2S, then
-    //                   D_O += P U (4 K steps, M = 64) -> MB_R2O of the set
+    //                   D_O += P U (4 K steps, M = 64) and the rest of Q^ S
+    //                   -> MB_R2O of the set
     //   warps 0-3:      the other half (while Kbar^T U runs), then
     //                   S = Diag(e^gamma_last) S + D_S   (after MB_R2S)
     // W S of chunk i completes after every MMA of chunk i - 1 (one issuing
@@ -332,7 +333,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
                             sdesc_add(dso, 256 * s), id_m64, s > 0);
                 mma_commit(&mbar[MB_R1]);
 #pragma unroll
-                for (int s = 0; s < 8; ++s)   // Q^ rows sit 8 KB after the W rows of each atom
+                for (int s = 0; s < QS_ROUND1; ++s)   // Q^ rows sit 8 KB after the W rows of each atom
                     mma_f16(d_w + 32, sdesc_add(dwq, 8192 + (s >> 2) * 16384 + (s & 3) * 32),
                             sdesc_add(dso, 256 * s), id_m64, s > 0);
                 // chunk i + 2's operands into the stage of chunk i - 1 (a stage
@@ -393,6 +394,8 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
             const uint64_t dkb = sdesc(stb + S2_KB, 8192, 1024, LAYOUT_SW128);
             const uint64_t dp = sdesc_k_sw128(stb + S2_PZ + 8192);
             const uint64_t duo = sdesc(smb + S2_UOP, 128, 1024, LAYOUT_NONE);
+            const uint64_t dwq = sdesc_k_sw128(stb + S2_WQ);
+            const uint64_t dso = sdesc(smb + S2_SOP, 128, 2048, LAYOUT_NONE);
             if (elect_one()) {
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
@@ -401,6 +404,10 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     mma_f16(d_w + 32, sdesc_add(dp, 32 * s), sdesc_add(duo, 256 * s), id_m64, 1);
+#pragma unroll
+                for (int s = QS_ROUND1; s < 8; ++s)   // the rest of Q^ S
+                    mma_f16(d_w + 32, sdesc_add(dwq, 8192 + (s >> 2) * 16384 + (s & 3) * 32),
+                            sdesc_add(dso, 256 * s), id_m64, 1);
                 mma_commit(&mbar[MB_R2O + set]);
             }
             __syncwarp();

@@ -169,6 +169,12 @@ struct K1Params {
 // ---- chain kernel (one 32-column slice per CTA) ------------------------------
 constexpr int K2_THREADS = 160;       // warps 0-3: the state, warp 4: MMA and load issue
 constexpr int K2_ISSUER = 4;
+// K steps of Q^ S issued in round 1 of a chunk; the other five follow P U in
+// round 2.  The issuing thread's MMAs run in order, so Q^ S steps queued in
+// round 1 delay Kbar^T U, which is on the chain's critical path; behind P U
+// they run while the state updates.
+constexpr int QS_ROUND1 = 3;
+static_assert(QS_ROUND1 >= 1 && QS_ROUND1 <= 8, "P U accumulates onto the round-1 steps of Q^ S");
 constexpr uint32_t S2_WQ = 0;          // [W ; Q^] K-major SW128, 2 atoms x 128 rows
 constexpr uint32_t S2_KB = 32768;      // Kbar [r][c] SW128 (MN-major A)
 constexpr uint32_t S2_PZ = 49152;      // P K-major SW128 at +8192 (64 rows)
