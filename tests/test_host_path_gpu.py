@@ -33,6 +33,9 @@ def _device_call(inp):
     ws = torch.empty(need, dtype=torch.uint8, device=DEV) if need else None
     o, S_T = kda.kda_prefill_chunked(*(inp[n] for n in NAMES), inp["cu_seqlens"], inp["S0"],
                                      workspace=ws)
+    if ws is not None:
+        st = kda.kda_prefill_check(ws)
+        assert st == kda.KDA_OK, kda.status_string(st)
     torch.cuda.synchronize()
     return o, S_T
 

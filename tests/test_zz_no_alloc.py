@@ -53,6 +53,9 @@ def _both(lib, inp):
                                  d, d, kda.KDA_BF16, 64, _p(o_ref), _p(S_ref), _p(ws),
                                  ws_bytes, _stream())
     assert st == kda.KDA_OK, kda.status_string(st)
+    # its device status too
+    st = kda.kda_prefill_check(ws)
+    assert st == kda.KDA_OK, kda.status_string(st)
     o = torch.full_like(v, float("nan"))
     S = torch.full((N, H, d, d), float("nan"), dtype=torch.float32, device=DEV)
     st = lib.kda_prefill_chunked_noalloc(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(cu),
