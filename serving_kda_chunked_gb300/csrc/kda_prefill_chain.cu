@@ -12,10 +12,13 @@ namespace tcp {
 // One CTA of 160 threads per (sequence, head, block of 32 state columns):
 // warps 0-3 hold the fp32 state (thread t = row t, a dk channel), warp 4
 // issues the MMAs and the operand loads.  Per chunk:
-//   round 1: D_A = [W ; Q^] S   (M = 128: rows 0-63 W S, 64-127 Q^ S)
+//   round 1: D_W = W S (M = 64), then part of D_O = Q^ S (M = 64)
 //   U = U~ - W S (fp16);
-//   round 2: D_S = Kbar^T U, then D_A += [0 ; P] U (rows 64-127 then hold O)
+//   round 2: D_S = Kbar^T U, then D_O += P U and the rest of Q^ S (D_O then
+//   holds O)
 //   S = Diag(e^gamma_last) S + D_S.
+// (The wide form below, one CTA per (sequence, head), keeps one M = 128
+// [W ; Q^] S and [0 ; P] U.)
 // TMEM accumulators alternate between two sets so that the outputs of chunk
 // i are read while the MMAs of chunk i + 1 run; operand images arrive with
 // bulk async copies two chunks ahead (three stages).
