@@ -107,6 +107,13 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     int slice = unit % NSLICE;
     int h = (unit / NSLICE) % H;
     int n = unit / (NSLICE * H);
+    // This kernel may run as the per-chunk kernel's programmatic dependent:
+    // its CTAs then start while that kernel's last CTAs still run.  They wait
+    // for its completion here, before the first global read of anything this
+    // call wrote (the chunk table, a previous window's final states, the
+    // images, the status word): the wait orders the writes of the kernels
+    // before it for this grid, and nothing else does.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (p.plan) {   // many sequences: the window plan's order, if it picked this form
         if (p.plan[0] != PLAN_SLICE || unit >= p.plan[1] * H * NSLICE) return;
         n = p.plan[2 + unit / (NSLICE * H)];
@@ -114,16 +121,9 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
     int32_t *ws_hdr = reinterpret_cast<int32_t *>(p.ws);
     const int32_t *chunk_base = reinterpret_cast<const int32_t *>(p.ws + WS_HEADER);
     const uint8_t *img_base = p.ws + ws_images_offset(p.N);
-    // This kernel may run as the per-chunk kernel's programmatic dependent:
-    // its CTAs then start while that kernel's last CTAs still run, and wait
-    // for its completion (griddepcontrol.wait) before the first read of what
-    // it wrote -- the images and the status word.  A per-chunk kernel of this
-    // call that gave up on a wait left its images incomplete: o and S_T stay
-    // untouched (the status reports it).
-    auto upstream_failed = [&]() {
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        return *reinterpret_cast<volatile int32_t *>(ws_hdr) != 0;
-    };
+    // A per-chunk kernel of this call that gave up on a wait left its images
+    // incomplete: o and S_T stay untouched (the status reports it).
+    auto upstream_failed = [&]() { return *reinterpret_cast<volatile int32_t *>(ws_hdr) != 0; };
 
     // A segment launch (one sequence): phase 0 runs, per head, segment 0
     // itself (slices 0-3) and, for each later segment, its state

@@ -209,8 +209,8 @@ cudaError_t run_prefill_tc(const PrefillArgs &a, uint8_t *ws, int64_t window, bo
             // right behind the per-chunk kernel: launched as its programmatic
             // dependent, so that its CTAs take the SMs the per-chunk kernel
             // frees while that kernel's last CTAs still run; they wait for
-            // its completion (griddepcontrol.wait) before reading anything it
-            // wrote
+            // its completion (griddepcontrol.wait) before their first global
+            // read of anything this call wrote
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)slices);
             cfg.blockDim = dim3(K2_THREADS);
