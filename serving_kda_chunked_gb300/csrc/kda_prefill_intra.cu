@@ -460,13 +460,21 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
         // ---- stage I, part 2 (task i) beside stage P (task i + 1) ------------
         if (warp < 8) {
             if (i >= 0) {
-                // task i - 1's W/U MMA done: T' is free, its W and U~ can leave TMEM
-                if (i >= 1 && !mbar_wait(&mbar[2], (uint32_t)((i - 1) & 1))) bad = true;
-                fence_after_sync();
-                if (warp < 6)
+                // task i - 1's W and U~ leave TMEM first (W by warps 0-3, U~ by
+                // warps 4-7, one lane quadrant each), once its W/U MMA has
+                // completed: their stores then run beside the gate scan, the
+                // inverse beside the prep
+                if (i >= 1) {
+                    if (!mbar_wait(&mbar[2], (uint32_t)((i - 1) & 1))) bad = true;
+                    fence_after_sync();
+                    drain_half(img_of(i - 1), warp >= 4);
+                }
+                // T = (I + A)^-1 of task i; its fp16 T' replaces task i - 1's
+                // in the W/U A operand, which that MMA no longer reads
+                if (warp < 6) {
                     invert_unit_lower(As, Ts, sB2 + 64 * (i & 1), sm + S1_TP, tid);
-                // W by warps 0-3, U~ by warps 4-7 (one lane quadrant each)
-                if (i >= 1) drain_half(img_of(i - 1), warp >= 4);
+                    fence_async_smem();
+                }
             }
         } else if (i + 1 < n) {
             const int k = i + 1;
@@ -663,23 +671,21 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
 
         // ---- W/U MMA of task i (warp 6's elected lane; warp 12 meanwhile
         // joins the A/P wait)
-        if (warp == K1_WU) {
+        if (warp == K1_WU && i >= 0) {
             const uint32_t smb = warp_uniform(smem_addr(sm));
             const uint32_t wu_acc = warp_uniform(tmem + W_COL);
             const uint64_t wu_dt = sdesc_k_sw128(smb + S1_TP);
             if (elect_one()) {
-                if (i >= 0) {
-                    // [W | U~] = T' [K e^g | V] (fp16, M = 64, N = 256: the two B
-                    // operands sit side by side as four 64-column MN-major
-                    // atoms, and the accumulators side by side in TMEM)
-                    const uint64_t wu_db = sdesc(smb + ((i & 1) ? S1_KGV1 : S1_KGV0), 8192, 1024,
-                                                 LAYOUT_SW128);
-                    constexpr uint32_t id = idesc(64, 256, FMT_F16, FMT_F16, 0, 1);
+                // [W | U~] = T' [K e^g | V] (fp16, M = 64, N = 256: the two B
+                // operands sit side by side as four 64-column MN-major atoms,
+                // and the accumulators side by side in TMEM)
+                const uint64_t wu_db = sdesc(smb + ((i & 1) ? S1_KGV1 : S1_KGV0), 8192, 1024,
+                                             LAYOUT_SW128);
+                constexpr uint32_t id = idesc(64, 256, FMT_F16, FMT_F16, 0, 1);
 #pragma unroll
-                    for (int s2 = 0; s2 < 4; ++s2)
-                        mma_f16(wu_acc, sdesc_add(wu_dt, 32 * s2), sdesc_add(wu_db, 2048 * s2), id, s2 > 0);
-                    mma_commit(&mbar[2]);
-                }
+                for (int s2 = 0; s2 < 4; ++s2)
+                    mma_f16(wu_acc, sdesc_add(wu_dt, 32 * s2), sdesc_add(wu_db, 2048 * s2), id, s2 > 0);
+                mma_commit(&mbar[2]);
             }
             __syncwarp();
         }
