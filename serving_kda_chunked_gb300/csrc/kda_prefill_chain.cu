@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
         bulk_g2s(dst + S2_WQ + 16384, src + IMG_W + 8192, 8192, mb);
         bulk_g2s(dst + S2_WQ + 24576, src + IMG_Q + 8192, 8192, mb);
         bulk_g2s(dst + S2_KB, src + IMG_KT, 16384, mb);
-        bulk_g2s(dst + S2_PZ + 8192, src + IMG_P, 8192, mb);
+        bulk_g2s(dst + S2_PZ, src + IMG_P, 8192, mb);
         bulk_g2s(dst + S2_U, src + IMG_U + slice * 4096, 4096, mb);
         bulk_g2s(dst + S2_G, src + IMG_G, 512, mb);
     };
@@ -315,7 +315,8 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
             for (int gq = 0; gq < DVS / 8; ++gq) {
                 uint4 v4 = make_uint4(pack_h2(S[8 * gq + 0], S[8 * gq + 1]), pack_h2(S[8 * gq + 2], S[8 * gq + 3]),
                                       pack_h2(S[8 * gq + 4], S[8 * gq + 5]), pack_h2(S[8 * gq + 6], S[8 * gq + 7]));
-                *reinterpret_cast<uint4 *>(sm + S2_SOP + gq * 2048 + (row >> 3) * 128 + (row & 7) * 16) = v4;
+                *reinterpret_cast<uint4 *>(sm + S2_SOP + 8192 * set + gq * 2048 + (row >> 3) * 128 +
+                                           (row & 7) * 16) = v4;
             }
             fence_async_smem();
         }
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
             const uint32_t stb = warp_uniform(smb + (uint32_t)stage * S2_STAGE);
             const uint32_t d_w = warp_uniform(tmem + 128u * (uint32_t)set);
             const uint64_t dwq = sdesc_k_sw128(stb + S2_WQ);
-            const uint64_t dso = sdesc(smb + S2_SOP, 128, 2048, LAYOUT_NONE);
+            const uint64_t dso = sdesc(smb + S2_SOP + 8192u * (uint32_t)set, 128, 2048, LAYOUT_NONE);
             if (elect_one()) {
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
@@ -395,10 +396,10 @@ __global__ void __launch_bounds__(K2_THREADS, 1) chain_kernel(const K2Params p) 
             const uint32_t stb = warp_uniform(smb + (uint32_t)stage * S2_STAGE);
             const uint32_t d_w = warp_uniform(tmem + 128u * (uint32_t)set);
             const uint64_t dkb = sdesc(stb + S2_KB, 8192, 1024, LAYOUT_SW128);
-            const uint64_t dp = sdesc_k_sw128(stb + S2_PZ + 8192);
+            const uint64_t dp = sdesc_k_sw128(stb + S2_PZ);
             const uint64_t duo = sdesc(smb + S2_UOP, 128, 1024, LAYOUT_NONE);
             const uint64_t dwq = sdesc_k_sw128(stb + S2_WQ);
-            const uint64_t dso = sdesc(smb + S2_SOP, 128, 2048, LAYOUT_NONE);
+            const uint64_t dso = sdesc(smb + S2_SOP + 8192u * (uint32_t)set, 128, 2048, LAYOUT_NONE);
             if (elect_one()) {
 #pragma unroll
                 for (int s = 0; s < 4; ++s)

@@ -177,15 +177,22 @@ constexpr int QS_ROUND1 = 3;
 static_assert(QS_ROUND1 >= 1 && QS_ROUND1 <= 8, "P U accumulates onto the round-1 steps of Q^ S");
 constexpr uint32_t S2_WQ = 0;          // [W ; Q^] K-major SW128, 2 atoms x 128 rows
 constexpr uint32_t S2_KB = 32768;      // Kbar [r][c] SW128 (MN-major A)
-constexpr uint32_t S2_PZ = 49152;      // P K-major SW128 at +8192 (64 rows)
-constexpr uint32_t S2_U = 65536;       // U~ slice [64][32] fp16
-constexpr uint32_t S2_G = 69632;       // e^gamma_last [128] fp32
-constexpr uint32_t S2_STAGE = 70656;   // bytes per stage (multiple of 1024)
+constexpr uint32_t S2_PZ = 49152;      // P K-major SW128 (64 rows)
+constexpr uint32_t S2_U = 57344;       // U~ slice [64][32] fp16
+constexpr uint32_t S2_G = 61440;       // e^gamma_last [128] fp32
+constexpr uint32_t S2_STAGE = 62464;   // bytes per stage (multiple of 1024)
 constexpr int S2_NSTAGE = 3;           // chunks in flight: loads run two chunks ahead
-constexpr uint32_t S2_SOP = S2_NSTAGE * S2_STAGE;         // S fp16, K=128 x N=32, MN-major
-constexpr uint32_t S2_UOP = S2_SOP + 8192;                // U fp16, K=64 x N=32, MN-major
+// S fp16 (K=128 x N=32, MN-major), one buffer per chunk parity: Q^ S steps
+// issued after Kbar^T U's commit still read chunk i's S while the state warps
+// write chunk i + 1's; the next writer of a buffer (chunk i + 2) waits for
+// W S of chunk i + 1, whose commit covers them
+constexpr uint32_t S2_SOP = S2_NSTAGE * S2_STAGE;
+constexpr uint32_t S2_UOP = S2_SOP + 2 * 8192;            // U fp16, K=64 x N=32, MN-major
 constexpr uint32_t S2_MISC = S2_UOP + 4096;
 constexpr uint32_t S2_BYTES = S2_MISC + 256 + 1024;
+static_assert(S2_PZ + 8192 <= S2_U && S2_U + 4096 <= S2_G && S2_G + 512 <= S2_STAGE &&
+              S2_STAGE % 1024 == 0 && S2_PZ % 1024 == 0 && S2_BYTES <= 232448,
+              "slice chain shared-memory layout");
 constexpr uint32_t S2_TX = 4 * 8192 + 16384 + 8192 + 4096 + 512;   // bytes landing per stage
 // TMEM set s (0, 1) at column 128 s: D_W +0 (W S, M = 64), D_O +32 (Q^ S,
 // then += P U, M = 64), D_S +64 (Kbar^T U)
