@@ -157,14 +157,21 @@ def test_prefill_single_sequence_workload():
     assert_close("S_T", S_T, S_ref, 2e-3)
 
 
-@pytest.mark.parametrize("variant", ["kda", "gdn"])
-def test_prefill_repeated_calls_are_bit_identical(variant):
+@pytest.mark.parametrize("variant,reps", [("kda", 60), ("gdn", 60), ("varlen", 12), ("scan", 30)])
+def test_prefill_repeated_calls_are_bit_identical(variant, reps):
     """The same call, repeated, gives the same bits: the kernels have no
     reduction whose order depends on timing, so any difference is a race
     (a buffer reused before its last reader finished).  Other work of
-    varying length is queued between calls to shift the timing."""
-    inp = ki.prefill_inputs("single", device=DEV, seed=0 if variant == "kda" else 14)
+    varying length is queued between calls to shift the timing.  The
+    variants cover the slice chain (KDA, GDN), the wide chain form (varlen)
+    and the chunk-affine scan (one sequence, H = 2)."""
     fn = prefill
+    if variant == "varlen":
+        inp = ki.prefill_inputs("varlen", device=DEV)
+    elif variant == "scan":
+        inp = ki.prefill_inputs(ki.prefill_config("single", H=2, T=131072), device=DEV)
+    else:
+        inp = ki.prefill_inputs("single", device=DEV, seed=0 if variant == "kda" else 14)
     if variant == "gdn":
         inp = dict(inp)
         inp["g"] = inp["g"][..., 0].contiguous()
@@ -174,7 +181,7 @@ def test_prefill_repeated_calls_are_bit_identical(variant):
     torch.cuda.synchronize()
     o0, S0 = o0.clone(), S0.clone()
     bad = []
-    for r in range(60):
+    for r in range(reps):
         if r % 3 == 1:
             torch.cuda._sleep(20000 * (r % 7))
         o, S_T = fn(*args)
