@@ -78,12 +78,12 @@ chunk_table_kernel(const int32_t *__restrict__ cu, int N, int64_t T, int cap,
 //      register-tiled block forward substitution), written as the fp16 image
 //      of T' = T Diag(beta).
 //   6. W = T' (K e^g), U~ = T' V on tcgen05 (fp16), moved from TMEM to the
-//      workspace during the next task's inverse.
-// Steps 2-4 of task k + 1 run on warps 8-15 while warps 0-5 run the inverse
-// of task k and warps 0-7 move task k - 1's W and U~ out.  Warp 12 issues the
-// A/P MMAs, warp 13 the staging loads and warp 6 the W/U MMAs, each from one
-// elected lane.  The inverse then hides the prep's latency instead of adding
-// to it.
+//      workspace before the next task's inverse.
+// Steps 2-4 of task k + 1 run on warps 8-15 while warps 0-7 first move task
+// k - 1's W and U~ out and warps 0-5 then run the inverse of task k.  Warp
+// 12 issues the A/P MMAs, warp 13 the staging loads and warp 6 the W/U MMAs,
+// each from one elected lane.  The inverse then hides the prep's latency
+// instead of adding to it.
 __device__ __forceinline__ void tma_load_3d(uint8_t *dst, const CUtensorMap *map, int c0, int c1,
                                             int c2, uint64_t *mbar) {
     asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
@@ -367,9 +367,9 @@ __global__ void __launch_bounds__(K1_THREADS, 1) intra_kernel(const __grid_const
 
     // Task k passes through: stage P (iteration k - 1: gate scan and prep by
     // warps 8-15, then the A/P MMA), stage I (iteration k: A/P readout by all
-    // warps, then the inverse by warps 0-5 while warps 8-15 run stage P of
-    // task k + 1; then the W/U MMA), and its W and U~ leave TMEM in iteration
-    // k + 1.  Positions: p0 = task i, pA = i + 1, pB = i + 2, rC = i + 3.
+    // warps, then task k - 1's W/U drain and the inverse by warps 0-7 / 0-5
+    // while warps 8-15 run stage P of task k + 1; then the W/U MMA), and its
+    // W and U~ leave TMEM at the start of iteration k + 1's stage I part 2.  Positions: p0 = task i, pA = i + 1, pB = i + 2, rC = i + 3.
     Pos p0{0, 0, 0}, pA = pos_finish(pos_fetch(0)), pB = pos_finish(pos_fetch(1));
     PosRaw rC = pos_fetch(2);
     float b_reg, gs_reg;
